@@ -1,0 +1,435 @@
+"""Benchmark of the block-FP8 projection hot path on GB300.
+
+One step = one pass of the dense-FFN W8A8 prefill chain, the workload the
+pages measure their prefill on (949 tokens of BF16 activations, hidden 5120,
+intermediate 17408):
+    bfp8_act_quant_group(x)              [949, 5120]  -> E4M3 + 1x128 scales
+    bfp8_linear_w8a8(gate/up)            [34816, 5120] as two member-local grids
+    bfp8_silu_mul_act_quant              [949, 34816] -> E4M3 [949, 17408]
+    bfp8_linear_w8a8(down)               [5120, 17408]
+The headline value is prefill TFLOP/s over the chain: 2*M*(N1*K1 + N2*K2)
+algorithmic FLOPs (true M, no padding) per step. The decode half of the
+metric (weight GB/s of the M <= 16 GEMV on the same weights) is reported in
+the "decode" object of the same line.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun each rank runs its own replica (replicas only: nothing is
+exchanged on the data path); the value is the aggregate over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "block-FP8 linear TFLOP/s (prefill), weight GB/s (decode); % of GB300 roofline"
+M_TOK, HID, INTER = 949, 5120, 17408
+FLOPS_STEP = 2 * M_TOK * (2 * INTER * HID + HID * INTER)
+FLOPS_GATE_UP = 2 * M_TOK * (2 * INTER) * HID
+WORKLOAD = ("dense-FFN prefill chain, W8A8 block-FP8: M=949 BF16 tokens (N(0,1), 0.5% x30 "
+            "outlier channels) -> 1x128 act quant -> gate/up [34816,5120] (two member grids "
+            "[136,40]) -> SiLU(gate)*up + 1x128 quant -> down [5120,17408] grid [40,136]; "
+            "weights N(0,0.02^2) with 128x128 BF16 scales")
+
+
+def _peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return {"hbm_gbs": d["hbm_gbs"], "bf16": d["bf16_tflops"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "source": "fallback"}
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _init_dist(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        if not dist.is_initialized():
+            dist.init_process_group("gloo")
+        return dist
+    return None
+
+
+def reduce_max(value: float, dist_mod) -> float:
+    """Max over ranks (host-side gloo reduction); identity on one process."""
+    if dist_mod is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist_mod) -> None:
+    if dist_mod is not None:
+        dist_mod.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = ROOT / "gpurun_out" / f"clocks_bench_{os.getpid()}.csv"
+
+    def start(self):
+        try:
+            self.path.parent.mkdir(exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = [r.split(",") for r in self.path.read_text().splitlines() if r.strip()]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local):
+    import torch
+
+    from block_scaled_fp8_token_gb300 import bfp8, synth
+
+    dist_mod = _init_dist(world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = _peaks()
+
+    d = synth.dense_ffn(0)
+    x_host = d["x"].pin_memory()
+    x = d["x"].to(dev)
+
+    def quantize(w):
+        N, K = w.shape
+        wd = w.to(dev)
+        q = torch.empty(N, K, dtype=torch.uint8, device=dev)
+        s = torch.empty((N + 127) // 128, (K + 127) // 128, dtype=torch.bfloat16, device=dev)
+        bfp8.bfp8_quantize_weight_block(wd, q, s)
+        del wd
+        return q, s
+
+    wgu, sgu = quantize(d["w_gate_up"])
+    wdn, sdn = quantize(d["w_down"])
+    del d
+    torch.cuda.synchronize()
+
+    qa = torch.empty(M_TOK, HID, dtype=torch.uint8, device=dev)
+    sa = torch.empty(M_TOK, HID // 128, dtype=torch.float32, device=dev)
+    gu = torch.empty(M_TOK, 2 * INTER, dtype=torch.bfloat16, device=dev)
+    qh = torch.empty(M_TOK, INTER, dtype=torch.uint8, device=dev)
+    sh = torch.empty(M_TOK, INTER // 128, dtype=torch.float32, device=dev)
+    y = torch.empty(M_TOK, HID, dtype=torch.bfloat16, device=dev)
+    y_host = torch.empty(M_TOK, HID, dtype=torch.bfloat16).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+    members = [INTER, INTER]
+    gu_events = []
+
+    def step(xin, record=False):
+        bfp8.bfp8_act_quant_group(xin, qa, sa, stream=stream)
+        if record:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        bfp8.bfp8_linear_w8a8(qa, sa, wgu, sgu, gu, member_rows=members, stream=stream)
+        if record:
+            e1.record(stream)
+            gu_events.append((e0, e1))
+        bfp8.bfp8_silu_mul_act_quant(gu, qh, sh, stream=stream)
+        bfp8.bfp8_linear_w8a8(qh, sh, wdn, sdn, y, stream=stream)
+
+    launches_per_step = 4
+    for _ in range(args.warmup):
+        step(x)
+    torch.cuda.synchronize()
+    if bfp8.bfp8_device_status() != 0:
+        raise RuntimeError("device status not OK after warm-up")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(dist_mod)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(x, record=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist_mod)
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    ms_max = reduce_max(ms, dist_mod)
+    gu_ms = statistics.mean(a.elapsed_time(b) for a, b in gu_events)
+    gu_events.clear()
+
+    # end to end through the public API: pinned host x -> device, chain, y -> pinned host
+    e2e_steps = max(3, min(args.steps, 50))
+    barrier(dist_mod)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(e2e_steps):
+        x.copy_(x_host, non_blocking=True)
+        step(x)
+        y_host.copy_(y, non_blocking=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(t0.elapsed_time(t1) / e2e_steps, dist_mod)
+
+    decode = run_decode(bfp8, torch, dev, wgu, sgu, wdn, sdn, peaks)
+    status = bfp8.bfp8_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {bfp8.bfp8_status_string(status)}")
+
+    if rank != 0:
+        return None
+    tflops = FLOPS_STEP * world / (ms_max * 1e-3) / 1e12
+    achieved = FLOPS_GATE_UP / (gu_ms * 1e-3) / 1e12
+    fp8_peak = 2.0 * peaks["bf16"]
+    out = {
+        "metric": METRIC,
+        "value": round(tflops, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3",
+        "data": "synthetic",
+        "config": {
+            "workload": WORKLOAD,
+            "M": M_TOK, "hidden": HID, "intermediate": INTER,
+            "flops_per_step": FLOPS_STEP,
+            "l2": "inputs larger than L2: 267 MB of E4M3 weights streamed per step",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": "tensor",
+            "kernel": "gemm_kernel<256,4,W8A8> (gate/up [34816,5120], M=949)",
+            "achieved": round(achieved, 1),
+            "peak": round(fp8_peak, 1),
+            "unit": "TFLOP/s",
+            "frac": round(achieved / fp8_peak, 4),
+            "traffic": None,
+            "peak_source": f"{peaks['source']} bf16 burst {peaks['bf16']} x 2 (FP8:BF16 nominal ratio 4.5:2.25)",
+            "launch_ms": round(gu_ms, 4),
+        },
+        "e2e": {
+            "value": round(FLOPS_STEP * world / (e2e_ms * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s",
+            "h2d_bytes_per_step": M_TOK * HID * 2,
+            "d2h_bytes_per_step": M_TOK * HID * 2,
+            "ms_per_step": round(e2e_ms, 4),
+        },
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "decode": decode,
+    }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.cpu_rows)
+    return out
+
+
+def run_decode(bfp8, torch, dev, wgu, sgu, wdn, sdn, peaks):
+    """Decode GEMV (M in {1, 4, 16}) on the same weights: weight GB/s, L2
+    flushed between timed launches."""
+    from block_scaled_fp8_token_gb300 import synth
+
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    res = {"metric": "weight GB/s (decode GEMV, W8A16 arithmetic)", "unit": "GB/s",
+           "l2": "flushed (512 MB write) before every timed launch", "shapes": {}}
+    stream = torch.cuda.current_stream(dev)
+    best = None
+    for M in (1, 4, 16):
+        row = {}
+        for name, w, s, members in (("gate_up", wgu, sgu, [INTER, INTER]), ("down", wdn, sdn, None)):
+            N, K = w.shape
+            x = synth.decode_tokens(100 + M, M, K).to(dev)
+            y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            ws = torch.empty(bfp8.bfp8_gemv_decode_workspace(M, N, K), dtype=torch.uint8, device=dev)
+            for _ in range(3):
+                bfp8.bfp8_gemv_decode(x, w, s, y, ws, member_rows=members, stream=stream)
+            times = []
+            for _ in range(20):
+                flush.zero_()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                bfp8.bfp8_gemv_decode(x, w, s, y, ws, member_rows=members, stream=stream)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+            us = statistics.median(times) * 1e3
+            nbytes = N * K + s.numel() * 2 + M * K * 2 + M * N * 2
+            gbs = nbytes / (us * 1e-6) / 1e9
+            row[name] = {"us": round(us, 2), "bytes": nbytes, "GB/s": round(gbs, 1),
+                         "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+            if name == "gate_up" and M == 16:
+                best = row[name]
+        res["shapes"][f"M={M}"] = row
+    res["roofline"] = {"bound": "hbm", "kernel": "gemv_kernel (gate/up [34816,5120], M=16)",
+                       "achieved": best["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                       "frac": best["frac_hbm"], "traffic": None,
+                       "peak_source": f"{peaks['source']} copy bandwidth"}
+    del flush
+    return res
+
+
+# --------------------------------------------------------------------------- oracle arm
+_ORACLE_INPUTS = None
+
+
+def _oracle_inputs():
+    """Oracle-quantized weights and the BF16 tokens of the chain (prepared once,
+    outside every timed region)."""
+    global _ORACLE_INPUTS
+    if _ORACLE_INPUTS is None:
+        import numpy as np
+        import torch
+
+        from block_scaled_fp8_token_gb300 import synth
+        from oracle import quant as Q
+
+        d = synth.dense_ffn(0)
+        qgu, sgu = Q.quantize_weight_blocks(d["w_gate_up"].numpy())
+        qd, sd = Q.quantize_weight_blocks(d["w_down"].numpy())
+        xb = d["x"].contiguous().view(torch.int16).numpy().view(np.uint16)
+        _ORACLE_INPUTS = (qgu, sgu, qd, sd, xb)
+    return _ORACLE_INPUTS
+
+
+def _oracle_chain_sample(rows: int):
+    """The CPU oracle, as it stands, on `rows` tokens of the same chain.
+    Returns (seconds, algorithmic flops of those rows)."""
+    from oracle import formats as F
+    from oracle import linear as L
+    from oracle import quant as Q
+
+    qgu, sgu, qd, sd, xb = _oracle_inputs()
+    t0 = time.perf_counter()
+    qa, sa = Q.act_quant_group(xb[:rows])
+    gu = L.linear_w8a8(qa, sa, qgu, sgu, [INTER, INTER])
+    qh, sh = Q.silu_mul_act_quant(F.f64_to_bf16_bits(gu))
+    L.linear_w8a8(qh, sh, qd, sd)
+    dt = time.perf_counter() - t0
+    return dt, 2 * rows * (2 * INTER * HID + HID * INTER)
+
+
+def _cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(rows: int) -> dict:
+    dt, flops = _oracle_chain_sample(rows)
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": _cores(),
+            "kind": "oracle",
+            "sample": f"{rows} of the 949 tokens through the whole chain (numpy float64; "
+                      f"BLAS threads = host cores), {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    per_step = []
+    _oracle_inputs()
+    # the oracle takes seconds per step: run at most 3 so the arm ends in minutes
+    steps = max(1, min(args.steps, 3))
+    for _ in range(steps):
+        dt, flops = _oracle_chain_sample(args.cpu_rows)
+        per_step.append(dt)
+    ms = statistics.mean(per_step) * 1e3
+    value = flops / (ms * 1e-3) / 1e12
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": steps, "warmup": 0, "ms_per_step": round(ms, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M_TOK, "hidden": HID, "intermediate": INTER,
+                   "sample_rows": args.cpu_rows, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": _cores(),
+                         "kind": "oracle",
+                         "sample": f"{args.cpu_rows} of the 949 tokens per step through the whole chain"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-rows", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = _dist()
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_ours(args, rank, world, local)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,246 @@
+"""Python binding of libbfp8: the C ABI of include/bfp8.h, name for name.
+
+Argument marshalling only. Every function takes torch tensors (device memory
+and shapes come from them), passes raw pointers, sizes and the current CUDA
+stream to the library, and raises Bfp8Error on a non-zero status. Nothing
+here computes. If libbfp8.so is missing, importing this module raises.
+Nothing falls back to another implementation.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from pathlib import Path
+
+import torch
+
+_LIB_PATH = Path(__file__).resolve().parent / "libbfp8.so"
+
+if not _LIB_PATH.exists():
+    raise ImportError(
+        f"{_LIB_PATH} is missing: build it with "
+        "`python -m block_scaled_fp8_token_gb300.build` (needs nvcc). "
+        "There is no fallback implementation.")
+
+_lib = ctypes.CDLL(os.fspath(_LIB_PATH))
+
+# ---- enums (include/bfp8.h) ------------------------------------------------
+BFP8_OK = 0
+STATUS_NAMES = {
+    0: "OK", 1: "INVALID_ARG", 2: "E5M2", 3: "NO_SCALE", 4: "ROW_SCALE",
+    5: "AMBIGUOUS_SCALE", 6: "GRID_TRANSPOSED", 7: "GRID_SHAPE", 8: "SCALE_DTYPE",
+    9: "BLOCK_SIZE", 10: "QUANT_METHOD", 11: "GROUP", 12: "NOT_FP8",
+    13: "UNSUPPORTED", 14: "CUDA", 15: "TIMEOUT",
+}
+BFP8_DT_NONE, BFP8_DT_E4M3, BFP8_DT_E5M2, BFP8_DT_BF16, BFP8_DT_F16, BFP8_DT_F32 = range(6)
+BFP8_MAX_MEMBERS = 8
+
+
+class Bfp8Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {bfp8_status_string(status)} ({status})")
+
+
+class bfp8_weight_desc(ctypes.Structure):
+    _fields_ = [
+        ("weight_dtype", ctypes.c_int32),
+        ("weight_rank", ctypes.c_int32),
+        ("weight_shape", ctypes.c_int64 * 2),
+        ("scale_dtype", ctypes.c_int32),
+        ("scale_rank", ctypes.c_int32),
+        ("scale_shape", ctypes.c_int64 * 2),
+        ("has_row_scale", ctypes.c_int32),
+        ("declared_quant_fp8", ctypes.c_int32),
+        ("declared_block", ctypes.c_int32 * 2),
+        ("n_members", ctypes.c_int32),
+        ("member_rows", ctypes.POINTER(ctypes.c_int64)),
+    ]
+
+
+class bfp8_members(ctypes.Structure):
+    _fields_ = [("n_members", ctypes.c_int32), ("member_rows", ctypes.POINTER(ctypes.c_int64))]
+
+
+_vp, _i64, _i32, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+_SIGS = {
+    "bfp8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "bfp8_validate_grid": (ctypes.c_int, [ctypes.POINTER(bfp8_weight_desc), ctypes.c_char_p, _sz]),
+    "bfp8_act_quant_group": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _vp]),
+    "bfp8_silu_mul_act_quant": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _vp]),
+    "bfp8_quantize_weight_block": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i32, _vp]),
+    "bfp8_linear_w8a8": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i32, _i64, _i64, _i64,
+                                        _vp, _i64, ctypes.POINTER(bfp8_members), _vp]),
+    "bfp8_linear_w8a16": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _i64,
+                                         ctypes.POINTER(bfp8_members), _vp]),
+    "bfp8_gemv_decode": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _i64,
+                                        ctypes.POINTER(bfp8_members), _vp, _sz, _vp]),
+    "bfp8_gemv_decode_workspace": (_sz, [_i64, _i64, _i64]),
+    "bfp8_grouped_linear": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i32, _vp, _i32, _i64,
+                                           _i64, _i64, _vp, _i64, _vp]),
+    "bfp8_device_status": (ctypes.c_int, [_vp]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+def library_path() -> Path:
+    return _LIB_PATH
+
+
+def bfp8_status_string(status: int) -> str:
+    return _lib.bfp8_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != BFP8_OK:
+        raise Bfp8Error(status, where)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _scale_dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BFP8_DT_BF16
+    if t.dtype == torch.float32:
+        return BFP8_DT_F32
+    if t.dtype == torch.float16:
+        return BFP8_DT_F16
+    return BFP8_DT_NONE
+
+
+def _members(member_rows):
+    if member_rows is None:
+        return None, None
+    arr = (ctypes.c_int64 * len(member_rows))(*[int(v) for v in member_rows])
+    m = bfp8_members(len(member_rows), arr)
+    return ctypes.byref(m), (m, arr)
+
+
+def bfp8_validate_grid(desc: bfp8_weight_desc, msg_len: int = 256) -> tuple[int, str]:
+    """Returns (status, message). Host only: needs no GPU."""
+    buf = ctypes.create_string_buffer(msg_len)
+    rc = _lib.bfp8_validate_grid(ctypes.byref(desc), buf, msg_len)
+    return rc, buf.value.decode()
+
+
+def make_weight_desc(weight_dtype: int, weight_shape, scale_dtype: int = BFP8_DT_NONE,
+                     scale_shape=None, has_row_scale: bool = False,
+                     declared_quant_fp8: bool = True, declared_block=(128, 128),
+                     member_rows=None):
+    """Builds a bfp8_weight_desc; returns (desc, keepalive)."""
+    d = bfp8_weight_desc()
+    d.weight_dtype = weight_dtype
+    d.weight_rank = len(weight_shape)
+    for i, v in enumerate(list(weight_shape)[:2]):
+        d.weight_shape[i] = int(v)
+    d.scale_dtype = scale_dtype
+    sshape = list(scale_shape) if scale_shape is not None else []
+    d.scale_rank = len(sshape)
+    for i, v in enumerate(sshape[:2]):
+        d.scale_shape[i] = int(v)
+    d.has_row_scale = int(bool(has_row_scale))
+    d.declared_quant_fp8 = int(bool(declared_quant_fp8))
+    d.declared_block[0], d.declared_block[1] = int(declared_block[0]), int(declared_block[1])
+    keep = None
+    if member_rows is not None:
+        keep = (ctypes.c_int64 * len(member_rows))(*[int(v) for v in member_rows])
+        d.n_members = len(member_rows)
+        d.member_rows = keep
+    return d, keep
+
+
+def bfp8_act_quant_group(x, q, scales, s_stride_m=None, s_stride_kb=None, stream=None) -> None:
+    M, K = x.shape
+    ssm = scales.stride(0) if s_stride_m is None else s_stride_m
+    sskb = scales.stride(1) if s_stride_kb is None else s_stride_kb
+    _check(_lib.bfp8_act_quant_group(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0),
+                                     _ptr(scales), ssm, sskb, _stream(stream)),
+           "bfp8_act_quant_group")
+
+
+def bfp8_silu_mul_act_quant(gu, q, scales, s_stride_m=None, s_stride_kb=None, stream=None) -> None:
+    M, two_i = gu.shape
+    ssm = scales.stride(0) if s_stride_m is None else s_stride_m
+    sskb = scales.stride(1) if s_stride_kb is None else s_stride_kb
+    _check(_lib.bfp8_silu_mul_act_quant(_ptr(gu), M, two_i // 2, gu.stride(0), _ptr(q),
+                                        q.stride(0), _ptr(scales), ssm, sskb, _stream(stream)),
+           "bfp8_silu_mul_act_quant")
+
+
+def bfp8_quantize_weight_block(w, q, scale, stream=None) -> None:
+    N, K = w.shape
+    _check(_lib.bfp8_quantize_weight_block(_ptr(w), N, K, w.stride(0), _ptr(q), q.stride(0),
+                                           _ptr(scale), _scale_dtype(scale), _stream(stream)),
+           "bfp8_quantize_weight_block")
+
+
+def bfp8_linear_w8a8(q_a, s_a, w, w_scale, y, member_rows=None, s_stride_m=None,
+                     s_stride_kb=None, stream=None) -> None:
+    M, K = q_a.shape
+    N = w.shape[0]
+    ssm = s_a.stride(0) if s_stride_m is None else s_stride_m
+    sskb = s_a.stride(1) if s_stride_kb is None else s_stride_kb
+    mref, _keep = _members(member_rows)
+    _check(_lib.bfp8_linear_w8a8(_ptr(q_a), _ptr(s_a), ssm, sskb, _ptr(w), _ptr(w_scale),
+                                 _scale_dtype(w_scale), M, N, K, _ptr(y), y.stride(0), mref,
+                                 _stream(stream)),
+           "bfp8_linear_w8a8")
+
+
+def bfp8_linear_w8a16(x, w, w_scale, y, member_rows=None, stream=None) -> None:
+    M, K = x.shape
+    N = w.shape[0]
+    mref, _keep = _members(member_rows)
+    _check(_lib.bfp8_linear_w8a16(_ptr(x), x.stride(0), _ptr(w), _ptr(w_scale),
+                                  _scale_dtype(w_scale), M, N, K, _ptr(y), y.stride(0), mref,
+                                  _stream(stream)),
+           "bfp8_linear_w8a16")
+
+
+def bfp8_gemv_decode_workspace(M: int, N: int, K: int) -> int:
+    return int(_lib.bfp8_gemv_decode_workspace(M, N, K))
+
+
+def bfp8_gemv_decode(x, w, w_scale, y, workspace, member_rows=None, stream=None) -> None:
+    M, K = x.shape
+    N = w.shape[0]
+    mref, _keep = _members(member_rows)
+    _check(_lib.bfp8_gemv_decode(_ptr(x), x.stride(0), _ptr(w), _ptr(w_scale),
+                                 _scale_dtype(w_scale), M, N, K, _ptr(y), y.stride(0), mref,
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream(stream)),
+           "bfp8_gemv_decode")
+
+
+def bfp8_grouped_linear(q_a, s_a, w, w_scale, offsets, y, s_stride_m=None, s_stride_kb=None,
+                        stream=None) -> None:
+    T, K = q_a.shape
+    G, N = w.shape[0], w.shape[1]
+    ssm = s_a.stride(0) if s_stride_m is None else s_stride_m
+    sskb = s_a.stride(1) if s_stride_kb is None else s_stride_kb
+    _check(_lib.bfp8_grouped_linear(_ptr(q_a), _ptr(s_a), ssm, sskb, _ptr(w), _ptr(w_scale),
+                                    _scale_dtype(w_scale), _ptr(offsets), G, T, N, K, _ptr(y),
+                                    y.stride(0), _stream(stream)),
+           "bfp8_grouped_linear")
+
+
+def bfp8_device_status(stream=None) -> int:
+    return int(_lib.bfp8_device_status(_stream(stream)))

@@ -1,0 +1,70 @@
+// bfp8_internal.h -- host-side glue shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/bfp8.h"
+
+namespace bfp8 {
+
+// Multiprocessor count of the current device (cached per device).
+int sm_count(int* out);
+// Map the last launch error (if any) to a status.
+int check_launch();
+// Make `kernel` accept `bytes` of dynamic shared memory on the current device.
+int set_max_dynamic_smem(const void* kernel, int bytes);
+
+// Tiled tensor maps (TMA descriptors). dims/strides innermost first; strides
+// are in bytes for dimensions 1.. (dimension 0 is contiguous).
+int make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t dim0,
+                 uint64_t dim1, uint64_t stride1_bytes, uint32_t box0, uint32_t box1,
+                 CUtensorMapSwizzle swizzle);
+int make_tmap_3d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t dim0,
+                 uint64_t dim1, uint64_t dim2, uint64_t stride1_bytes, uint64_t stride2_bytes,
+                 uint32_t box0, uint32_t box1, uint32_t box2, CUtensorMapSwizzle swizzle);
+
+// Member table resolved on the host: member i covers output rows
+// [n0[i], n0[i] + rows[i]) and its scale rows start at sbase[i].
+struct MemberTable {
+  int32_t count;
+  int64_t n0[BFP8_MAX_MEMBERS];
+  int64_t rows[BFP8_MAX_MEMBERS];
+  int64_t sbase[BFP8_MAX_MEMBERS];
+  int64_t scale_rows;  // sum_i ceil(rows_i / 128)
+};
+int resolve_members(int64_t N, const bfp8_members* members, MemberTable* out);
+
+// Launchers (argument checks beyond the common ones happen inside).
+int launch_act_quant(const void* x, int64_t M, int64_t K, int64_t ldx, void* q, int64_t ldq,
+                     float* s, int64_t ssm, int64_t sskb, void* stream);
+int launch_silu_mul_act_quant(const void* gu, int64_t M, int64_t I, int64_t ld, void* q,
+                              int64_t ldq, float* s, int64_t ssm, int64_t sskb, void* stream);
+int launch_weight_quant(const float* w, int64_t N, int64_t K, int64_t ldw, void* q, int64_t ldq,
+                        void* scale, int32_t scale_dtype, void* stream);
+
+int launch_gemm_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
+                     const void* w, const void* w_scale, int32_t w_scale_dtype, int64_t M,
+                     int64_t N, int64_t K, void* y, int64_t ldy, const MemberTable& mt,
+                     void* stream);
+int launch_gemm_w8a16(const void* x, int64_t ldx, const void* w, const void* w_scale,
+                      int32_t w_scale_dtype, int64_t M, int64_t N, int64_t K, void* y,
+                      int64_t ldy, const MemberTable& mt, void* stream);
+int launch_grouped_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
+                        const void* w, const void* w_scale, int32_t w_scale_dtype,
+                        const int32_t* offsets, int32_t G, int64_t total_M, int64_t N,
+                        int64_t K, void* y, int64_t ldy, void* stream);
+
+size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K, int sms);
+int launch_gemv(const void* x, int64_t ldx, const void* w, const void* w_scale,
+                int32_t w_scale_dtype, int64_t M, int64_t N, int64_t K, void* y, int64_t ldy,
+                const MemberTable& mt, void* workspace, size_t ws_bytes, void* stream);
+
+// Device error words, one per translation unit with bounded waits: read and
+// clear. Return BFP8_OK, BFP8_ERR_TIMEOUT or BFP8_ERR_CUDA.
+int gemm_read_clear_error();
+int gemv_read_clear_error();
+
+}  // namespace bfp8

@@ -1,0 +1,622 @@
+// gemm_sm103.cu -- block-scaled FP8 projections on the sm_103a tensor cores.
+//
+// One persistent, warp-specialised kernel template serves three entry points:
+//   W8A8    y = sum_kb (s_a[m,kb] * s_w[r(n),kb]) * (qa_kb . qw_kb^T)
+//           [Module w8a8_prefill, arithmetic paragraph: per-token 1x128
+//            activation scales times 128x128 weight scales in an FP32
+//            epilogue per K-block]
+//   W8A16   y = sum_kb s_w[r(n),kb] * (x_kb . e4m3(qw_kb)^T), with the E4M3
+//           weight tile decoded to BF16 in shared memory just before a BF16
+//           MMA [FP8 Native Serving, "Native FP8 vs dequant-to-BF16"]
+//   grouped the W8A8 arithmetic per expert over an expert-sorted token table
+//           [Module w8a8_prefill, "WHY": MoE expert projections on W8A8]
+//
+// Roles per CTA (one CTA per SM, persistent over output tiles of 128 x BN):
+//   warp 0      TMA producer: one elected lane streams the A and B K-block
+//               tiles (128 deep, 128-byte swizzle) into a STAGES-deep ring.
+//   warp 1      allocates TMEM. One lane issues the tcgen05.mma of each
+//               K-block into a fresh TMEM partial (two partial buffers, so
+//               the tensor cores run one K-block ahead of the promotion).
+//   warps 2-9   promotion + epilogue: tcgen05.ld the partial, acc += P * f in
+//               FP32 registers (f = s_a * s_w), then BF16 stores of the tile.
+//               Warp w reads TMEM lanes 32*(w%4)..+31 (the rows it owns) and
+//               half (w-2)/4 of the tile's columns.
+//   warps 10-13 (W8A16 only) decode the raw E4M3 tile to BF16 in the
+//               canonical 128-byte-swizzled K-major layout the MMA reads.
+//
+// The 128x128 scale blocks are not powers of two, so they cannot be folded
+// into the hardware's block-scaled MMA kinds (those take UE8M0 scales per 32
+// elements). The promotion therefore runs as an FP32 epilogue per K-block, on
+// TMEM partials.
+//
+// Every mbarrier wait is bounded. On a timeout the kernel raises a CTA-wide
+// abort flag and the device error word, drains its in-flight copies and MMAs,
+// frees TMEM and returns.
+#include "bfp8_internal.h"
+#include "ptx.cuh"
+
+namespace bfp8 {
+
+namespace {
+using namespace dev;
+
+__device__ int g_gemm_err;
+
+constexpr int BM = 128;
+constexpr int BK = 128;
+constexpr int kMaxExperts = 1024;
+constexpr unsigned long long kDrainLimitNs = 100000000ull;
+
+struct GemmParams {
+  int32_t M;   // rows of A (dense) or total expert-sorted rows (grouped)
+  int32_t K, Kb;
+  const float* s_a;
+  int64_t sa_sm, sa_skb;
+  const void* s_w;
+  int32_t sw_f32;
+  int64_t sw_expert_stride;  // scale elements between two experts' grids
+  __nv_bfloat16* y;
+  int64_t ldy;
+  int32_t vec_store;
+  // dense / member mode
+  int32_t m_tiles, total_tiles, n_members;
+  int32_t mem_n0[BFP8_MAX_MEMBERS], mem_rows[BFP8_MAX_MEMBERS], mem_sbase[BFP8_MAX_MEMBERS];
+  int32_t mem_tile0[BFP8_MAX_MEMBERS + 1];
+  // grouped mode
+  const int32_t* offsets;
+  int32_t G, N, n_tiles;
+};
+
+struct Tile {
+  int32_t a_row0, m_valid;   // first A / output row, rows valid from it
+  int32_t b_row0, expert;    // first weight row (expert-local when grouped)
+  int32_t n_out0, n_valid;   // first output column, columns valid from it
+  int32_t srow0, srow_last;  // scale row of the first 128 columns; member's last row
+};
+
+template <int BN, int STAGES, bool W8A16, bool GROUPED>
+struct Cfg {
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kConvWarps = W8A16 ? 4 : 0;
+  static constexpr int kWarps = 2 + kEpiWarps + kConvWarps;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kEpiCols = BN / 2;
+  static constexpr uint32_t kABytes = W8A16 ? BM * BK * 2 : BM * BK;
+  static constexpr uint32_t kBRawBytes = BN * BK;
+  static constexpr uint32_t kBConvBytes = W8A16 ? BN * BK * 2 : 0;
+  static constexpr uint32_t kStage = kABytes + kBRawBytes + kBConvBytes;
+  static constexpr uint32_t kTmaBytes = kABytes + kBRawBytes;
+  static constexpr uint32_t kStgPitch = 80;  // 32 BF16 (64 B) + 16 B pad per row
+  static constexpr uint32_t kStgWarp = 32 * kStgPitch;
+  static constexpr uint32_t kTmemCols = 2 * BN;
+  static constexpr uint32_t kOffStg = STAGES * kStage;
+  static constexpr uint32_t kOffBar = kOffStg + kEpiWarps * kStgWarp;
+  static constexpr uint32_t kNumBars = 3 * STAGES + 5;
+  static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr uint32_t kOffOff = kOffMisc + 16;
+  static constexpr uint32_t kOffPre = kOffOff + (kMaxExperts + 1) * 4;
+  static constexpr uint32_t kSmemUsed = GROUPED ? kOffPre + (kMaxExperts + 1) * 4 : kOffOff;
+  static constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // 1024-byte alignment slack
+  static constexpr uint32_t kIdesc = W8A16 ? idesc_bf16(BM, BN) : idesc_e4m3(BM, BN);
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of two");
+  static_assert(kEpiCols % 32 == 0, "epilogue columns come in 32-column TMEM loads");
+};
+
+template <int BN, bool GROUPED>
+__device__ __forceinline__ void decode_tile(const GemmParams& p, const int* s_off,
+                                            const int* s_pre, int t, Tile& tl) {
+  if (!GROUPED) {
+    const int nt = t / p.m_tiles;
+    const int mt = t - nt * p.m_tiles;
+    int i = 0;
+#pragma unroll 1
+    while (i + 1 < p.n_members && nt >= p.mem_tile0[i + 1]) ++i;
+    const int nl0 = (nt - p.mem_tile0[i]) * BN;
+    tl.a_row0 = mt * BM;
+    tl.m_valid = min(BM, p.M - tl.a_row0);
+    tl.b_row0 = p.mem_n0[i] + nl0;
+    tl.expert = 0;
+    tl.n_out0 = tl.b_row0;
+    tl.n_valid = min(BN, p.mem_rows[i] - nl0);
+    tl.srow0 = p.mem_sbase[i] + nl0 / 128;
+    tl.srow_last = p.mem_sbase[i] + (p.mem_rows[i] + 127) / 128 - 1;
+  } else {
+    int lo = 0, hi = p.G;  // invariant: s_pre[lo] <= t < s_pre[hi]
+#pragma unroll 1
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_pre[mid] <= t) lo = mid; else hi = mid;
+    }
+    const int e = lo;
+    const int row0 = s_off[e];
+    const int rows = s_off[e + 1] - row0;
+    const int mte = (rows + BM - 1) / BM;
+    const int local = t - s_pre[e];
+    const int nt = local / mte;
+    const int mt = local - nt * mte;
+    tl.a_row0 = row0 + mt * BM;
+    tl.m_valid = min(BM, rows - mt * BM);
+    tl.b_row0 = nt * BN;
+    tl.expert = e;
+    tl.n_out0 = nt * BN;
+    tl.n_valid = min(BN, p.N - nt * BN);
+    tl.srow0 = (nt * BN) / 128;
+    tl.srow_last = (p.N + 127) / 128 - 1;
+  }
+}
+
+// Grouped schedule, built by one warp: clamp the offsets into [0, M], make
+// them non-decreasing, then prefix-sum the tiles of every expert.
+__device__ void build_schedule(const GemmParams& p, int* s_off, int* s_pre, int lane) {
+  const int n = p.G + 1;
+  const int per = (n + 31) / 32;
+  const int b = min(n, lane * per), e = min(n, b + per);
+  int run = 0;
+  for (int i = b; i < e; ++i) {
+    int v = p.offsets[i];
+    v = max(0, min(v, p.M));
+    run = max(run, v);
+    s_off[i] = run;
+  }
+  int incl = run;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl = max(incl, o);
+  }
+  int excl = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) excl = 0;
+  for (int i = b; i < e; ++i) s_off[i] = max(s_off[i], excl);
+  __syncwarp();
+  const int per2 = (p.G + 31) / 32;
+  const int b2 = min(p.G, lane * per2), e2 = min(p.G, b2 + per2);
+  int sum = 0;
+  for (int i = b2; i < e2; ++i) sum += ((s_off[i + 1] - s_off[i] + BM - 1) / BM) * p.n_tiles;
+  int incl2 = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl2, off);
+    if (lane >= off) incl2 += o;
+  }
+  int run2 = incl2 - sum;
+  for (int i = b2; i < e2; ++i) {
+    s_pre[i] = run2;
+    run2 += ((s_off[i + 1] - s_off[i] + BM - 1) / BM) * p.n_tiles;
+  }
+  if (lane == 31) s_pre[p.G] = incl2;
+  __syncwarp();
+}
+
+BFP8_DEV bool wait_bounded(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0u && globaltimer() - t0 > limit_ns) return false;
+  }
+}
+
+BFP8_DEV void raise_abort(volatile int* abort_flag) {
+  *abort_flag = 1;
+  atomicExch(&g_gemm_err, static_cast<int>(BFP8_ERR_TIMEOUT));
+}
+
+BFP8_DEV uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int BN, int STAGES, bool W8A16, bool GROUPED>
+__global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ GemmParams p) {
+  using C = Cfg<BN, STAGES, W8A16, GROUPED>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_raw + (base - raw_u32);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const uint32_t bar0 = base + C::kOffBar;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto conv_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (3 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::kOffMisc + 4);
+  int* s_off = reinterpret_cast<int*>(base_ptr + C::kOffOff);
+  int* s_pre = reinterpret_cast<int*>(base_ptr + C::kOffPre);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+      mbar_init(conv_bar(s), W8A16 ? C::kConvWarps : 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), C::kEpiWarps);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (GROUPED && warp == 2) build_schedule(p, s_off, s_pre, lane);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = GROUPED ? s_pre[p.G] : p.total_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        Tile tl;
+        decode_tile<BN, GROUPED>(p, s_off, s_pre, t, tl);
+        for (int kb = 0; kb < p.Kb; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
+          const uint32_t sA = base + stage * C::kStage;
+          const uint32_t sB = sA + C::kABytes;
+          mbar_arrive_expect_tx(full_bar(stage), C::kTmaBytes);
+          if (W8A16) {
+            tma_load_2d(sA, &tmA, kb * BK, tl.a_row0, full_bar(stage));
+            tma_load_2d(sA + BM * 128, &tmA, kb * BK + 64, tl.a_row0, full_bar(stage));
+          } else {
+            tma_load_2d(sA, &tmA, kb * BK, tl.a_row0, full_bar(stage));
+          }
+          if (GROUPED)
+            tma_load_3d(sB, &tmB, kb * BK, tl.b_row0, tl.expert, full_bar(stage));
+          else
+            tma_load_2d(sB, &tmB, kb * BK, tl.b_row0, full_bar(stage));
+          armed |= 1u << stage;
+          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) raise_abort(abort_flag);
+      // No copy may still be landing in shared memory when the CTA exits.
+      for (int s = 0; s < STAGES; ++s)
+        if ((armed >> s) & 1u) wait_bounded(full_bar(s), (armed_phase >> s) & 1u, kDrainLimitNs);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0, buf = 0;
+      uint32_t phase = 0, bphase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int kb = 0; kb < p.Kb; ++kb) {
+          if (!mbar_wait(tempty_bar(buf), bphase ^ 1u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
+          if (W8A16 && !mbar_wait(conv_bar(stage), phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
+          const uint32_t sA = base + stage * C::kStage;
+          if (!W8A16) {
+            const uint64_t da = smem_desc_sw128(sA);
+            const uint64_t db = smem_desc_sw128(sA + C::kABytes);
+#pragma unroll
+            for (int k = 0; k < BK / 32; ++k)  // K = 32 bytes per MMA: +2 in 16-byte units
+              umma_e4m3(d, da + 2u * k, db + 2u * k, C::kIdesc, k > 0 ? 1u : 0u);
+          } else {
+            const uint32_t sConv = sA + C::kABytes + C::kBRawBytes;
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {  // K = 16 BF16 = 32 bytes per MMA
+              const int j = k >> 2, kk = k & 3;
+              const uint64_t da = smem_desc_sw128(sA + j * (BM * 128)) + 2u * kk;
+              const uint64_t db = smem_desc_sw128(sConv + j * (BN * 128)) + 2u * kk;
+              umma_bf16(d, da, db, C::kIdesc, k > 0 ? 1u : 0u);
+            }
+          }
+          umma_commit(empty_bar(stage));
+          umma_commit(tfull_bar(buf));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++buf == 2) { buf = 0; bphase ^= 1u; }
+        }
+      }
+      if (!ok) raise_abort(abort_flag);
+      umma_commit(drain_bar);
+      wait_bounded(drain_bar, 0, kDrainLimitNs);
+    }
+  } else if (warp < 2 + C::kEpiWarps) {
+    // ------------------------------------------------------------ promotion + epilogue
+    const int ew = warp - 2;
+    const int q = warp & 3;
+    const int h = ew >> 2;
+    const int row_in_tile = q * 32 + lane;
+    const uint32_t stg = base + C::kOffStg + ew * C::kStgWarp;
+    const uint16_t* sw16 = static_cast<const uint16_t*>(p.s_w);
+    const float* sw32 = static_cast<const float*>(p.s_w);
+    int buf = 0;
+    uint32_t bphase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      Tile tl;
+      decode_tile<BN, GROUPED>(p, s_off, s_pre, t, tl);
+      const bool row_ok = row_in_tile < tl.m_valid;
+      const int64_t arow = static_cast<int64_t>(tl.a_row0) + row_in_tile;
+      const int srow = min(tl.srow0 + (h * C::kEpiCols) / 128, tl.srow_last);
+      const int64_t sw_idx = (GROUPED ? tl.expert * p.sw_expert_stride : 0) +
+                             static_cast<int64_t>(srow) * p.Kb;
+      const float* sa_row = p.s_a + (row_ok ? arow * p.sa_sm : 0);
+      auto factor = [&](int kb) -> float {
+        const float sw = p.sw_f32 ? __ldg(sw32 + sw_idx + kb) : bf16_bits_to_f32(__ldg(sw16 + sw_idx + kb));
+        if (W8A16) return sw;
+        const float sa = row_ok ? __ldg(sa_row + kb * p.sa_skb) : 0.0f;
+        return sa * sw;
+      };
+      float acc[C::kEpiCols];
+#pragma unroll
+      for (int i = 0; i < C::kEpiCols; ++i) acc[i] = 0.0f;
+      float f_next = factor(0);
+      for (int kb = 0; kb < p.Kb; ++kb) {
+        const float f = f_next;
+        if (kb + 1 < p.Kb) f_next = factor(kb + 1);
+        const bool w_ok = mbar_wait(tfull_bar(buf), bphase, abort_flag);
+        if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                               static_cast<uint32_t>(buf * BN + h * C::kEpiCols);
+#pragma unroll
+        for (int c = 0; c < C::kEpiCols / 32; ++c) {
+          float v[32];
+          tmem_ld32(taddr + 32u * c, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(v[j], f, acc[32 * c + j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(buf));
+        if (++buf == 2) { buf = 0; bphase ^= 1u; }
+      }
+      if (!ok) break;
+      // BF16 tile store: stage 32 rows x 32 columns through shared memory so
+      // that global stores are row-contiguous 64-byte segments.
+#pragma unroll
+      for (int ps = 0; ps < C::kEpiCols / 32; ++ps) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint4 v;
+          v.x = pack_bf16x2(acc[32 * ps + 8 * i + 0], acc[32 * ps + 8 * i + 1]);
+          v.y = pack_bf16x2(acc[32 * ps + 8 * i + 2], acc[32 * ps + 8 * i + 3]);
+          v.z = pack_bf16x2(acc[32 * ps + 8 * i + 4], acc[32 * ps + 8 * i + 5]);
+          v.w = pack_bf16x2(acc[32 * ps + 8 * i + 6], acc[32 * ps + 8 * i + 7]);
+          sts128(stg + lane * C::kStgPitch + 16u * i, v);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int chunk = it * 32 + lane;
+          const int r = chunk >> 2, cq = chunk & 3;
+          const uint4 v = lds128(stg + r * C::kStgPitch + 16u * cq);
+          const int rt = q * 32 + r;
+          const int ct = h * C::kEpiCols + ps * 32 + cq * 8;
+          if (rt < tl.m_valid) {
+            __nv_bfloat16* dst = p.y + (static_cast<int64_t>(tl.a_row0) + rt) * p.ldy + tl.n_out0 + ct;
+            if (p.vec_store && ct + 8 <= tl.n_valid) {
+              *reinterpret_cast<uint4*>(dst) = v;
+            } else {
+              const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (ct + e < tl.n_valid)
+                  reinterpret_cast<uint16_t*>(dst)[e] = static_cast<uint16_t>(wv[e >> 1] >> (16 * (e & 1)));
+            }
+          }
+        }
+        __syncwarp();
+      }
+    }
+    if (!ok) raise_abort(abort_flag);
+  } else {
+    // ------------------------------------------------------------ E4M3 -> BF16 decode (W8A16)
+    const int cw = warp - 2 - C::kEpiWarps;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int kb = 0; kb < p.Kb; ++kb) {
+        const bool w_ok = mbar_wait(full_bar(stage), phase, abort_flag);
+        if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
+        const uint32_t sRaw = base + stage * C::kStage + C::kABytes;
+        const uint32_t sConv = sRaw + C::kBRawBytes;
+        for (int idx = cw * 32 + lane; idx < BN * 8; idx += C::kConvWarps * 32) {
+          const int r = idx >> 3, c = idx & 7;  // row, 16-byte chunk (16 K values)
+          const uint4 raw = lds128(sRaw + r * 128 + c * 16);
+          uint4 o0, o1;
+          e4m3x4_to_bf16x4(raw.x, o0.x, o0.y);
+          e4m3x4_to_bf16x4(raw.y, o0.z, o0.w);
+          e4m3x4_to_bf16x4(raw.z, o1.x, o1.y);
+          e4m3x4_to_bf16x4(raw.w, o1.z, o1.w);
+          const int j = c >> 2, cc = (c & 3) * 2;
+          const uint32_t row_addr = sConv + j * (BN * 128) + r * 128;
+          sts128(row_addr + (static_cast<uint32_t>(cc ^ (r & 7)) << 4), o0);
+          sts128(row_addr + (static_cast<uint32_t>((cc + 1) ^ (r & 7)) << 4), o1);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(conv_bar(stage));
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok) raise_abort(abort_flag);
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+template <int BN, int STAGES, bool W8A16, bool GROUPED>
+int launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int grid,
+           void* stream) {
+  using C = Cfg<BN, STAGES, W8A16, GROUPED>;
+  auto kernel = gemm_kernel<BN, STAGES, W8A16, GROUPED>;
+  int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel), C::kSmemBytes);
+  if (rc != BFP8_OK) return rc;
+  kernel<<<grid, C::kThreads, C::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(ta, tb, p);
+  return check_launch();
+}
+
+bool aligned16(const void* ptr) { return reinterpret_cast<uintptr_t>(ptr) % 16 == 0; }
+
+int fill_members(GemmParams& p, const MemberTable& mt, int bn, int64_t M, const void* y,
+                 int64_t ldy) {
+  p.n_members = mt.count;
+  int tiles = 0;
+  bool vec = aligned16(y) && (ldy % 8 == 0);
+  for (int i = 0; i < mt.count; ++i) {
+    p.mem_n0[i] = static_cast<int32_t>(mt.n0[i]);
+    p.mem_rows[i] = static_cast<int32_t>(mt.rows[i]);
+    p.mem_sbase[i] = static_cast<int32_t>(mt.sbase[i]);
+    p.mem_tile0[i] = tiles;
+    tiles += static_cast<int>((mt.rows[i] + bn - 1) / bn);
+    if (mt.n0[i] % 8 != 0) vec = false;
+  }
+  p.mem_tile0[mt.count] = tiles;
+  p.m_tiles = static_cast<int32_t>((M + BM - 1) / BM);
+  const int64_t total = static_cast<int64_t>(p.m_tiles) * tiles;
+  if (total > 0x7FFFFFFF) return BFP8_ERR_UNSUPPORTED;
+  p.total_tiles = static_cast<int32_t>(total);
+  p.vec_store = vec ? 1 : 0;
+  return BFP8_OK;
+}
+
+bool fits_i32(int64_t v) { return v >= 0 && v <= 0x7FFFFFFF; }
+
+}  // namespace
+
+constexpr int kBN8 = 256, kStages8 = 4;
+constexpr int kBN16 = 128, kStages16 = 2;
+
+int launch_gemm_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
+                     const void* w, const void* w_scale, int32_t w_scale_dtype, int64_t M,
+                     int64_t N, int64_t K, void* y, int64_t ldy, const MemberTable& mt,
+                     void* stream) {
+  if (K % 16 != 0 || !aligned16(q_a) || !aligned16(w)) return BFP8_ERR_UNSUPPORTED;
+  if (!fits_i32(M) || !fits_i32(N) || !fits_i32(K)) return BFP8_ERR_UNSUPPORTED;
+  if (sa_sm < 0 || sa_skb < 0) return BFP8_ERR_INVALID_ARG;
+  int sms = 0;
+  int rc = sm_count(&sms);
+  if (rc != BFP8_OK) return rc;
+  CUtensorMap ta, tb;
+  rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_a, K, M, K, BK, BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != BFP8_OK) return rc;
+  rc = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, K, BK, kBN8,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != BFP8_OK) return rc;
+  GemmParams p{};
+  p.M = static_cast<int32_t>(M);
+  p.K = static_cast<int32_t>(K);
+  p.Kb = static_cast<int32_t>((K + BK - 1) / BK);
+  p.s_a = s_a;
+  p.sa_sm = sa_sm;
+  p.sa_skb = sa_skb;
+  p.s_w = w_scale;
+  p.sw_f32 = w_scale_dtype == BFP8_DT_F32;
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.ldy = ldy;
+  rc = fill_members(p, mt, kBN8, M, y, ldy);
+  if (rc != BFP8_OK) return rc;
+  const int grid = p.total_tiles < sms ? p.total_tiles : sms;
+  return launch<kBN8, kStages8, false, false>(ta, tb, p, grid, stream);
+}
+
+int launch_gemm_w8a16(const void* x, int64_t ldx, const void* w, const void* w_scale,
+                      int32_t w_scale_dtype, int64_t M, int64_t N, int64_t K, void* y,
+                      int64_t ldy, const MemberTable& mt, void* stream) {
+  if (K % 16 != 0 || ldx % 8 != 0 || !aligned16(x) || !aligned16(w)) return BFP8_ERR_UNSUPPORTED;
+  if (!fits_i32(M) || !fits_i32(N) || !fits_i32(K)) return BFP8_ERR_UNSUPPORTED;
+  int sms = 0;
+  int rc = sm_count(&sms);
+  if (rc != BFP8_OK) return rc;
+  CUtensorMap ta, tb;
+  rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, ldx * 2, 64, BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != BFP8_OK) return rc;
+  rc = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, K, BK, kBN16,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc != BFP8_OK) return rc;
+  GemmParams p{};
+  p.M = static_cast<int32_t>(M);
+  p.K = static_cast<int32_t>(K);
+  p.Kb = static_cast<int32_t>((K + BK - 1) / BK);
+  p.s_a = nullptr;
+  p.s_w = w_scale;
+  p.sw_f32 = w_scale_dtype == BFP8_DT_F32;
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.ldy = ldy;
+  rc = fill_members(p, mt, kBN16, M, y, ldy);
+  if (rc != BFP8_OK) return rc;
+  const int grid = p.total_tiles < sms ? p.total_tiles : sms;
+  return launch<kBN16, kStages16, true, false>(ta, tb, p, grid, stream);
+}
+
+int launch_grouped_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
+                        const void* w, const void* w_scale, int32_t w_scale_dtype,
+                        const int32_t* offsets, int32_t G, int64_t total_M, int64_t N,
+                        int64_t K, void* y, int64_t ldy, void* stream) {
+  if (K % 16 != 0 || !aligned16(q_a) || !aligned16(w)) return BFP8_ERR_UNSUPPORTED;
+  if (!fits_i32(total_M) || !fits_i32(N) || !fits_i32(K)) return BFP8_ERR_UNSUPPORTED;
+  if (G < 1 || G > kMaxExperts) return BFP8_ERR_INVALID_ARG;
+  if (sa_sm < 0 || sa_skb < 0) return BFP8_ERR_INVALID_ARG;
+  int sms = 0;
+  int rc = sm_count(&sms);
+  if (rc != BFP8_OK) return rc;
+  CUtensorMap ta, tb;
+  rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_a, K, total_M, K, BK, BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != BFP8_OK) return rc;
+  rc = make_tmap_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, G, K, N * K, BK, kBN8, 1,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != BFP8_OK) return rc;
+  GemmParams p{};
+  p.M = static_cast<int32_t>(total_M);
+  p.K = static_cast<int32_t>(K);
+  p.Kb = static_cast<int32_t>((K + BK - 1) / BK);
+  p.s_a = s_a;
+  p.sa_sm = sa_sm;
+  p.sa_skb = sa_skb;
+  p.s_w = w_scale;
+  p.sw_f32 = w_scale_dtype == BFP8_DT_F32;
+  p.sw_expert_stride = ((N + 127) / 128) * static_cast<int64_t>(p.Kb);
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.ldy = ldy;
+  p.vec_store = (aligned16(y) && ldy % 8 == 0) ? 1 : 0;
+  p.offsets = offsets;
+  p.G = G;
+  p.N = static_cast<int32_t>(N);
+  p.n_tiles = static_cast<int32_t>((N + kBN8 - 1) / kBN8);
+  p.n_members = 1;
+  return launch<kBN8, kStages8, false, true>(ta, tb, p, sms, stream);
+}
+
+int gemm_read_clear_error() {
+  int v = 0;
+  const int zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_gemm_err, sizeof(int)) != cudaSuccess) return BFP8_ERR_CUDA;
+  if (v != 0 && cudaMemcpyToSymbol(g_gemm_err, &zero, sizeof(int)) != cudaSuccess)
+    return BFP8_ERR_CUDA;
+  return v == 0 ? BFP8_OK : v;
+}
+
+}  // namespace bfp8

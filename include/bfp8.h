@@ -1,0 +1,279 @@
+/*
+ * bfp8.h -- C ABI of libbfp8, the block-scaled FP8 linear projection for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation: y[M,N] = x[M,K] . W^T. W is E4M3 [N,K] row-major ([out,in],
+ * K contiguous), with a "weight_scale_inv" grid of one MULTIPLIER (not a
+ * reciprocal) per 128x128 block, stored as BF16 or F32. Scale grids are
+ * ceil-divided for partial tails. A grouped tensor (fused QKV, gate/up) keeps
+ * a block-row origin per member.
+ *   [Qwen checkpoints with block FP8 weights, paragraphs 1-3]
+ *   [th#1803 decoder PR, "What lands"]
+ *   [FP8 Native Serving, "The two FP8 checkpoint shapes"]
+ *
+ * Conventions that hold for every entry point:
+ *  - Returns an int status (bfp8_status). 0 means success. No exception,
+ *    abort or exit crosses this boundary. bfp8_status_string() names each code.
+ *  - Tensor pointers are DEVICE pointers owned by the caller. The library
+ *    allocates nothing and keeps no per-tensor state; the only state it holds
+ *    is a per-device cache of attributes and kernel settings.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Work is enqueued asynchronously on it. Launch failures are
+ *    reported as BFP8_ERR_CUDA.
+ *  - Sizes and leading dimensions are in ELEMENTS unless a name says bytes.
+ *  - Geometry that the tensor-memory-accelerator (TMA) path cannot address
+ *    (row strides that are not multiples of 16 bytes, base pointers not
+ *    16-byte aligned) is refused with BFP8_ERR_UNSUPPORTED. There is no
+ *    silent fallback and no CPU path.
+ *  - Calls are thread-safe and re-entrant. Calls on different streams may
+ *    overlap on the GPU unless an entry point says otherwise.
+ *  - Kernel waits are bounded. If one runs out (which means a bug, not a
+ *    data condition), the kernel records BFP8_ERR_TIMEOUT in a device word and
+ *    returns early. bfp8_device_status() reads and clears that word.
+ */
+#ifndef BFP8_H_
+#define BFP8_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------- */
+enum bfp8_status {
+  BFP8_OK = 0,
+  BFP8_ERR_INVALID_ARG = 1,     /* null pointer, negative size, bad stride   */
+  BFP8_ERR_E5M2 = 2,            /* E5M2 weight encoding                       */
+  BFP8_ERR_NO_SCALE = 3,        /* FP8 weight without weight_scale_inv        */
+  BFP8_ERR_ROW_SCALE = 4,       /* rank-1 / per-row weight_scale tree         */
+  BFP8_ERR_AMBIGUOUS_SCALE = 5, /* both row and block scales, or a per-row grid */
+  BFP8_ERR_GRID_TRANSPOSED = 6, /* grid shaped [ceil(K/128), ceil(N/128)]     */
+  BFP8_ERR_GRID_SHAPE = 7,      /* any other mis-blocked grid                 */
+  BFP8_ERR_SCALE_DTYPE = 8,     /* scale neither BF16 nor F32                 */
+  BFP8_ERR_BLOCK_SIZE = 9,      /* declared weight_block_size != [128,128]    */
+  BFP8_ERR_QUANT_METHOD = 10,   /* declared quant_method != fp8               */
+  BFP8_ERR_GROUP = 11,          /* member rows do not partition N / grid not member-local */
+  BFP8_ERR_NOT_FP8 = 12,        /* dense (BF16/F16/F32) weight                */
+  BFP8_ERR_UNSUPPORTED = 13,    /* geometry outside what the kernels address  */
+  BFP8_ERR_CUDA = 14,           /* a CUDA runtime/driver call failed          */
+  BFP8_ERR_TIMEOUT = 15         /* a bounded device wait ran out              */
+};
+
+/* ---- element / scale types --------------------------------------------- */
+enum bfp8_dtype {
+  BFP8_DT_NONE = 0,
+  BFP8_DT_E4M3 = 1,
+  BFP8_DT_E5M2 = 2,
+  BFP8_DT_BF16 = 3,
+  BFP8_DT_F16 = 4,
+  BFP8_DT_F32 = 5
+};
+
+/* Largest number of members a grouped (fused) weight may have. */
+#define BFP8_MAX_MEMBERS 8
+
+/* Name of a status code ("OK", "E5M2", ...). Never NULL. */
+const char* bfp8_status_string(int status);
+
+/* ---- a1: grid validation (host only, metadata only) --------------------- */
+/*
+ * Header-only view of one weight tensor, as read from a checkpoint's
+ * safetensors header and quantization config before any weight byte is read.
+ *   [th#1803 decoder PR, "What lands": verification from headers alone]
+ */
+typedef struct {
+  int32_t weight_dtype;        /* bfp8_dtype of the weight bytes              */
+  int32_t weight_rank;         /* must be 2                                   */
+  int64_t weight_shape[2];     /* [N, K]                                      */
+  int32_t scale_dtype;         /* dtype of weight_scale_inv, BFP8_DT_NONE if absent */
+  int32_t scale_rank;          /* rank of weight_scale_inv (1 or 2)           */
+  int64_t scale_shape[2];      /* its shape (scale_shape[1] unused if rank 1) */
+  int32_t has_row_scale;       /* a per-row "weight_scale" leaf is present    */
+  int32_t declared_quant_fp8;  /* config declares quant_method == "fp8"       */
+  int32_t declared_block[2];   /* config's weight_block_size                  */
+  int32_t n_members;           /* 0 = plain tensor; else rows per member below */
+  const int64_t* member_rows;  /* host array [n_members], NULL if n_members==0 */
+} bfp8_weight_desc;
+
+/*
+ * bfp8_validate_grid -- accept or refuse a block-FP8 weight before upload.
+ *   [Qwen checkpoints with block FP8 weights, paragraph 3: E5M2, ambiguous
+ *    row/block scales, malformed grids and incompatible declarations refuse
+ *    before model upload]
+ *   [th#1803 decoder PR, "Why the refusals matter more than the load": a
+ *    row-wise tree, a transposed or mis-blocked grid, an FP8 weight with no
+ *    scale, a rank-1 scale and a config that disagrees with the bytes are each
+ *    refused by name]
+ * Pure host code; needs no GPU. The first failing rule decides:
+ *   INVALID_ARG, E5M2, NOT_FP8, QUANT_METHOD, BLOCK_SIZE, AMBIGUOUS_SCALE
+ *   (row+block), ROW_SCALE (row leaf only), NO_SCALE, ROW_SCALE (rank 1),
+ *   SCALE_DTYPE, GRID_SHAPE (rank != 2), GROUP (members), OK (grid equals
+ *   [sum ceil(N_i/128), ceil(K/128)]), GRID_TRANSPOSED, AMBIGUOUS_SCALE
+ *   (rows == N), GROUP (grid built on the stacked rows), GRID_SHAPE.
+ * msg (optional, may be NULL): receives a NUL-terminated explanation,
+ * truncated to msg_len bytes.
+ */
+int bfp8_validate_grid(const bfp8_weight_desc* desc, char* msg, size_t msg_len);
+
+/* ---- a2: per-token 1x128 activation quantization ------------------------ */
+/*
+ * bfp8_act_quant_group -- dynamic E4M3 quantization of BF16 activations.
+ *   [Module w8a8_prefill, arithmetic paragraph: per-token 1x128 FP32
+ *    activation scales, as per_token_group_quant_fp8 computes them]
+ * For token m and group g (columns [128g, min(128g+128, K))):
+ *   amax = max|x|, s = max(amax, 1e-10f) / 448.0f, q = RNE_satfinite_e4m3(x / s)
+ * with IEEE float32 division. This is bit-exact with the CPU oracle for finite
+ * inputs.
+ *   x_bf16  [M, K] BF16, row stride ldx >= K (elements)
+ *   q_e4m3  [M, K] E4M3 bytes, row stride ldq >= K (bytes)
+ *   scales  float32, element (m, g) at scales[m*s_stride_m + g*s_stride_kb];
+ *           row-major [M, ceil(K/128)] is (ceil(K/128), 1); the token-
+ *           contiguous (MN-major) layout is (1, M).
+ * M == 0 or K == 0 is a no-op. Errors: INVALID_ARG for null pointers,
+ * negative sizes or ld < K.
+ */
+int bfp8_act_quant_group(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
+                         void* q_e4m3, int64_t ldq, float* scales,
+                         int64_t s_stride_m, int64_t s_stride_kb, void* stream);
+
+/* ---- a10: SiLU(gate)*up fused with the 1x128 quantization --------------- */
+/*
+ * bfp8_silu_mul_act_quant -- the glue between the gate/up and down
+ * projections of the dense FFN [Module w8a8_prefill, first paragraph: the
+ * gate/up/down GEMM arm].
+ *   gu_bf16 [M, 2I] BF16 (gate columns 0..I-1, up columns I..2I-1), row stride ld
+ *   h = bf16_rn( silu(g) * u ) with silu(g) = g / (1 + exp(-g)) in float32,
+ *   then the same quantization as bfp8_act_quant_group over [M, I].
+ * Output arguments as for bfp8_act_quant_group with K = I.
+ */
+int bfp8_silu_mul_act_quant(const void* gu_bf16, int64_t M, int64_t I, int64_t ld,
+                            void* q_e4m3, int64_t ldq, float* scales,
+                            int64_t s_stride_m, int64_t s_stride_kb, void* stream);
+
+/* ---- ahead-of-time weight block quantization (conversion endpoint) ------ */
+/*
+ * bfp8_quantize_weight_block -- produce a block-FP8 weight from float32.
+ * Quantization happens ahead of time through a conversion step, never at load
+ * [th#1803 decoder PR, "Why the refusals matter more than the load"]. Per
+ * 128x128 block: s = max(amax, 1e-10f)/448.0f, stored RNE to BF16 (or as F32);
+ * q = RNE_satfinite_e4m3(w / s_stored).
+ *   w      [N, K] float32, row stride ldw (elements)
+ *   q      [N, K] E4M3 bytes, row stride ldq (bytes)
+ *   scale  [ceil(N/128), ceil(K/128)] row-major, BFP8_DT_BF16 or BFP8_DT_F32
+ */
+int bfp8_quantize_weight_block(const float* w, int64_t N, int64_t K, int64_t ldw,
+                               void* q, int64_t ldq, void* scale, int32_t scale_dtype,
+                               void* stream);
+
+/* Member table of a grouped weight: rows of each stacked member, in order.
+ * Host memory; NULL (or n_members == 0) means a single member of N rows. */
+typedef struct {
+  int32_t n_members;
+  const int64_t* member_rows;
+} bfp8_members;
+
+/* ---- a3-a5, a8: W8A8 block-scaled projection (tcgen05 / TMEM) ----------- */
+/*
+ * bfp8_linear_w8a8 -- y = dequant(q_a) . dequant(W)^T.
+ *   [Module w8a8_prefill, arithmetic paragraph: per-token 1x128 activation
+ *    scales times 128x128 weight scales in an FP32 epilogue per K-block, FP32
+ *    accumulation]
+ *   [FP8 Native Serving, "Native FP8 vs dequant-to-BF16": FP8 through the
+ *    tensor cores, BF16 only when the result is written]
+ * For every 128-wide K-block kb the tensor cores form the exact FP8 product
+ * sum P in FP32. The kernel then does acc += P * (s_a[m,kb] * s_w[r(n),kb]) in
+ * FP32 and finally writes y = bf16_rn(acc). r(n) is the member-local scale row.
+ *   q_a      [M, K] E4M3, row stride K bytes (densely packed)
+ *   s_a      float32 activation scales, (m,kb) at s_a[m*s_stride_m + kb*s_stride_kb]
+ *   w_e4m3   [N, K] E4M3 row-major (members stacked), row stride K bytes
+ *   w_scale  [sum_i ceil(N_i/128), ceil(K/128)] row-major, w_scale_dtype BF16 or F32
+ *   y_bf16   [M, N] BF16, row stride ldy >= N (elements)
+ *   members  member table (host), NULL for one member
+ * Requirements: K % 16 == 0 (TMA row pitch); q_a, w_e4m3 16-byte aligned;
+ * y_bf16 16-byte aligned and ldy % 8 == 0. M == 0 is a no-op.
+ */
+int bfp8_linear_w8a8(const void* q_a, const float* s_a, int64_t s_stride_m, int64_t s_stride_kb,
+                     const void* w_e4m3, const void* w_scale, int32_t w_scale_dtype,
+                     int64_t M, int64_t N, int64_t K, void* y_bf16, int64_t ldy,
+                     const bfp8_members* members, void* stream);
+
+/* ---- a6: W8A16 block-scaled projection ---------------------------------- */
+/*
+ * bfp8_linear_w8a16 -- BF16 activations, FP8 weights decoded exactly to BF16
+ * in shared memory right before a BF16 tensor-core MMA.
+ *   [FP8 Native Serving, "Native FP8 vs dequant-to-BF16": convert to BF16 in
+ *    the GEMM fragment, MMA in BF16]
+ *   [Qwen checkpoints with block FP8 weights, paragraph 2: block multipliers
+ *    applied inside the projection reduction, F32 accumulation]
+ * y[m,n] = bf16_rn( sum_kb s_w[r(n),kb] * sum_{k in kb} x[m,k] * e4m3(W[n,k]) ), FP32.
+ *   x_bf16 [M, K] BF16, row stride ldx (elements), ldx % 8 == 0, 16-byte aligned
+ *   other arguments and requirements as bfp8_linear_w8a8.
+ */
+int bfp8_linear_w8a16(const void* x_bf16, int64_t ldx, const void* w_e4m3, const void* w_scale,
+                      int32_t w_scale_dtype, int64_t M, int64_t N, int64_t K,
+                      void* y_bf16, int64_t ldy, const bfp8_members* members, void* stream);
+
+/* ---- a7: decode GEMV, M <= 16 ------------------------------------------- */
+/*
+ * bfp8_gemv_decode -- the memory-bound small-M projection (W8A16 arithmetic).
+ *   [Module w8a8_prefill, "Reachability": the GB10 decode path is an unfused
+ *    per-projection GEMV]
+ * Streams W once with 16-byte loads. Each 16x16 fragment is decoded E4M3->BF16
+ * in registers, multiplied on the tensor cores and scaled per 128-K block in
+ * FP32 registers. Split-K partial sums are reduced in a fixed order through
+ * `workspace`, so results are deterministic.
+ *   x_bf16 [M, K] BF16, row stride ldx (ldx % 8 == 0, 16-byte aligned), 1 <= M <= 16
+ *   w_e4m3 [N, K], w_scale grid as bfp8_linear_w8a8 (K % 16 == 0)
+ *   y_bf16 [M, N] BF16, row stride ldy (elements)
+ *   workspace  device scratch of at least bfp8_gemv_decode_workspace(M,N,K)
+ *              bytes, caller-owned. Its contents need not be initialised. Two
+ *              calls that share one workspace must not overlap on the GPU.
+ */
+int bfp8_gemv_decode(const void* x_bf16, int64_t ldx, const void* w_e4m3, const void* w_scale,
+                     int32_t w_scale_dtype, int64_t M, int64_t N, int64_t K,
+                     void* y_bf16, int64_t ldy, const bfp8_members* members,
+                     void* workspace, size_t ws_bytes, void* stream);
+
+/* Workspace bytes bfp8_gemv_decode needs on the current device (0 if none). */
+size_t bfp8_gemv_decode_workspace(int64_t M, int64_t N, int64_t K);
+
+/* ---- a9: grouped (per-expert) W8A8 projection ---------------------------- */
+/*
+ * bfp8_grouped_linear -- the MoE expert projections over a token-offset table.
+ *   [Module w8a8_prefill, "WHY": the MoE expert path on the W8A8 block-scaled
+ *    projection]
+ * Rows offsets[e] .. offsets[e+1]-1 of the expert-sorted activations use
+ * expert e's weight W[e] and scale grid s_w[e]. The arithmetic per row is that
+ * of bfp8_linear_w8a8. The tile schedule is built on the device from
+ * `offsets_dev`, so there is no host synchronisation. Empty experts cost
+ * nothing.
+ *   q_a        [total_M, K] E4M3 (expert-sorted), row stride K bytes
+ *   s_a        float32 activation scales as bfp8_linear_w8a8
+ *   w_e4m3     [G, N, K] E4M3; w_scale [G, ceil(N/128), ceil(K/128)]
+ *   offsets_dev int32 [G+1] on the device. They should be non-decreasing with
+ *              offsets[0] == 0 and offsets[G] == total_M. The kernel clamps
+ *              values outside [0, total_M] and never reads or writes outside
+ *              the tensors.
+ *   y_bf16     [total_M, N] BF16, row stride ldy
+ * Requirements: 1 <= G <= 1024; K % 16 == 0; alignments as bfp8_linear_w8a8.
+ */
+int bfp8_grouped_linear(const void* q_a, const float* s_a, int64_t s_stride_m, int64_t s_stride_kb,
+                        const void* w_e4m3, const void* w_scale, int32_t w_scale_dtype,
+                        const int32_t* offsets_dev, int32_t G, int64_t total_M, int64_t N,
+                        int64_t K, void* y_bf16, int64_t ldy, void* stream);
+
+/* ---- diagnostics ---------------------------------------------------------- */
+/*
+ * bfp8_device_status -- synchronise `stream`, then read and clear the library's
+ * device error word on the current device. Returns BFP8_OK, BFP8_ERR_TIMEOUT
+ * if a bounded wait ran out in a kernel since the last call, or BFP8_ERR_CUDA.
+ */
+int bfp8_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BFP8_H_ */

@@ -1,0 +1,96 @@
+"""GPU parity: bfp8_gemv_decode (M <= 16) against the oracle's W8A16 definition.
+
+Cases: a one-hot probe with unit scales whose outputs are exact E4M3 values
+(it pins the in-register decode, the K permutation and the row mapping);
+small ragged shapes; member-local grids; the decode workload's full shapes
+(gate/up [34816, 5120], down [5120, 17408], M in {1, 4, 16}) on sampled output
+columns; and bitwise determinism across calls that share one workspace.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_fp8_token_gb300 import synth
+from gpu_util import (assert_close, bits16, dense_ffn_weights, gpu_bf16_to_f64, quantize_members,
+                      sample_indices, scale_to_dev, to_dev_bf16, to_dev_u8)
+from oracle import formats as F
+from oracle import linear as L
+
+pytestmark = pytest.mark.gpu
+
+
+def _gemv(bfp8, dev, xb, q, s, members=None):
+    M, K = xb.shape
+    N = q.shape[0]
+    x = to_dev_bf16(xb, dev)
+    w = to_dev_u8(q, dev)
+    sw = scale_to_dev(s, dev)
+    y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(bfp8.bfp8_gemv_decode_workspace(M, N, K), dtype=torch.uint8, device=dev)
+    bfp8.bfp8_gemv_decode(x, w, sw, y, ws, member_rows=members)
+    torch.cuda.synchronize()
+    assert bfp8.bfp8_device_status() == 0
+    return y
+
+
+def test_gemv_one_hot_exact_decode(bfp8, cuda_device):
+    rng = np.random.default_rng(0)
+    N, K, M = 256, 512, 16
+    q = rng.integers(0, 256, (N, K), dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x38                      # no NaN codes
+    s = F.f32_to_bf16_bits(np.ones((2, 4), np.float32))
+    ks = rng.choice(K, M, replace=False)
+    x = np.zeros((M, K), np.float32)
+    x[np.arange(M), ks] = 1.0
+    y = _gemv(bfp8, cuda_device, F.f32_to_bf16_bits(x), q, s)
+    got = gpu_bf16_to_f64(y)
+    want = F.e4m3_decode_lut()[q[:, ks].T]
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("M,N,K,members", [
+    (1, 192, 320, None), (3, 200, 320, None), (8, 130, 256, None), (9, 384, 640, None),
+    (16, 300, 1024, [100, 200]), (5, 1000, 2048, [500, 500]), (16, 256, 128, None),
+])
+def test_gemv_small(bfp8, cuda_device, M, N, K, members):
+    g = synth.generator(M * 1000 + N + K)
+    w = synth.weight_f32(g, N, K).numpy()
+    xb = bits16(synth.activations_bf16(g, M, K))
+    q, s = quantize_members(w, members)
+    y = _gemv(bfp8, cuda_device, xb, q, s, members)
+    ref = L.linear_w8a16(xb, q, s, members)
+    assert_close(gpu_bf16_to_f64(y), ref, f"gemv M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("which", ["gate_up", "down"])
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_gemv_decode_workload(bfp8, cuda_device, which, M):
+    qgu, sgu, qd, sd, _ = dense_ffn_weights(0)
+    q, s = (qgu, sgu) if which == "gate_up" else (qd, sd)
+    members = [17408, 17408] if which == "gate_up" else None
+    N, K = q.shape
+    xb = bits16(synth.decode_tokens(100 + M, M, K))
+    y = _gemv(bfp8, cuda_device, xb, q, s, members)
+    cols = sample_indices(N, 1500, seed=M)
+    ref = L.linear_w8a16(xb, q, s, members, cols=cols)
+    assert_close(gpu_bf16_to_f64(y)[:, cols], ref, f"decode {which} M={M}")
+
+
+def test_gemv_deterministic_workspace_reuse(bfp8, cuda_device):
+    qgu, sgu, qd, sd, _ = dense_ffn_weights(0)
+    dev = cuda_device
+    M, K = 16, qd.shape[1]
+    N = qd.shape[0]
+    x = to_dev_bf16(bits16(synth.decode_tokens(7, M, K)), dev)
+    w = to_dev_u8(qd, dev)
+    sw = scale_to_dev(sd, dev)
+    ws = torch.empty(bfp8.bfp8_gemv_decode_workspace(M, N, K), dtype=torch.uint8, device=dev)
+    ys = []
+    for _ in range(3):
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        bfp8.bfp8_gemv_decode(x, w, sw, y, ws)
+        ys.append(y)
+    torch.cuda.synchronize()
+    assert torch.equal(ys[0].view(torch.int16), ys[1].view(torch.int16))
+    assert torch.equal(ys[0].view(torch.int16), ys[2].view(torch.int16))
