@@ -77,6 +77,8 @@ _SIGS = {
     "bfp8_gemv_decode": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _i64,
                                         ctypes.POINTER(bfp8_members), _vp, _sz, _vp]),
     "bfp8_gemv_decode_workspace": (_sz, [_i64, _i64, _i64]),
+    "bfp8_gemv_decode_noalloc": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _i64, _i64, _i64, _vp,
+                                                _i64, ctypes.POINTER(bfp8_members), _vp]),
     "bfp8_grouped_linear": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i32, _vp, _i32, _i64,
                                            _i64, _i64, _vp, _i64, _vp]),
     "bfp8_device_status": (ctypes.c_int, [_vp]),
@@ -228,6 +230,18 @@ def bfp8_gemv_decode(x, w, w_scale, y, workspace, member_rows=None, stream=None)
                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _stream(stream)),
            "bfp8_gemv_decode")
+
+
+def bfp8_gemv_decode_noalloc(x, w, w_scale, y, member_rows=None, stream=None) -> None:
+    """bfp8_gemv_decode without a workspace argument, for callers that cannot
+    allocate device memory; its scratch is a fixed array inside the library."""
+    M, K = x.shape
+    N = w.shape[0]
+    mref, _keep = _members(member_rows)
+    _check(_lib.bfp8_gemv_decode_noalloc(_ptr(x), x.stride(0), _ptr(w), _ptr(w_scale),
+                                         _scale_dtype(w_scale), M, N, K, _ptr(y), y.stride(0),
+                                         mref, _stream(stream)),
+           "bfp8_gemv_decode_noalloc")
 
 
 def bfp8_grouped_linear(q_a, s_a, w, w_scale, offsets, y, s_stride_m=None, s_stride_kb=None,

@@ -27,6 +27,8 @@
 //     BF16 directly. Partial tiles go to the workspace, and the last CTA to
 //     arrive sums the partials in CTA order (deterministic) and writes y. No
 //     CTA ever waits on another.
+#include <mutex>
+
 #include "bfp8_internal.h"
 #include "ptx.cuh"
 
@@ -404,6 +406,43 @@ int launch_gemv(const void* x, int64_t ldx, const void* w, const void* w_scale,
   return ntb == 1 ? launch_t<1>(tw, tx, p, stream) : launch_t<2>(tw, tx, p, stream);
 }
 
+// ---------------------------------------------------------------------------
+// bfp8_gemv_decode_noalloc: the decode GEMV for callers that cannot allocate
+// device memory. Its split-K scratch (tile counters + partial tiles) lives in
+// this fixed array instead of a caller-provided workspace. Every GPU that
+// loads the library holds the array until the process exits. All calls on one
+// device share it, so calls that overlap on the GPU race.
+static __device__ __align__(256) unsigned char g_gemv_noalloc_scratch[BFP8_GEMV_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+
+struct NoAllocSlot {
+  std::once_flag once;
+  void* ptr = nullptr;
+  cudaError_t err = cudaSuccess;
+};
+NoAllocSlot g_noalloc_slots[kNoAllocMaxDevices];
+
+// The host-side name of a __device__ array is only a stand-in, not a device
+// address, so look the real address up once per device, with that device
+// current (the first call on each device does this).
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BFP8_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return BFP8_ERR_UNSUPPORTED;
+  NoAllocSlot& slot = g_noalloc_slots[dev];
+  std::call_once(slot.once, [&slot] {
+    slot.err = cudaGetSymbolAddress(&slot.ptr, g_gemv_noalloc_scratch);
+  });
+  if (slot.err != cudaSuccess || slot.ptr == nullptr) return BFP8_ERR_CUDA;
+  *out = slot.ptr;
+  return BFP8_OK;
+}
+
+}  // namespace
+
 int gemv_read_clear_error() {
   int v = 0;
   const int zero = 0;
@@ -414,3 +453,27 @@ int gemv_read_clear_error() {
 }
 
 }  // namespace bfp8
+
+extern "C" int bfp8_gemv_decode_noalloc(const void* x_bf16, int64_t ldx, const void* w_e4m3,
+                                        const void* w_scale, int32_t w_scale_dtype, int64_t M,
+                                        int64_t N, int64_t K, void* y_bf16, int64_t ldy,
+                                        const bfp8_members* members, void* stream) {
+  using namespace bfp8;
+  if (M < 1 || M > 16 || N <= 0 || K <= 0) return BFP8_ERR_INVALID_ARG;
+  if (!x_bf16 || !w_e4m3 || !w_scale || !y_bf16 || ldy < N || ldx < K)
+    return BFP8_ERR_INVALID_ARG;
+  if (w_scale_dtype != BFP8_DT_BF16 && w_scale_dtype != BFP8_DT_F32) return BFP8_ERR_SCALE_DTYPE;
+  MemberTable mt;
+  int rc = resolve_members(N, members, &mt);
+  if (rc != BFP8_OK) return rc;
+  int sms = 0;
+  rc = sm_count(&sms);
+  if (rc != BFP8_OK) return rc;
+  if (gemv_workspace_bytes(M, N, K, sms) > BFP8_GEMV_NOALLOC_SCRATCH_BYTES)
+    return BFP8_ERR_UNSUPPORTED;  // the problem needs more scratch than the fixed array holds
+  void* scratch = nullptr;
+  rc = noalloc_scratch(&scratch);
+  if (rc != BFP8_OK) return rc;
+  return launch_gemv(x_bf16, ldx, w_e4m3, w_scale, w_scale_dtype, M, N, K, y_bf16, ldy, mt,
+                     scratch, BFP8_GEMV_NOALLOC_SCRATCH_BYTES, stream);
+}

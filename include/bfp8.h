@@ -239,6 +239,37 @@ int bfp8_gemv_decode(const void* x_bf16, int64_t ldx, const void* w_e4m3, const 
 /* Workspace bytes bfp8_gemv_decode needs on the current device (0 if none). */
 size_t bfp8_gemv_decode_workspace(int64_t M, int64_t N, int64_t K);
 
+/* ---- decode GEMV for callers that cannot allocate ------------------------- */
+/*
+ * The pages have no counterpart for this entry point. It exists for callers
+ * that cannot call cudaMalloc: code that runs under an allocator it must not
+ * bypass (a framework's memory pool, a plugin inside another process), or
+ * code that must keep device memory fixed once serving has started.
+ *
+ * bfp8_gemv_decode_noalloc computes exactly what bfp8_gemv_decode computes,
+ * with the same arguments minus the workspace. Its split-K scratch is a fixed
+ * device array of BFP8_GEMV_NOALLOC_SCRATCH_BYTES compiled into the library.
+ * Every GPU that loads libbfp8.so holds that array until the process exits.
+ *  - Limit: the problem must need at most BFP8_GEMV_NOALLOC_SCRATCH_BYTES of
+ *    scratch, i.e. bfp8_gemv_decode_workspace(M, N, K) <= 4 MiB. On a
+ *    152-SM GB300 that holds any N up to about 54 million rows. Larger
+ *    problems return BFP8_ERR_UNSUPPORTED before any GPU work.
+ *  - The first call on each device does a one-time set-up: it looks up the
+ *    array's device address with cudaGetSymbolAddress. Make that first call
+ *    before capturing any stream.
+ *  - All calls on one device share the array, and each call clears the
+ *    counters it needs on its stream before the kernel runs. Calls that
+ *    overlap on the GPU (two streams, or two host threads without ordering)
+ *    race on the array and give wrong results. Order them on one stream or
+ *    with events.
+ *  - It allocates no memory and calls no allocating routine.
+ */
+#define BFP8_GEMV_NOALLOC_SCRATCH_BYTES (4u << 20)
+int bfp8_gemv_decode_noalloc(const void* x_bf16, int64_t ldx, const void* w_e4m3,
+                             const void* w_scale, int32_t w_scale_dtype, int64_t M, int64_t N,
+                             int64_t K, void* y_bf16, int64_t ldy, const bfp8_members* members,
+                             void* stream);
+
 /* ---- a9: grouped (per-expert) W8A8 projection ---------------------------- */
 /*
  * bfp8_grouped_linear -- the MoE expert projections over a token-offset table.
