@@ -329,6 +329,126 @@ def run_decode(bfp8, torch, dev, wgu, sgu, wdn, sdn, peaks):
     return res
 
 
+# --------------------------------------------------------------------------- single-launch mode
+PROFILE_CASES = ("act_quant", "gate_up", "silu_quant", "down", "gemv_gate_up", "gemv_down",
+                 "qkv", "o_proj", "moe_gate_up", "moe_down", "w8a16_gate_up")
+
+
+def run_profile(args, local):
+    """Set up one launch of the hot path and run it warmup + steps times on its
+    own: the target for ncu captures and for per-kernel timing of the other
+    workloads (attention projections, MoE experts). Prints one JSON line with
+    the CUDA-event time per launch and the algorithmic work."""
+    import torch
+
+    from block_scaled_fp8_token_gb300 import bfp8, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    gen = synth.generator(0)
+    case = args.profile
+
+    def qweight(N, K, G=None):
+        if G is None:
+            w = synth.weight_f32(gen, N, K).to(dev)
+            q = torch.empty(N, K, dtype=torch.uint8, device=dev)
+            s = torch.empty((N + 127) // 128, (K + 127) // 128, dtype=torch.bfloat16, device=dev)
+            bfp8.bfp8_quantize_weight_block(w, q, s)
+            return q, s
+        q = torch.empty(G, N, K, dtype=torch.uint8, device=dev)
+        s = torch.empty(G, (N + 127) // 128, (K + 127) // 128, dtype=torch.bfloat16, device=dev)
+        for e in range(G):
+            w = synth.weight_f32(gen, N, K).to(dev)
+            bfp8.bfp8_quantize_weight_block(w, q[e], s[e])
+        return q, s
+
+    def qact(M, K):
+        x = synth.activations_bf16(gen, M, K).to(dev)
+        q = torch.empty(M, K, dtype=torch.uint8, device=dev)
+        s = torch.empty(M, (K + 127) // 128, dtype=torch.float32, device=dev)
+        bfp8.bfp8_act_quant_group(x, q, s)
+        return x, q, s
+
+    work, unit = 0, "TFLOP/s"
+    if case in ("act_quant", "silu_quant"):
+        K = HID if case == "act_quant" else INTER
+        width = K if case == "act_quant" else 2 * K
+        x = synth.activations_bf16(gen, M_TOK, width).to(dev)
+        q = torch.empty(M_TOK, K, dtype=torch.uint8, device=dev)
+        s = torch.empty(M_TOK, K // 128, dtype=torch.float32, device=dev)
+        fn = bfp8.bfp8_act_quant_group if case == "act_quant" else bfp8.bfp8_silu_mul_act_quant
+        launch = lambda: fn(x, q, s)
+        work, unit = M_TOK * width * 2 + M_TOK * K + 4 * M_TOK * (K // 128), "GB/s"
+    elif case in ("gate_up", "down", "w8a16_gate_up"):
+        N, K = (2 * INTER, HID) if case != "down" else (HID, INTER)
+        members = [INTER, INTER] if case != "down" else None
+        w, sw = qweight(N, K)
+        x, qa, sa = qact(M_TOK, K)
+        y = torch.empty(M_TOK, N, dtype=torch.bfloat16, device=dev)
+        if case == "w8a16_gate_up":
+            launch = lambda: bfp8.bfp8_linear_w8a16(x, w, sw, y, member_rows=members)
+        else:
+            launch = lambda: bfp8.bfp8_linear_w8a8(qa, sa, w, sw, y, member_rows=members)
+        work = 2 * M_TOK * N * K
+    elif case in ("gemv_gate_up", "gemv_down"):
+        N, K = (2 * INTER, HID) if case == "gemv_gate_up" else (HID, INTER)
+        members = [INTER, INTER] if case == "gemv_gate_up" else None
+        w, sw = qweight(N, K)
+        M = args.decode_m
+        x = synth.decode_tokens(1, M, K).to(dev)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(bfp8.bfp8_gemv_decode_workspace(M, N, K), dtype=torch.uint8, device=dev)
+        launch = lambda: bfp8.bfp8_gemv_decode(x, w, sw, y, ws, member_rows=members)
+        work, unit = N * K + sw.numel() * 2 + 2 * M * K + 2 * M * N, "GB/s"
+    elif case in ("qkv", "o_proj"):
+        c = synth.ATTENTION_PROJ
+        M = c["M"]
+        N, K = (c["q"] + c["k"] + c["v"], c["hidden"]) if case == "qkv" else (c["hidden"], c["o_in"])
+        members = [c["q"], c["k"], c["v"]] if case == "qkv" else None
+        w, sw = qweight(N, K)
+        x, qa, sa = qact(M, K)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        launch = lambda: bfp8.bfp8_linear_w8a8(qa, sa, w, sw, y, member_rows=members)
+        work = 2 * M * N * K
+    elif case in ("moe_gate_up", "moe_down"):
+        c = synth.MOE_PREFILL
+        T, E, k = c["tokens"], c["experts"], c["top_k"]
+        N, K = (2 * c["inter"], c["hidden"]) if case == "moe_gate_up" else (c["hidden"], c["inter"])
+        logits = synth.router_logits(gen, T, E).to(dev)
+        top = torch.topk(torch.softmax(logits.double(), dim=1), k, dim=1).indices.reshape(-1)
+        counts = torch.bincount(top, minlength=E)
+        offsets = torch.zeros(E + 1, dtype=torch.int32, device=dev)
+        offsets[1:] = torch.cumsum(counts, 0).to(torch.int32)
+        w, sw = qweight(N, K, G=E)
+        x, qa, sa = qact(T * k, K)
+        y = torch.empty(T * k, N, dtype=torch.bfloat16, device=dev)
+        launch = lambda: bfp8.bfp8_grouped_linear(qa, sa, w, sw, offsets, y)
+        work = 2 * T * k * N * K
+    else:
+        raise SystemExit(f"unknown profile case {case}; one of {PROFILE_CASES}")
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()   # keep only the launch's own buffers on the device
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        launch()
+        e1.record()
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    if bfp8.bfp8_device_status() != 0:
+        raise RuntimeError("device status not OK")
+    ms = statistics.median(a.elapsed_time(b) for a, b in times) if times else float("nan")
+    rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9) if times else None
+    print(json.dumps({"profile": case, "ms": round(ms, 5) if times else None,
+                      "rate": round(rate, 1) if rate else None, "unit": unit,
+                      "l2": "warm (back-to-back launches)"}), flush=True)
+
+
 # --------------------------------------------------------------------------- oracle arm
 _ORACLE_INPUTS = None
 
@@ -419,10 +539,15 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-rows", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", default=None, help="run one launch of: " + ", ".join(PROFILE_CASES))
+    ap.add_argument("--decode-m", type=int, default=16)
     args = ap.parse_args(argv)
-    if args.warmup < 3:
+    if args.warmup < 3 and not args.profile:
         args.warmup = 3
     rank, world, local = _dist()
+    if args.profile:
+        run_profile(args, local)
+        return
     if args.impl == "reference":
         out = run_reference(args, rank, world)
     else:

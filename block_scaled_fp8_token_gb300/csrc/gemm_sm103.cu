@@ -17,10 +17,13 @@
 //   warp 1      allocates TMEM. One lane issues the tcgen05.mma of each
 //               K-block into a fresh TMEM partial (two partial buffers, so
 //               the tensor cores run one K-block ahead of the promotion).
-//   warps 2-9   promotion + epilogue: tcgen05.ld the partial, acc += P * f in
-//               FP32 registers (f = s_a * s_w), then BF16 stores of the tile.
-//               Warp w reads TMEM lanes 32*(w%4)..+31 (the rows it owns) and
-//               half (w-2)/4 of the tile's columns.
+//   epilogue    eight warps (4-11 for W8A8, 2-9 for W8A16): tcgen05.ld the
+//               partial, acc += P * f in FP32 registers (f = s_a * s_w), then
+//               BF16 stores of the tile. Warp w reads TMEM lanes 32*(w%4)..+31
+//               (the rows it owns) and one half of the tile's columns. For
+//               W8A8, setmaxnreg gives these warps 224 registers (the 128x256
+//               FP32 accumulator is 128 registers per thread) and warpgroup 0
+//               56.
 //   warps 10-13 (W8A16 only) decode the raw E4M3 tile to BF16 in the
 //               canonical 128-byte-swizzled K-major layout the MMA reads.
 //
@@ -32,6 +35,8 @@
 // Every mbarrier wait is bounded. On a timeout the kernel raises a CTA-wide
 // abort flag and the device error word, drains its in-flight copies and MMAs,
 // frees TMEM and returns.
+#include <mutex>
+
 #include "bfp8_internal.h"
 #include "ptx.cuh"
 
@@ -78,8 +83,18 @@ template <int BN, int STAGES, bool W8A16, bool GROUPED>
 struct Cfg {
   static constexpr int kEpiWarps = 8;
   static constexpr int kConvWarps = W8A16 ? 4 : 0;
-  static constexpr int kWarps = 2 + kEpiWarps + kConvWarps;
+  // W8A8: warpgroup 0 = producer, MMA and two idle warps; warpgroups 1-2 =
+  // promotion/epilogue. setmaxnreg moves registers from warpgroup 0 to the
+  // epilogue, whose FP32 tile accumulator takes 128 registers per thread.
+  static constexpr bool kSplitRegs = !W8A16;
+  static constexpr int kEpiWarp0 = kSplitRegs ? 4 : 2;
+  static constexpr int kWarps = kEpiWarp0 + kEpiWarps + kConvWarps;
   static constexpr int kThreads = kWarps * 32;
+  static constexpr int kLaunchRegs = 168;      // 65536 / 384 rounded down to a multiple of 8
+  static constexpr int kCtrlRegs = 56;
+  static constexpr int kEpiRegs = 224;
+  static_assert(!kSplitRegs || kCtrlRegs * 128 + kEpiRegs * 256 == kLaunchRegs * kThreads,
+                "register split must add up to the launch allocation");
   static constexpr int kEpiCols = BN / 2;
   static constexpr uint32_t kABytes = W8A16 ? BM * BK * 2 : BM * BK;
   static constexpr uint32_t kBRawBytes = BN * BK;
@@ -253,90 +268,95 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
-  if (GROUPED && warp == 2) build_schedule(p, s_off, s_pre, lane);
+  if (GROUPED && warp == C::kEpiWarp0) build_schedule(p, s_off, s_pre, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = GROUPED ? s_pre[p.G] : p.total_tiles;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0, armed = 0, armed_phase = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        Tile tl;
-        decode_tile<BN, GROUPED>(p, s_off, s_pre, t, tl);
-        for (int kb = 0; kb < p.Kb; ++kb) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
-          const uint32_t sA = base + stage * C::kStage;
-          const uint32_t sB = sA + C::kABytes;
-          mbar_arrive_expect_tx(full_bar(stage), C::kTmaBytes);
-          if (W8A16) {
-            tma_load_2d(sA, &tmA, kb * BK, tl.a_row0, full_bar(stage));
-            tma_load_2d(sA + BM * 128, &tmA, kb * BK + 64, tl.a_row0, full_bar(stage));
-          } else {
-            tma_load_2d(sA, &tmA, kb * BK, tl.a_row0, full_bar(stage));
-          }
-          if (GROUPED)
-            tma_load_3d(sB, &tmB, kb * BK, tl.b_row0, tl.expert, full_bar(stage));
-          else
-            tma_load_2d(sB, &tmB, kb * BK, tl.b_row0, full_bar(stage));
-          armed |= 1u << stage;
-          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        }
-      }
-      if (!ok) raise_abort(abort_flag);
-      // No copy may still be landing in shared memory when the CTA exits.
-      for (int s = 0; s < STAGES; ++s)
-        if ((armed >> s) & 1u) wait_bounded(full_bar(s), (armed_phase >> s) & 1u, kDrainLimitNs);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int stage = 0, buf = 0;
-      uint32_t phase = 0, bphase = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        for (int kb = 0; kb < p.Kb; ++kb) {
-          if (!mbar_wait(tempty_bar(buf), bphase ^ 1u, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
-          if (W8A16 && !mbar_wait(conv_bar(stage), phase, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
-          const uint32_t sA = base + stage * C::kStage;
-          if (!W8A16) {
-            const uint64_t da = smem_desc_sw128(sA);
-            const uint64_t db = smem_desc_sw128(sA + C::kABytes);
-#pragma unroll
-            for (int k = 0; k < BK / 32; ++k)  // K = 32 bytes per MMA: +2 in 16-byte units
-              umma_e4m3(d, da + 2u * k, db + 2u * k, C::kIdesc, k > 0 ? 1u : 0u);
-          } else {
-            const uint32_t sConv = sA + C::kABytes + C::kBRawBytes;
-#pragma unroll
-            for (int k = 0; k < BK / 16; ++k) {  // K = 16 BF16 = 32 bytes per MMA
-              const int j = k >> 2, kk = k & 3;
-              const uint64_t da = smem_desc_sw128(sA + j * (BM * 128)) + 2u * kk;
-              const uint64_t db = smem_desc_sw128(sConv + j * (BN * 128)) + 2u * kk;
-              umma_bf16(d, da, db, C::kIdesc, k > 0 ? 1u : 0u);
+  if (warp < C::kEpiWarp0) {
+    // warpgroup 0: producer (warp 0) and MMA issuer (warp 1)
+    if constexpr (C::kSplitRegs) warpgroup_reg_dealloc<C::kCtrlRegs>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0, armed = 0, armed_phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+          Tile tl;
+          decode_tile<BN, GROUPED>(p, s_off, s_pre, t, tl);
+          for (int kb = 0; kb < p.Kb; ++kb) {
+            if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
+            const uint32_t sA = base + stage * C::kStage;
+            const uint32_t sB = sA + C::kABytes;
+            mbar_arrive_expect_tx(full_bar(stage), C::kTmaBytes);
+            if (W8A16) {
+              tma_load_2d(sA, &tmA, kb * BK, tl.a_row0, full_bar(stage));
+              tma_load_2d(sA + BM * 128, &tmA, kb * BK + 64, tl.a_row0, full_bar(stage));
+            } else {
+              tma_load_2d(sA, &tmA, kb * BK, tl.a_row0, full_bar(stage));
             }
+            if (GROUPED)
+              tma_load_3d(sB, &tmB, kb * BK, tl.b_row0, tl.expert, full_bar(stage));
+            else
+              tma_load_2d(sB, &tmB, kb * BK, tl.b_row0, full_bar(stage));
+            armed |= 1u << stage;
+            armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
-          umma_commit(empty_bar(stage));
-          umma_commit(tfull_bar(buf));
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-          if (++buf == 2) { buf = 0; bphase ^= 1u; }
         }
+        if (!ok) raise_abort(abort_flag);
+        // No copy may still be landing in shared memory when the CTA exits.
+        for (int s = 0; s < STAGES; ++s)
+          if ((armed >> s) & 1u) wait_bounded(full_bar(s), (armed_phase >> s) & 1u, kDrainLimitNs);
       }
-      if (!ok) raise_abort(abort_flag);
-      umma_commit(drain_bar);
-      wait_bounded(drain_bar, 0, kDrainLimitNs);
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        int stage = 0, buf = 0;
+        uint32_t phase = 0, bphase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+          for (int kb = 0; kb < p.Kb; ++kb) {
+            if (!mbar_wait(tempty_bar(buf), bphase ^ 1u, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
+            if (W8A16 && !mbar_wait(conv_bar(stage), phase, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
+            const uint32_t sA = base + stage * C::kStage;
+            if (!W8A16) {
+              const uint64_t da = smem_desc_sw128(sA);
+              const uint64_t db = smem_desc_sw128(sA + C::kABytes);
+  #pragma unroll
+              for (int k = 0; k < BK / 32; ++k)  // K = 32 bytes per MMA: +2 in 16-byte units
+                umma_e4m3(d, da + 2u * k, db + 2u * k, C::kIdesc, k > 0 ? 1u : 0u);
+            } else {
+              const uint32_t sConv = sA + C::kABytes + C::kBRawBytes;
+  #pragma unroll
+              for (int k = 0; k < BK / 16; ++k) {  // K = 16 BF16 = 32 bytes per MMA
+                const int j = k >> 2, kk = k & 3;
+                const uint64_t da = smem_desc_sw128(sA + j * (BM * 128)) + 2u * kk;
+                const uint64_t db = smem_desc_sw128(sConv + j * (BN * 128)) + 2u * kk;
+                umma_bf16(d, da, db, C::kIdesc, k > 0 ? 1u : 0u);
+              }
+            }
+            umma_commit(empty_bar(stage));
+            umma_commit(tfull_bar(buf));
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            if (++buf == 2) { buf = 0; bphase ^= 1u; }
+          }
+        }
+        if (!ok) raise_abort(abort_flag);
+        umma_commit(drain_bar);
+        wait_bounded(drain_bar, 0, kDrainLimitNs);
+      }
     }
-  } else if (warp < 2 + C::kEpiWarps) {
+  } else if (warp < C::kEpiWarp0 + C::kEpiWarps) {
+    if constexpr (C::kSplitRegs) warpgroup_reg_alloc<C::kEpiRegs>();
     // ------------------------------------------------------------ promotion + epilogue
-    const int ew = warp - 2;
+    const int ew = warp - C::kEpiWarp0;
     const int q = warp & 3;
     const int h = ew >> 2;
     const int row_in_tile = q * 32 + lane;
@@ -373,12 +393,22 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                static_cast<uint32_t>(buf * BN + h * C::kEpiCols);
+        if constexpr (C::kSplitRegs) {
 #pragma unroll
-        for (int c = 0; c < C::kEpiCols / 32; ++c) {
-          float v[32];
-          tmem_ld32(taddr + 32u * c, v);
+          for (int c = 0; c < C::kEpiCols / 64; ++c) {
+            float v[64];
+            tmem_ld64(taddr + 64u * c, v);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(v[j], f, acc[32 * c + j]);
+            for (int j = 0; j < 64; ++j) acc[64 * c + j] = fmaf(v[j], f, acc[64 * c + j]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < C::kEpiCols / 32; ++c) {
+            float v[32];
+            tmem_ld32(taddr + 32u * c, v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(v[j], f, acc[32 * c + j]);
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -426,7 +456,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
     if (!ok) raise_abort(abort_flag);
   } else {
     // ------------------------------------------------------------ E4M3 -> BF16 decode (W8A16)
-    const int cw = warp - 2 - C::kEpiWarps;
+    const int cw = warp - C::kEpiWarp0 - C::kEpiWarps;
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -470,6 +500,19 @@ int launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, in
            void* stream) {
   using C = Cfg<BN, STAGES, W8A16, GROUPED>;
   auto kernel = gemm_kernel<BN, STAGES, W8A16, GROUPED>;
+  if constexpr (C::kSplitRegs) {
+    // setmaxnreg.inc waits until the CTA's launch allocation can cover the
+    // request, so the split is only safe if the kernel was built with exactly
+    // kLaunchRegs registers per thread. Refuse to launch otherwise.
+    static int regs = -1;
+    static std::once_flag once;
+    std::call_once(once, [&] {
+      cudaFuncAttributes attr{};
+      if (cudaFuncGetAttributes(&attr, reinterpret_cast<const void*>(kernel)) == cudaSuccess)
+        regs = attr.numRegs;
+    });
+    if (regs != C::kLaunchRegs) return BFP8_ERR_UNSUPPORTED;
+  }
   int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel), C::kSmemBytes);
   if (rc != BFP8_OK) return rc;
   kernel<<<grid, C::kThreads, C::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(ta, tb, p);
