@@ -79,6 +79,11 @@ struct Tile {
   int32_t srow0, srow_last;  // scale row of the first 128 columns; member's last row
 };
 
+#ifndef BFP8_W8A8_CLUSTER
+#define BFP8_W8A8_CLUSTER 1
+#endif
+constexpr int kW8A8Cluster = BFP8_W8A8_CLUSTER;
+
 template <int BN, int STAGES, bool W8A16, bool GROUPED>
 struct Cfg {
   static constexpr int kEpiWarps = 8;
@@ -87,13 +92,16 @@ struct Cfg {
   // promotion/epilogue. setmaxnreg moves registers from warpgroup 0 to the
   // epilogue, whose FP32 tile accumulator takes 128 registers per thread.
   static constexpr bool kSplitRegs = !W8A16;
+  // W8A8 runs in 2-CTA clusters on adjacent M tiles: each CTA loads its own A
+  // tile and half of the shared B tile, multicast to both CTAs.
+  static constexpr int kCluster = W8A16 ? 1 : kW8A8Cluster;
   static constexpr int kEpiWarp0 = kSplitRegs ? 4 : 2;
   static constexpr int kWarps = kEpiWarp0 + kEpiWarps + kConvWarps;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kLaunchRegs = 168;      // 65536 / 384 rounded down to a multiple of 8
-  static constexpr int kCtrlRegs = 56;
-  static constexpr int kEpiRegs = 224;
-  static_assert(!kSplitRegs || kCtrlRegs * 128 + kEpiRegs * 256 == kLaunchRegs * kThreads,
+  static constexpr int kCtrlRegs = 64;
+  static constexpr int kEpiRegs = 216;
+  static_assert(!kSplitRegs || kCtrlRegs * 128 + kEpiRegs * 256 <= kLaunchRegs * kThreads,
                 "register split must add up to the launch allocation");
   static constexpr int kEpiCols = BN / 2;
   static constexpr uint32_t kABytes = W8A16 ? BM * BK * 2 : BM * BK;
@@ -103,10 +111,13 @@ struct Cfg {
   static constexpr uint32_t kTmaBytes = kABytes + kBRawBytes;
   static constexpr uint32_t kStgPitch = 80;  // 32 BF16 (64 B) + 16 B pad per row
   static constexpr uint32_t kStgWarp = 32 * kStgPitch;
-  static constexpr uint32_t kTmemCols = 2 * BN;
+  // TMEM (512 columns) holds 512/BN partial buffers, so the tensor cores run
+  // up to that many K-blocks minus one ahead of the promotion.
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kNumBufs = 512 / BN;
   static constexpr uint32_t kOffStg = STAGES * kStage;
   static constexpr uint32_t kOffBar = kOffStg + kEpiWarps * kStgWarp;
-  static constexpr uint32_t kNumBars = 3 * STAGES + 5;
+  static constexpr uint32_t kNumBars = 3 * STAGES + 2 * kNumBufs + 1;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffOff = kOffMisc + 16;
   static constexpr uint32_t kOffPre = kOffOff + (kMaxExperts + 1) * 4;
@@ -114,16 +125,20 @@ struct Cfg {
   static constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // 1024-byte alignment slack
   static constexpr uint32_t kIdesc = W8A16 ? idesc_bf16(BM, BN) : idesc_e4m3(BM, BN);
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of two");
+  static_assert(kNumBufs >= 2 && kNumBufs * BN == 512, "TMEM partial buffers must tile 512 columns");
   static_assert(kEpiCols % 32 == 0, "epilogue columns come in 32-column TMEM loads");
 };
 
-template <int BN, bool GROUPED>
+// Work item t covers CL adjacent M tiles (one per CTA of the cluster) of one
+// N tile; `rank` picks this CTA's M tile. A rank past the last M tile gets
+// m_valid <= 0: it still loads and multicasts its share of B, but stores nothing.
+template <int BN, int CL, bool GROUPED>
 __device__ __forceinline__ void decode_tile(const GemmParams& p, const int* s_off,
-                                            const int* s_pre, int t, Tile& tl) {
+                                            const int* s_pre, int t, int rank, Tile& tl) {
   if (!GROUPED) {
-    const int nt = t / p.m_tiles;
-    const int mt = t - nt * p.m_tiles;
+    const int m_units = (p.m_tiles + CL - 1) / CL;
+    const int nt = t / m_units;
+    const int mt = (t - nt * m_units) * CL + rank;
     int i = 0;
 #pragma unroll 1
     while (i + 1 < p.n_members && nt >= p.mem_tile0[i + 1]) ++i;
@@ -146,10 +161,10 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, const int* s_of
     const int e = lo;
     const int row0 = s_off[e];
     const int rows = s_off[e + 1] - row0;
-    const int mte = (rows + BM - 1) / BM;
+    const int units = ((rows + BM - 1) / BM + CL - 1) / CL;
     const int local = t - s_pre[e];
-    const int nt = local / mte;
-    const int mt = local - nt * mte;
+    const int nt = local / units;
+    const int mt = (local - nt * units) * CL + rank;
     tl.a_row0 = row0 + mt * BM;
     tl.m_valid = min(BM, rows - mt * BM);
     tl.b_row0 = nt * BN;
@@ -162,7 +177,9 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, const int* s_of
 }
 
 // Grouped schedule, built by one warp: clamp the offsets into [0, M], make
-// them non-decreasing, then prefix-sum the tiles of every expert.
+// them non-decreasing, then prefix-sum the work items (CL M tiles x one N tile)
+// of every expert.
+template <int CL>
 __device__ void build_schedule(const GemmParams& p, int* s_off, int* s_pre, int lane) {
   const int n = p.G + 1;
   const int per = (n + 31) / 32;
@@ -187,7 +204,8 @@ __device__ void build_schedule(const GemmParams& p, int* s_off, int* s_pre, int 
   const int per2 = (p.G + 31) / 32;
   const int b2 = min(p.G, lane * per2), e2 = min(p.G, b2 + per2);
   int sum = 0;
-  for (int i = b2; i < e2; ++i) sum += ((s_off[i + 1] - s_off[i] + BM - 1) / BM) * p.n_tiles;
+  for (int i = b2; i < e2; ++i)
+    sum += (((s_off[i + 1] - s_off[i] + BM - 1) / BM + CL - 1) / CL) * p.n_tiles;
   int incl2 = sum;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -197,7 +215,7 @@ __device__ void build_schedule(const GemmParams& p, int* s_off, int* s_pre, int 
   int run2 = incl2 - sum;
   for (int i = b2; i < e2; ++i) {
     s_pre[i] = run2;
-    run2 += ((s_off[i + 1] - s_off[i] + BM - 1) / BM) * p.n_tiles;
+    run2 += (((s_off[i + 1] - s_off[i] + BM - 1) / BM + CL - 1) / CL) * p.n_tiles;
   }
   if (lane == 31) s_pre[p.G] = incl2;
   __syncwarp();
@@ -233,14 +251,18 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
   uint8_t* const base_ptr = smem_raw + (base - raw_u32);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  constexpr int CL = C::kCluster;
+  const int rank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int cid = blockIdx.x / CL;     // cluster index (CTAs of a cluster are consecutive)
+  const int ncl = gridDim.x / CL;
 
   const uint32_t bar0 = base + C::kOffBar;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
   auto conv_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
   auto tfull_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + b); };
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (3 * STAGES + 4);
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + C::kNumBufs + b); };
+  const uint32_t drain_bar = bar0 + 8u * (3 * STAGES + 2 * C::kNumBufs);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::kOffMisc + 4);
   int* s_off = reinterpret_cast<int*>(base_ptr + C::kOffOff);
@@ -249,10 +271,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), CL);  // released by the MMA of every CTA that reads the stage
       mbar_init(conv_bar(s), W8A16 ? C::kConvWarps : 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::kNumBufs; ++b) {
       mbar_init(tfull_bar(b), 1);
       mbar_init(tempty_bar(b), C::kEpiWarps);
     }
@@ -268,9 +290,12 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
-  if (GROUPED && warp == C::kEpiWarp0) build_schedule(p, s_off, s_pre, lane);
+  if (GROUPED && warp == C::kEpiWarp0) build_schedule<CL>(p, s_off, s_pre, lane);
   tc_fence_before();
   __syncthreads();
+  // The peer CTA multicasts into this CTA's shared memory and arrives on its
+  // barriers: both must be initialised before either CTA issues anything.
+  if constexpr (CL > 1) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = GROUPED ? s_pre[p.G] : p.total_tiles;
@@ -284,9 +309,9 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
         int stage = 0;
         uint32_t phase = 0, armed = 0, armed_phase = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int t = cid; t < total && ok; t += ncl) {
           Tile tl;
-          decode_tile<BN, GROUPED>(p, s_off, s_pre, t, tl);
+          decode_tile<BN, CL, GROUPED>(p, s_off, s_pre, t, rank, tl);
           for (int kb = 0; kb < p.Kb; ++kb) {
             if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
             const uint32_t sA = base + stage * C::kStage;
@@ -298,10 +323,19 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
             } else {
               tma_load_2d(sA, &tmA, kb * BK, tl.a_row0, full_bar(stage));
             }
-            if (GROUPED)
+            if constexpr (CL > 1) {
+              // this CTA's half of the B tile, into the same offset of both CTAs
+              const uint32_t half = static_cast<uint32_t>(rank) * (BN / CL) * 128u;
+              const int brow = tl.b_row0 + rank * (BN / CL);
+              if (GROUPED)
+                tma_load_3d_mc(sB + half, &tmB, kb * BK, brow, tl.expert, full_bar(stage), 0x3);
+              else
+                tma_load_2d_mc(sB + half, &tmB, kb * BK, brow, full_bar(stage), 0x3);
+            } else if (GROUPED) {
               tma_load_3d(sB, &tmB, kb * BK, tl.b_row0, tl.expert, full_bar(stage));
-            else
+            } else {
               tma_load_2d(sB, &tmB, kb * BK, tl.b_row0, full_bar(stage));
+            }
             armed |= 1u << stage;
             armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -318,7 +352,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
         int stage = 0, buf = 0;
         uint32_t phase = 0, bphase = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int t = cid; t < total && ok; t += ncl) {
           for (int kb = 0; kb < p.Kb; ++kb) {
             if (!mbar_wait(tempty_bar(buf), bphase ^ 1u, abort_flag)) { ok = false; break; }
             if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
@@ -342,10 +376,13 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
                 umma_bf16(d, da, db, C::kIdesc, k > 0 ? 1u : 0u);
               }
             }
-            umma_commit(empty_bar(stage));
+            if constexpr (CL > 1)
+              umma_commit_mc(empty_bar(stage), 0x3);  // frees the stage in both CTAs
+            else
+              umma_commit(empty_bar(stage));
             umma_commit(tfull_bar(buf));
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-            if (++buf == 2) { buf = 0; bphase ^= 1u; }
+            if (++buf == C::kNumBufs) { buf = 0; bphase ^= 1u; }
           }
         }
         if (!ok) raise_abort(abort_flag);
@@ -366,9 +403,9 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
     int buf = 0;
     uint32_t bphase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    for (int t = cid; t < total && ok; t += ncl) {
       Tile tl;
-      decode_tile<BN, GROUPED>(p, s_off, s_pre, t, tl);
+      decode_tile<BN, CL, GROUPED>(p, s_off, s_pre, t, rank, tl);
       const bool row_ok = row_in_tile < tl.m_valid;
       const int64_t arow = static_cast<int64_t>(tl.a_row0) + row_in_tile;
       const int srow = min(tl.srow0 + (h * C::kEpiCols) / 128, tl.srow_last);
@@ -381,12 +418,14 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
         const float sa = row_ok ? __ldg(sa_row + kb * p.sa_skb) : 0.0f;
         return sa * sw;
       };
-      float acc[C::kEpiCols];
+      // FP32 accumulator pairs: the promotion runs as packed FP32x2 FMAs
+      float2 acc[C::kEpiCols / 2];
 #pragma unroll
-      for (int i = 0; i < C::kEpiCols; ++i) acc[i] = 0.0f;
+      for (int i = 0; i < C::kEpiCols / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
       float f_next = factor(0);
       for (int kb = 0; kb < p.Kb; ++kb) {
         const float f = f_next;
+        const float2 f2 = make_float2(f, f);
         if (kb + 1 < p.Kb) f_next = factor(kb + 1);
         const bool w_ok = mbar_wait(tfull_bar(buf), bphase, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
@@ -394,26 +433,33 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                static_cast<uint32_t>(buf * BN + h * C::kEpiCols);
         if constexpr (C::kSplitRegs) {
+          // 64-column single-instruction loads (fewer tcgen05 instructions per
+          // K-block than 32-column ones), then packed FP32x2 FMAs.
 #pragma unroll
           for (int c = 0; c < C::kEpiCols / 64; ++c) {
             float v[64];
             tmem_ld64(taddr + 64u * c, v);
 #pragma unroll
-            for (int j = 0; j < 64; ++j) acc[64 * c + j] = fmaf(v[j], f, acc[64 * c + j]);
+            for (int j = 0; j < 32; ++j)
+              acc[32 * c + j] = __ffma2_rn(make_float2(v[2 * j], v[2 * j + 1]), f2, acc[32 * c + j]);
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(buf));
         } else {
 #pragma unroll
           for (int c = 0; c < C::kEpiCols / 32; ++c) {
             float v[32];
             tmem_ld32(taddr + 32u * c, v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(v[j], f, acc[32 * c + j]);
+            for (int j = 0; j < 16; ++j)
+              acc[16 * c + j] = __ffma2_rn(make_float2(v[2 * j], v[2 * j + 1]), f2, acc[16 * c + j]);
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(buf));
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar(buf));
-        if (++buf == 2) { buf = 0; bphase ^= 1u; }
+        if (++buf == C::kNumBufs) { buf = 0; bphase ^= 1u; }
       }
       if (!ok) break;
       // BF16 tile store: stage 32 rows x 32 columns through shared memory so
@@ -423,10 +469,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint4 v;
-          v.x = pack_bf16x2(acc[32 * ps + 8 * i + 0], acc[32 * ps + 8 * i + 1]);
-          v.y = pack_bf16x2(acc[32 * ps + 8 * i + 2], acc[32 * ps + 8 * i + 3]);
-          v.z = pack_bf16x2(acc[32 * ps + 8 * i + 4], acc[32 * ps + 8 * i + 5]);
-          v.w = pack_bf16x2(acc[32 * ps + 8 * i + 6], acc[32 * ps + 8 * i + 7]);
+          v.x = pack_bf16x2(acc[16 * ps + 4 * i + 0].x, acc[16 * ps + 4 * i + 0].y);
+          v.y = pack_bf16x2(acc[16 * ps + 4 * i + 1].x, acc[16 * ps + 4 * i + 1].y);
+          v.z = pack_bf16x2(acc[16 * ps + 4 * i + 2].x, acc[16 * ps + 4 * i + 2].y);
+          v.w = pack_bf16x2(acc[16 * ps + 4 * i + 3].x, acc[16 * ps + 4 * i + 3].y);
           sts128(stg + lane * C::kStgPitch + 16u * i, v);
         }
         __syncwarp();
@@ -460,7 +506,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    for (int t = cid; t < total && ok; t += ncl) {
       for (int kb = 0; kb < p.Kb; ++kb) {
         const bool w_ok = mbar_wait(full_bar(stage), phase, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
@@ -489,6 +535,8 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
   }
 
   __syncthreads();
+  // No CTA may exit while its peer can still arrive on its barriers.
+  if constexpr (CL > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
@@ -496,7 +544,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
 }
 
 template <int BN, int STAGES, bool W8A16, bool GROUPED>
-int launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int grid,
+int launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int work_items,
            void* stream) {
   using C = Cfg<BN, STAGES, W8A16, GROUPED>;
   auto kernel = gemm_kernel<BN, STAGES, W8A16, GROUPED>;
@@ -515,14 +563,32 @@ int launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, in
   }
   int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel), C::kSmemBytes);
   if (rc != BFP8_OK) return rc;
-  kernel<<<grid, C::kThreads, C::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(ta, tb, p);
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C::kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // persistent: at most as many clusters as can be resident at once
+  int max_clusters = 0;
+  cfg.gridDim = dim3(C::kCluster);
+  if (cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg) != cudaSuccess || max_clusters < 1)
+    return BFP8_ERR_CUDA;
+  const int clusters = work_items < max_clusters ? work_items : max_clusters;
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * C::kCluster));
+  if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, p) != cudaSuccess) return BFP8_ERR_CUDA;
   return check_launch();
 }
 
 bool aligned16(const void* ptr) { return reinterpret_cast<uintptr_t>(ptr) % 16 == 0; }
 
-int fill_members(GemmParams& p, const MemberTable& mt, int bn, int64_t M, const void* y,
-                 int64_t ldy) {
+int fill_members(GemmParams& p, const MemberTable& mt, int bn, int cluster, int64_t M,
+                 const void* y, int64_t ldy) {
   p.n_members = mt.count;
   int tiles = 0;
   bool vec = aligned16(y) && (ldy % 8 == 0);
@@ -536,7 +602,8 @@ int fill_members(GemmParams& p, const MemberTable& mt, int bn, int64_t M, const 
   }
   p.mem_tile0[mt.count] = tiles;
   p.m_tiles = static_cast<int32_t>((M + BM - 1) / BM);
-  const int64_t total = static_cast<int64_t>(p.m_tiles) * tiles;
+  const int64_t m_units = (p.m_tiles + cluster - 1) / cluster;
+  const int64_t total = m_units * tiles;
   if (total > 0x7FFFFFFF) return BFP8_ERR_UNSUPPORTED;
   p.total_tiles = static_cast<int32_t>(total);
   p.vec_store = vec ? 1 : 0;
@@ -557,14 +624,13 @@ int launch_gemm_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t s
   if (K % 16 != 0 || !aligned16(q_a) || !aligned16(w)) return BFP8_ERR_UNSUPPORTED;
   if (!fits_i32(M) || !fits_i32(N) || !fits_i32(K)) return BFP8_ERR_UNSUPPORTED;
   if (sa_sm < 0 || sa_skb < 0) return BFP8_ERR_INVALID_ARG;
-  int sms = 0;
-  int rc = sm_count(&sms);
-  if (rc != BFP8_OK) return rc;
+  using C8 = Cfg<kBN8, kStages8, false, false>;
   CUtensorMap ta, tb;
-  rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_a, K, M, K, BK, BM,
-                    CU_TENSOR_MAP_SWIZZLE_128B);
+  int rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_a, K, M, K, BK, BM,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != BFP8_OK) return rc;
-  rc = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, K, BK, kBN8,
+  // each CTA of a cluster loads (and multicasts) its share of the B tile rows
+  rc = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, K, BK, kBN8 / C8::kCluster,
                     CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != BFP8_OK) return rc;
   GemmParams p{};
@@ -578,10 +644,9 @@ int launch_gemm_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t s
   p.sw_f32 = w_scale_dtype == BFP8_DT_F32;
   p.y = static_cast<__nv_bfloat16*>(y);
   p.ldy = ldy;
-  rc = fill_members(p, mt, kBN8, M, y, ldy);
+  rc = fill_members(p, mt, kBN8, C8::kCluster, M, y, ldy);
   if (rc != BFP8_OK) return rc;
-  const int grid = p.total_tiles < sms ? p.total_tiles : sms;
-  return launch<kBN8, kStages8, false, false>(ta, tb, p, grid, stream);
+  return launch<kBN8, kStages8, false, false>(ta, tb, p, p.total_tiles, stream);
 }
 
 int launch_gemm_w8a16(const void* x, int64_t ldx, const void* w, const void* w_scale,
@@ -589,11 +654,8 @@ int launch_gemm_w8a16(const void* x, int64_t ldx, const void* w, const void* w_s
                       int64_t ldy, const MemberTable& mt, void* stream) {
   if (K % 16 != 0 || ldx % 8 != 0 || !aligned16(x) || !aligned16(w)) return BFP8_ERR_UNSUPPORTED;
   if (!fits_i32(M) || !fits_i32(N) || !fits_i32(K)) return BFP8_ERR_UNSUPPORTED;
-  int sms = 0;
-  int rc = sm_count(&sms);
-  if (rc != BFP8_OK) return rc;
   CUtensorMap ta, tb;
-  rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, ldx * 2, 64, BM,
+  int rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, ldx * 2, 64, BM,
                     CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != BFP8_OK) return rc;
   rc = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, K, BK, kBN16,
@@ -608,10 +670,9 @@ int launch_gemm_w8a16(const void* x, int64_t ldx, const void* w, const void* w_s
   p.sw_f32 = w_scale_dtype == BFP8_DT_F32;
   p.y = static_cast<__nv_bfloat16*>(y);
   p.ldy = ldy;
-  rc = fill_members(p, mt, kBN16, M, y, ldy);
+  rc = fill_members(p, mt, kBN16, Cfg<kBN16, kStages16, true, false>::kCluster, M, y, ldy);
   if (rc != BFP8_OK) return rc;
-  const int grid = p.total_tiles < sms ? p.total_tiles : sms;
-  return launch<kBN16, kStages16, true, false>(ta, tb, p, grid, stream);
+  return launch<kBN16, kStages16, true, false>(ta, tb, p, p.total_tiles, stream);
 }
 
 int launch_grouped_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
@@ -622,15 +683,13 @@ int launch_grouped_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_
   if (!fits_i32(total_M) || !fits_i32(N) || !fits_i32(K)) return BFP8_ERR_UNSUPPORTED;
   if (G < 1 || G > kMaxExperts) return BFP8_ERR_INVALID_ARG;
   if (sa_sm < 0 || sa_skb < 0) return BFP8_ERR_INVALID_ARG;
-  int sms = 0;
-  int rc = sm_count(&sms);
-  if (rc != BFP8_OK) return rc;
+  using CG = Cfg<kBN8, kStages8, false, true>;
   CUtensorMap ta, tb;
-  rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_a, K, total_M, K, BK, BM,
-                    CU_TENSOR_MAP_SWIZZLE_128B);
+  int rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_a, K, total_M, K, BK, BM,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != BFP8_OK) return rc;
-  rc = make_tmap_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, G, K, N * K, BK, kBN8, 1,
-                    CU_TENSOR_MAP_SWIZZLE_128B);
+  rc = make_tmap_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, G, K, N * K, BK,
+                    kBN8 / CG::kCluster, 1, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != BFP8_OK) return rc;
   GemmParams p{};
   p.M = static_cast<int32_t>(total_M);
@@ -650,7 +709,8 @@ int launch_grouped_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_
   p.N = static_cast<int32_t>(N);
   p.n_tiles = static_cast<int32_t>((N + kBN8 - 1) / kBN8);
   p.n_members = 1;
-  return launch<kBN8, kStages8, false, true>(ta, tb, p, sms, stream);
+  // the work-item count is only known on the device: launch every resident cluster
+  return launch<kBN8, kStages8, false, true>(ta, tb, p, 0x7FFFFFFF, stream);
 }
 
 int gemm_read_clear_error() {
