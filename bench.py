@@ -174,6 +174,10 @@ def run_ours(args, rank, world, local):
     y_host = torch.empty(M_TOK, HID, dtype=torch.bfloat16).pin_memory()
     stream = torch.cuda.current_stream(dev)
     members = [INTER, INTER]
+    ws_gu = torch.empty(bfp8.bfp8_linear_w8a8_workspace(M_TOK, 2 * INTER, HID, members),
+                        dtype=torch.uint8, device=dev)
+    ws_dn = torch.empty(bfp8.bfp8_linear_w8a8_workspace(M_TOK, HID, INTER), dtype=torch.uint8,
+                        device=dev)
     gu_events = []
 
     def step(xin, record=False):
@@ -182,12 +186,13 @@ def run_ours(args, rank, world, local):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-        bfp8.bfp8_linear_w8a8(qa, sa, wgu, sgu, gu, member_rows=members, stream=stream)
+        bfp8.bfp8_linear_w8a8(qa, sa, wgu, sgu, gu, member_rows=members, workspace=ws_gu,
+                              stream=stream)
         if record:
             e1.record(stream)
             gu_events.append((e0, e1))
         bfp8.bfp8_silu_mul_act_quant(gu, qh, sh, stream=stream)
-        bfp8.bfp8_linear_w8a8(qh, sh, wdn, sdn, y, stream=stream)
+        bfp8.bfp8_linear_w8a8(qh, sh, wdn, sdn, y, workspace=ws_dn, stream=stream)
 
     launches_per_step = 4
     for _ in range(args.warmup):
@@ -388,7 +393,10 @@ def run_profile(args, local):
         if case == "w8a16_gate_up":
             launch = lambda: bfp8.bfp8_linear_w8a16(x, w, sw, y, member_rows=members)
         else:
-            launch = lambda: bfp8.bfp8_linear_w8a8(qa, sa, w, sw, y, member_rows=members)
+            ws = torch.empty(bfp8.bfp8_linear_w8a8_workspace(M_TOK, N, K, members),
+                             dtype=torch.uint8, device=dev)
+            launch = lambda: bfp8.bfp8_linear_w8a8(qa, sa, w, sw, y, member_rows=members,
+                                                   workspace=ws)
         work = 2 * M_TOK * N * K
     elif case in ("gemv_gate_up", "gemv_down"):
         N, K = (2 * INTER, HID) if case == "gemv_gate_up" else (HID, INTER)
@@ -408,7 +416,9 @@ def run_profile(args, local):
         w, sw = qweight(N, K)
         x, qa, sa = qact(M, K)
         y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-        launch = lambda: bfp8.bfp8_linear_w8a8(qa, sa, w, sw, y, member_rows=members)
+        ws = torch.empty(bfp8.bfp8_linear_w8a8_workspace(M, N, K, members), dtype=torch.uint8,
+                         device=dev)
+        launch = lambda: bfp8.bfp8_linear_w8a8(qa, sa, w, sw, y, member_rows=members, workspace=ws)
         work = 2 * M * N * K
     elif case in ("moe_gate_up", "moe_down"):
         c = synth.MOE_PREFILL
@@ -422,7 +432,9 @@ def run_profile(args, local):
         w, sw = qweight(N, K, G=E)
         x, qa, sa = qact(T * k, K)
         y = torch.empty(T * k, N, dtype=torch.bfloat16, device=dev)
-        launch = lambda: bfp8.bfp8_grouped_linear(qa, sa, w, sw, offsets, y)
+        ws = torch.empty(bfp8.bfp8_grouped_linear_workspace(T * k, E, N, K), dtype=torch.uint8,
+                         device=dev)
+        launch = lambda: bfp8.bfp8_grouped_linear(qa, sa, w, sw, offsets, y, workspace=ws)
         work = 2 * T * k * N * K
     else:
         raise SystemExit(f"unknown profile case {case}; one of {PROFILE_CASES}")

@@ -71,7 +71,8 @@ _SIGS = {
     "bfp8_silu_mul_act_quant": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _vp]),
     "bfp8_quantize_weight_block": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i32, _vp]),
     "bfp8_linear_w8a8": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i32, _i64, _i64, _i64,
-                                        _vp, _i64, ctypes.POINTER(bfp8_members), _vp]),
+                                        _vp, _i64, ctypes.POINTER(bfp8_members), _vp, _sz, _vp]),
+    "bfp8_linear_w8a8_workspace": (_sz, [_i64, _i64, _i64, ctypes.POINTER(bfp8_members)]),
     "bfp8_linear_w8a16": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _i64,
                                          ctypes.POINTER(bfp8_members), _vp]),
     "bfp8_gemv_decode": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _i64,
@@ -80,7 +81,8 @@ _SIGS = {
     "bfp8_gemv_decode_noalloc": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _i64, _i64, _i64, _vp,
                                                 _i64, ctypes.POINTER(bfp8_members), _vp]),
     "bfp8_grouped_linear": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i32, _vp, _i32, _i64,
-                                           _i64, _i64, _vp, _i64, _vp]),
+                                           _i64, _i64, _vp, _i64, _vp, _sz, _vp]),
+    "bfp8_grouped_linear_workspace": (_sz, [_i64, _i32, _i64, _i64]),
     "bfp8_device_status": (ctypes.c_int, [_vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -194,16 +196,28 @@ def bfp8_quantize_weight_block(w, q, scale, stream=None) -> None:
            "bfp8_quantize_weight_block")
 
 
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+
+def bfp8_linear_w8a8_workspace(M: int, N: int, K: int, member_rows=None) -> int:
+    mref, _keep = _members(member_rows)
+    return int(_lib.bfp8_linear_w8a8_workspace(M, N, K, mref))
+
+
 def bfp8_linear_w8a8(q_a, s_a, w, w_scale, y, member_rows=None, s_stride_m=None,
-                     s_stride_kb=None, stream=None) -> None:
+                     s_stride_kb=None, workspace=None, stream=None) -> None:
     M, K = q_a.shape
     N = w.shape[0]
     ssm = s_a.stride(0) if s_stride_m is None else s_stride_m
     sskb = s_a.stride(1) if s_stride_kb is None else s_stride_kb
     mref, _keep = _members(member_rows)
+    wsp, wsb = _ws(workspace)
     _check(_lib.bfp8_linear_w8a8(_ptr(q_a), _ptr(s_a), ssm, sskb, _ptr(w), _ptr(w_scale),
                                  _scale_dtype(w_scale), M, N, K, _ptr(y), y.stride(0), mref,
-                                 _stream(stream)),
+                                 wsp, wsb, _stream(stream)),
            "bfp8_linear_w8a8")
 
 
@@ -244,15 +258,20 @@ def bfp8_gemv_decode_noalloc(x, w, w_scale, y, member_rows=None, stream=None) ->
            "bfp8_gemv_decode_noalloc")
 
 
+def bfp8_grouped_linear_workspace(total_M: int, G: int, N: int, K: int) -> int:
+    return int(_lib.bfp8_grouped_linear_workspace(total_M, G, N, K))
+
+
 def bfp8_grouped_linear(q_a, s_a, w, w_scale, offsets, y, s_stride_m=None, s_stride_kb=None,
-                        stream=None) -> None:
+                        workspace=None, stream=None) -> None:
     T, K = q_a.shape
     G, N = w.shape[0], w.shape[1]
     ssm = s_a.stride(0) if s_stride_m is None else s_stride_m
     sskb = s_a.stride(1) if s_stride_kb is None else s_stride_kb
+    wsp, wsb = _ws(workspace)
     _check(_lib.bfp8_grouped_linear(_ptr(q_a), _ptr(s_a), ssm, sskb, _ptr(w), _ptr(w_scale),
                                     _scale_dtype(w_scale), _ptr(offsets), G, T, N, K, _ptr(y),
-                                    y.stride(0), _stream(stream)),
+                                    y.stride(0), wsp, wsb, _stream(stream)),
            "bfp8_grouped_linear")
 
 

@@ -285,10 +285,20 @@ int bfp8_quantize_weight_block(const float* w, int64_t N, int64_t K, int64_t ldw
   return launch_weight_quant(w, N, K, ldw, q, ldq, scale, scale_dtype, stream);
 }
 
+size_t bfp8_linear_w8a8_workspace(int64_t M, int64_t N, int64_t K, const bfp8_members* members) {
+  (void)K;
+  if (M <= 0 || N <= 0) return 0;
+  MemberTable mt;
+  int sms = 0;
+  if (resolve_members(N, members, &mt) != BFP8_OK || sm_count(&sms) != BFP8_OK) return 0;
+  return gemm_w8a8_workspace_bytes(M, N, mt, sms);
+}
+
 int bfp8_linear_w8a8(const void* q_a, const float* s_a, int64_t s_stride_m, int64_t s_stride_kb,
                      const void* w_e4m3, const void* w_scale, int32_t w_scale_dtype, int64_t M,
                      int64_t N, int64_t K, void* y_bf16, int64_t ldy,
-                     const bfp8_members* members, void* stream) {
+                     const bfp8_members* members, void* workspace, size_t ws_bytes,
+                     void* stream) {
   if (M < 0 || N <= 0 || K <= 0) return BFP8_ERR_INVALID_ARG;
   if (M == 0) return BFP8_OK;
   if (!q_a || !s_a || !w_e4m3 || !w_scale || !y_bf16 || ldy < N) return BFP8_ERR_INVALID_ARG;
@@ -297,7 +307,7 @@ int bfp8_linear_w8a8(const void* q_a, const float* s_a, int64_t s_stride_m, int6
   int rc = resolve_members(N, members, &mt);
   if (rc != BFP8_OK) return rc;
   return launch_gemm_w8a8(q_a, s_a, s_stride_m, s_stride_kb, w_e4m3, w_scale, w_scale_dtype, M,
-                          N, K, y_bf16, ldy, mt, stream);
+                          N, K, y_bf16, ldy, mt, workspace, ws_bytes, stream);
 }
 
 int bfp8_linear_w8a16(const void* x_bf16, int64_t ldx, const void* w_e4m3, const void* w_scale,
@@ -336,18 +346,26 @@ int bfp8_gemv_decode(const void* x_bf16, int64_t ldx, const void* w_e4m3, const 
                      workspace, ws_bytes, stream);
 }
 
+size_t bfp8_grouped_linear_workspace(int64_t total_M, int32_t G, int64_t N, int64_t K) {
+  (void)K;
+  int sms = 0;
+  if (total_M <= 0 || G < 1 || N <= 0 || sm_count(&sms) != BFP8_OK) return 0;
+  return grouped_w8a8_workspace_bytes(total_M, G, N, sms);
+}
+
 int bfp8_grouped_linear(const void* q_a, const float* s_a, int64_t s_stride_m,
                         int64_t s_stride_kb, const void* w_e4m3, const void* w_scale,
                         int32_t w_scale_dtype, const int32_t* offsets_dev, int32_t G,
                         int64_t total_M, int64_t N, int64_t K, void* y_bf16, int64_t ldy,
-                        void* stream) {
+                        void* workspace, size_t ws_bytes, void* stream) {
   if (G < 1 || G > 1024 || total_M < 0 || N <= 0 || K <= 0) return BFP8_ERR_INVALID_ARG;
   if (total_M == 0) return BFP8_OK;
   if (!q_a || !s_a || !w_e4m3 || !w_scale || !offsets_dev || !y_bf16 || ldy < N)
     return BFP8_ERR_INVALID_ARG;
   if (w_scale_dtype != BFP8_DT_BF16 && w_scale_dtype != BFP8_DT_F32) return BFP8_ERR_SCALE_DTYPE;
   return launch_grouped_w8a8(q_a, s_a, s_stride_m, s_stride_kb, w_e4m3, w_scale, w_scale_dtype,
-                             offsets_dev, G, total_M, N, K, y_bf16, ldy, stream);
+                             offsets_dev, G, total_M, N, K, y_bf16, ldy, workspace, ws_bytes,
+                             stream);
 }
 
 int bfp8_device_status(void* stream) {

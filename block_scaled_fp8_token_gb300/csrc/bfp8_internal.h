@@ -45,17 +45,20 @@ int launch_silu_mul_act_quant(const void* gu, int64_t M, int64_t I, int64_t ld, 
 int launch_weight_quant(const float* w, int64_t N, int64_t K, int64_t ldw, void* q, int64_t ldq,
                         void* scale, int32_t scale_dtype, void* stream);
 
+size_t gemm_w8a8_workspace_bytes(int64_t M, int64_t N, const MemberTable& mt, int sms);
+size_t grouped_w8a8_workspace_bytes(int64_t total_M, int32_t G, int64_t N, int sms);
 int launch_gemm_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
                      const void* w, const void* w_scale, int32_t w_scale_dtype, int64_t M,
                      int64_t N, int64_t K, void* y, int64_t ldy, const MemberTable& mt,
-                     void* stream);
+                     void* workspace, size_t ws_bytes, void* stream);
 int launch_gemm_w8a16(const void* x, int64_t ldx, const void* w, const void* w_scale,
                       int32_t w_scale_dtype, int64_t M, int64_t N, int64_t K, void* y,
                       int64_t ldy, const MemberTable& mt, void* stream);
 int launch_grouped_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
                         const void* w, const void* w_scale, int32_t w_scale_dtype,
                         const int32_t* offsets, int32_t G, int64_t total_M, int64_t N,
-                        int64_t K, void* y, int64_t ldy, void* stream);
+                        int64_t K, void* y, int64_t ldy, void* workspace, size_t ws_bytes,
+                        void* stream);
 
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K, int sms);
 int launch_gemv(const void* x, int64_t ldx, const void* w, const void* w_scale,

@@ -70,7 +70,68 @@ struct GemmParams {
   // grouped mode
   const int32_t* offsets;
   int32_t G, N, n_tiles;
+  // stream-K: split tiles exchange FP32 partials through a caller workspace
+  int32_t stream_k;
+  int32_t* ws_counters;   // one arrival counter per tile, zero on entry
+  float* ws_partials;     // [CTAs][2][BM][BN] FP32 partial tiles
 };
+
+// Work partition over G CTAs. Whole tiles: CTA c takes tiles c, c + G, ...,
+// so the CTAs running at the same time work on neighbouring tiles and share
+// weight tiles through L2. With stream-K, all but the last one-to-two waves are
+// still whole tiles in that order. The K-block units of the remaining tiles are
+// cut into G equal contiguous ranges, one per CTA, so the last wave leaves no
+// SM idle, and each of those tiles has only two or three contributors.
+// Work is walked as segments: runs of K-blocks inside one tile.
+struct SegIter {
+  int64_t u, ue;   // stream-K part: next unit, end of this CTA's range (absolute units)
+  int t, t_end, step;  // whole-tile part: next tile, end, stride
+};
+struct SkSplit {
+  int dp_tiles;    // tiles handed out whole
+  int64_t U0;      // first stream-K unit (dp_tiles * Kb)
+  int64_t U;       // stream-K units
+};
+BFP8_DEV SkSplit sk_split(bool sk, int total, int Kb, int G) {
+  SkSplit s;
+  const int waves = total / G;
+  s.dp_tiles = sk ? (waves > 1 ? (waves - 1) * G : 0) : total;
+  s.U0 = static_cast<int64_t>(s.dp_tiles) * Kb;
+  s.U = static_cast<int64_t>(total - s.dp_tiles) * Kb;
+  return s;
+}
+BFP8_DEV int64_t sk_unit_begin(int64_t U, int G, int64_t c) { return (c * U) / G; }
+// The CTA whose range holds unit u.
+BFP8_DEV int64_t sk_cta_of_unit(int64_t U, int G, int64_t u) { return ((u + 1) * G + U - 1) / U - 1; }
+
+BFP8_DEV SegIter seg_begin(bool sk, int total, int Kb, int cid, int ncl) {
+  const SkSplit sp = sk_split(sk, total, Kb, ncl);
+  SegIter it;
+  it.t = cid;
+  it.t_end = sp.dp_tiles;
+  it.step = ncl;
+  it.u = sk ? sp.U0 + sk_unit_begin(sp.U, ncl, cid) : 0;
+  it.ue = sk ? sp.U0 + sk_unit_begin(sp.U, ncl, cid + 1) : 0;
+  return it;
+}
+BFP8_DEV bool next_seg(bool sk, SegIter& it, int total, int Kb, int& t, int& kb0, int& kb1) {
+  (void)sk;
+  (void)total;
+  if (it.t < it.t_end) {
+    t = it.t;
+    kb0 = 0;
+    kb1 = Kb;
+    it.t += it.step;
+    return true;
+  }
+  if (it.u >= it.ue) return false;
+  t = static_cast<int>(it.u / Kb);
+  kb0 = static_cast<int>(it.u - static_cast<int64_t>(t) * Kb);
+  const int64_t left = it.ue - it.u;
+  kb1 = left < Kb - kb0 ? kb0 + static_cast<int>(left) : Kb;
+  it.u += kb1 - kb0;
+  return true;
+}
 
 struct Tile {
   int32_t a_row0, m_valid;   // first A / output row, rows valid from it
@@ -119,7 +180,7 @@ struct Cfg {
   static constexpr uint32_t kOffBar = kOffStg + kEpiWarps * kStgWarp;
   static constexpr uint32_t kNumBars = 3 * STAGES + 2 * kNumBufs + 1;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr uint32_t kOffOff = kOffMisc + 16;
+  static constexpr uint32_t kOffOff = kOffMisc + 16;  // misc: TMEM slot, abort flag, last-arriver flag
   static constexpr uint32_t kOffPre = kOffOff + (kMaxExperts + 1) * 4;
   static constexpr uint32_t kSmemUsed = GROUPED ? kOffPre + (kMaxExperts + 1) * 4 : kOffOff;
   static constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // 1024-byte alignment slack
@@ -265,6 +326,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
   const uint32_t drain_bar = bar0 + 8u * (3 * STAGES + 2 * C::kNumBufs);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::kOffMisc + 4);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(base_ptr + C::kOffMisc + 8);
   int* s_off = reinterpret_cast<int*>(base_ptr + C::kOffOff);
   int* s_pre = reinterpret_cast<int*>(base_ptr + C::kOffPre);
 
@@ -299,6 +361,13 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = GROUPED ? s_pre[p.G] : p.total_tiles;
+  // Stream-K only pays when whole-tile waves would leave the last wave mostly
+  // empty (partial tiles cost an FP32 round trip through L2 and a fixup); it
+  // also needs every CTA to own at least one K-block unit of the split part.
+  const int waves = (total + ncl - 1) / ncl;
+  const bool sparse_tail = waves > 0 && 5 * total < 4 * waves * ncl;   // fill < 80%
+  const bool sk = CL == 1 && p.stream_k && sparse_tail &&
+                  sk_split(true, total, p.Kb, ncl).U >= static_cast<int64_t>(ncl);
 
   if (warp < C::kEpiWarp0) {
     // warpgroup 0: producer (warp 0) and MMA issuer (warp 1)
@@ -309,10 +378,12 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
         int stage = 0;
         uint32_t phase = 0, armed = 0, armed_phase = 0;
         bool ok = true;
-        for (int t = cid; t < total && ok; t += ncl) {
+        SegIter it = seg_begin(sk, total, p.Kb, cid, ncl);
+        int t, kb0, kb1;
+        while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
           Tile tl;
           decode_tile<BN, CL, GROUPED>(p, s_off, s_pre, t, rank, tl);
-          for (int kb = 0; kb < p.Kb; ++kb) {
+          for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
             const uint32_t sA = base + stage * C::kStage;
             const uint32_t sB = sA + C::kABytes;
@@ -352,8 +423,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
         int stage = 0, buf = 0;
         uint32_t phase = 0, bphase = 0;
         bool ok = true;
-        for (int t = cid; t < total && ok; t += ncl) {
-          for (int kb = 0; kb < p.Kb; ++kb) {
+        SegIter it = seg_begin(sk, total, p.Kb, cid, ncl);
+        int t, kb0, kb1;
+        while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
+          for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(tempty_bar(buf), bphase ^ 1u, abort_flag)) { ok = false; break; }
             if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
             if (W8A16 && !mbar_wait(conv_bar(stage), phase, abort_flag)) { ok = false; break; }
@@ -403,7 +476,11 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
     int buf = 0;
     uint32_t bphase = 0;
     bool ok = true;
-    for (int t = cid; t < total && ok; t += ncl) {
+    // Every epilogue warp walks every segment, even after a failed wait, so
+    // that all of them reach the same named barriers (those cannot time out).
+    SegIter it = seg_begin(sk, total, p.Kb, cid, ncl);
+    int t, kb0, kb1;
+    while (next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
       Tile tl;
       decode_tile<BN, CL, GROUPED>(p, s_off, s_pre, t, rank, tl);
       const bool row_ok = row_in_tile < tl.m_valid;
@@ -422,11 +499,11 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
       float2 acc[C::kEpiCols / 2];
 #pragma unroll
       for (int i = 0; i < C::kEpiCols / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
-      float f_next = factor(0);
-      for (int kb = 0; kb < p.Kb; ++kb) {
+      float f_next = factor(kb0);
+      for (int kb = kb0; kb < kb1 && ok; ++kb) {
         const float f = f_next;
         const float2 f2 = make_float2(f, f);
-        if (kb + 1 < p.Kb) f_next = factor(kb + 1);
+        if (kb + 1 < kb1) f_next = factor(kb + 1);
         const bool w_ok = mbar_wait(tfull_bar(buf), bphase, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
         tc_fence_after();
@@ -461,7 +538,57 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
         }
         if (++buf == C::kNumBufs) { buf = 0; bphase ^= 1u; }
       }
-      if (!ok) break;
+      if (kb0 != 0 || kb1 != p.Kb) {
+        // Split tile: publish this CTA's FP32 partial. The last contributor to
+        // arrive sums every contributor's partial in CTA order (deterministic)
+        // and stores the tile; nobody waits for anybody.
+        const SkSplit sp = sk_split(true, total, p.Kb, ncl);
+        const int64_t U = sp.U;
+        const int64_t tile_u0 = static_cast<int64_t>(t) * p.Kb - sp.U0;  // within the split part
+        const int slot = (tile_u0 + kb0 == sk_unit_begin(U, ncl, cid)) ? 0 : 1;
+        float4* mine = reinterpret_cast<float4*>(
+            p.ws_partials + ((static_cast<int64_t>(cid) * 2 + slot) * BM + row_in_tile) * BN +
+            h * C::kEpiCols);
+        if (ok) {
+#pragma unroll
+          for (int i = 0; i < C::kEpiCols / 4; ++i)
+            __stcg(mine + i, make_float4(acc[2 * i].x, acc[2 * i].y, acc[2 * i + 1].x, acc[2 * i + 1].y));
+        }
+        __threadfence();
+        named_bar_sync(1, 32 * C::kEpiWarps);
+        const int64_t c_first = sk_cta_of_unit(U, ncl, tile_u0);
+        const int64_t c_last = sk_cta_of_unit(U, ncl, tile_u0 + p.Kb - 1);
+        if (ew == 0 && lane == 0) {
+          int last_arrival = 0;
+          if (ok && !*abort_flag) {
+            const int old = atomicAdd(p.ws_counters + t, 1);
+            last_arrival = (old == static_cast<int>(c_last - c_first)) ? 1 : 0;
+          }
+          *last_flag = last_arrival;
+        }
+        named_bar_sync(1, 32 * C::kEpiWarps);
+        const bool last = *last_flag != 0;
+        named_bar_sync(1, 32 * C::kEpiWarps);  // the flag is read before the next segment rewrites it
+        if (!last) continue;
+        __threadfence();
+#pragma unroll
+        for (int i = 0; i < C::kEpiCols / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
+        for (int64_t c = c_first; c <= c_last; ++c) {
+          const int sl = (sk_unit_begin(U, ncl, c) >= tile_u0) ? 0 : 1;
+          const float4* src = reinterpret_cast<const float4*>(
+              p.ws_partials + ((c * 2 + sl) * BM + row_in_tile) * BN + h * C::kEpiCols);
+#pragma unroll
+          for (int i = 0; i < C::kEpiCols / 4; ++i) {
+            const float4 v = __ldcg(src + i);
+            acc[2 * i].x += v.x;
+            acc[2 * i].y += v.y;
+            acc[2 * i + 1].x += v.z;
+            acc[2 * i + 1].y += v.w;
+          }
+        }
+        if (ew == 0 && lane == 0) p.ws_counters[t] = 0;  // leave the workspace clean
+      }
+      if (!ok) continue;
       // BF16 tile store: stage 32 rows x 32 columns through shared memory so
       // that global stores are row-contiguous 64-byte segments.
 #pragma unroll
@@ -506,8 +633,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int t = cid; t < total && ok; t += ncl) {
-      for (int kb = 0; kb < p.Kb; ++kb) {
+    SegIter it = seg_begin(sk, total, p.Kb, cid, ncl);
+    int t, kb0, kb1;
+    while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         const bool w_ok = mbar_wait(full_bar(stage), phase, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
         const uint32_t sRaw = base + stage * C::kStage + C::kABytes;
@@ -579,7 +708,9 @@ int launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, in
   cfg.gridDim = dim3(C::kCluster);
   if (cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg) != cudaSuccess || max_clusters < 1)
     return BFP8_ERR_CUDA;
-  const int clusters = work_items < max_clusters ? work_items : max_clusters;
+  int64_t items = work_items;
+  if (p.stream_k) items = static_cast<int64_t>(work_items) * p.Kb;  // stream-K splits by K-block units
+  const int clusters = items < max_clusters ? static_cast<int>(items) : max_clusters;
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * C::kCluster));
   if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, p) != cudaSuccess) return BFP8_ERR_CUDA;
   return check_launch();
@@ -612,15 +743,61 @@ int fill_members(GemmParams& p, const MemberTable& mt, int bn, int cluster, int6
 
 bool fits_i32(int64_t v) { return v >= 0 && v <= 0x7FFFFFFF; }
 
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+// Stream-K workspace: [tile counters][CTAs x 2 FP32 partial tiles].
+size_t sk_workspace_bytes(int64_t tiles, int sms, int bn) {
+  return align256(static_cast<size_t>(tiles) * 4) +
+         static_cast<size_t>(sms) * 2 * BM * bn * sizeof(float);
+}
+
+// Enables stream-K when the caller's workspace is large enough; the tile
+// counters are cleared on the stream first (the kernel also leaves them clear).
+int sk_setup(GemmParams& p, int64_t tiles, int bn, void* ws, size_t ws_bytes, void* stream) {
+  p.stream_k = 0;
+  if (!ws) return BFP8_OK;
+  int sms = 0;
+  int rc = sm_count(&sms);
+  if (rc != BFP8_OK) return rc;
+  if (ws_bytes < sk_workspace_bytes(tiles, sms, bn) || reinterpret_cast<uintptr_t>(ws) % 256 != 0)
+    return BFP8_ERR_INVALID_ARG;
+  p.stream_k = 1;
+  p.ws_counters = static_cast<int32_t*>(ws);
+  p.ws_partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
+                                           align256(static_cast<size_t>(tiles) * 4));
+  if (cudaMemsetAsync(ws, 0, static_cast<size_t>(tiles) * 4, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return BFP8_ERR_CUDA;
+  return BFP8_OK;
+}
+
+int64_t member_tiles(const MemberTable& mt, int bn) {
+  int64_t tiles = 0;
+  for (int i = 0; i < mt.count; ++i) tiles += (mt.rows[i] + bn - 1) / bn;
+  return tiles;
+}
+
 }  // namespace
 
 constexpr int kBN8 = 256, kStages8 = 4;
 constexpr int kBN16 = 128, kStages16 = 2;
 
+size_t gemm_w8a8_workspace_bytes(int64_t M, int64_t N, const MemberTable& mt, int sms) {
+  (void)N;
+  const int64_t m_tiles = (M + BM - 1) / BM;
+  return sk_workspace_bytes(m_tiles * member_tiles(mt, kBN8), sms, kBN8);
+}
+
+size_t grouped_w8a8_workspace_bytes(int64_t total_M, int32_t G, int64_t N, int sms) {
+  // an upper bound on the device-built tile count: sum_e ceil(M_e/128) <= total_M/128 + G
+  const int64_t tiles = ((total_M + BM - 1) / BM + G) * ((N + kBN8 - 1) / kBN8);
+  return sk_workspace_bytes(tiles, sms, kBN8);
+}
+
 int launch_gemm_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
                      const void* w, const void* w_scale, int32_t w_scale_dtype, int64_t M,
                      int64_t N, int64_t K, void* y, int64_t ldy, const MemberTable& mt,
-                     void* stream) {
+                     void* workspace, size_t ws_bytes, void* stream) {
   if (K % 16 != 0 || !aligned16(q_a) || !aligned16(w)) return BFP8_ERR_UNSUPPORTED;
   if (!fits_i32(M) || !fits_i32(N) || !fits_i32(K)) return BFP8_ERR_UNSUPPORTED;
   if (sa_sm < 0 || sa_skb < 0) return BFP8_ERR_INVALID_ARG;
@@ -646,6 +823,10 @@ int launch_gemm_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t s
   p.ldy = ldy;
   rc = fill_members(p, mt, kBN8, C8::kCluster, M, y, ldy);
   if (rc != BFP8_OK) return rc;
+  if (C8::kCluster == 1) {
+    rc = sk_setup(p, p.total_tiles, kBN8, workspace, ws_bytes, stream);
+    if (rc != BFP8_OK) return rc;
+  }
   return launch<kBN8, kStages8, false, false>(ta, tb, p, p.total_tiles, stream);
 }
 
@@ -678,7 +859,8 @@ int launch_gemm_w8a16(const void* x, int64_t ldx, const void* w, const void* w_s
 int launch_grouped_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
                         const void* w, const void* w_scale, int32_t w_scale_dtype,
                         const int32_t* offsets, int32_t G, int64_t total_M, int64_t N,
-                        int64_t K, void* y, int64_t ldy, void* stream) {
+                        int64_t K, void* y, int64_t ldy, void* workspace, size_t ws_bytes,
+                        void* stream) {
   if (K % 16 != 0 || !aligned16(q_a) || !aligned16(w)) return BFP8_ERR_UNSUPPORTED;
   if (!fits_i32(total_M) || !fits_i32(N) || !fits_i32(K)) return BFP8_ERR_UNSUPPORTED;
   if (G < 1 || G > kMaxExperts) return BFP8_ERR_INVALID_ARG;
@@ -709,6 +891,11 @@ int launch_grouped_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_
   p.N = static_cast<int32_t>(N);
   p.n_tiles = static_cast<int32_t>((N + kBN8 - 1) / kBN8);
   p.n_members = 1;
+  if (CG::kCluster == 1) {
+    const int64_t tile_bound = ((total_M + BM - 1) / BM + G) * p.n_tiles;
+    rc = sk_setup(p, tile_bound, kBN8, workspace, ws_bytes, stream);
+    if (rc != BFP8_OK) return rc;
+  }
   // the work-item count is only known on the device: launch every resident cluster
   return launch<kBN8, kStages8, false, true>(ta, tb, p, 0x7FFFFFFF, stream);
 }

@@ -5,9 +5,9 @@
 //   * the same, fused behind SiLU(gate)*up (the dense-FFN gate/up/down arm);
 //   * ahead-of-time 128x128 weight block quantization (a conversion endpoint
 //     [th#1803 decoder PR: quantization is ahead of time, never at load]).
-// One warp owns one (token, 128-column group). Each lane holds 4 consecutive
-// elements, the group maximum is a 5-step shuffle reduction, and the scale is
-// max(amax, 1e-10f) / 448.0f with IEEE division. Codes come from
+// Half a warp owns one (token, 128-column group). Each lane holds 8
+// consecutive elements, the group maximum is a 4-step shuffle reduction, and
+// the scale is max(amax, 1e-10f) / 448.0f with IEEE division. Codes come from
 // cvt.rn.satfinite.e4m3x2.f32 applied to x / s (IEEE division, not a reciprocal
 // multiply), which makes the result bit-exact against the CPU definition.
 #include "bfp8_internal.h"
@@ -28,6 +28,43 @@ __device__ __forceinline__ float silu_mul_bf16_round(float g, float u) {
 // SILU == false: x is [M, K] with row stride ld; values are x[m, c].
 // SILU == true : x is [M, 2K] with row stride ld; values are
 //                bf16(silu(x[m, c]) * x[m, K + c]).
+// A half-warp owns one (token, 128-column group): each lane holds 8 consecutive
+// elements (one 16-byte load), the group maximum is a 4-step shuffle within the
+// half-warp, and each half-warp keeps kUnroll groups in flight.
+constexpr int kUnroll = 2;
+
+template <bool SILU>
+__device__ __forceinline__ void load8(const __nv_bfloat16* row, int64_t c, int64_t K, bool vec,
+                                      float (&v)[8]) {
+  if (vec && c + 8 <= K) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(row + c);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = bf16_bits_to_f32(static_cast<uint16_t>(w[i] & 0xFFFFu));
+      v[2 * i + 1] = bf16_bits_to_f32(static_cast<uint16_t>(w[i] >> 16));
+    }
+    if (SILU) {
+      const uint4 ru = *reinterpret_cast<const uint4*>(row + K + c);
+      const uint32_t u[4] = {ru.x, ru.y, ru.z, ru.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[2 * i] = silu_mul_bf16_round(v[2 * i], bf16_bits_to_f32(static_cast<uint16_t>(u[i] & 0xFFFFu)));
+        v[2 * i + 1] = silu_mul_bf16_round(v[2 * i + 1], bf16_bits_to_f32(static_cast<uint16_t>(u[i] >> 16)));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[i] = 0.0f;
+      if (c + i < K) {
+        v[i] = __bfloat162float(row[c + i]);
+        if (SILU) v[i] = silu_mul_bf16_round(v[i], __bfloat162float(row[K + c + i]));
+      }
+    }
+  }
+}
+
 template <bool SILU>
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K, int64_t ld,
@@ -36,54 +73,51 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(
   const int64_t Kb = (K + 127) / 128;
   const int64_t total = M * Kb;
   const int lane = threadIdx.x & 31;
-  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t item = warp0; item < total; item += nwarps) {
-    const int64_t m = item / Kb;
-    const int64_t g = item - m * Kb;
-    const int64_t c = g * 128 + lane * 4;
-    const __nv_bfloat16* row = x + m * ld;
-    float v[4];
-    if (c + 4 <= K && vec_in) {
-      const uint2 raw = *reinterpret_cast<const uint2*>(row + c);
-      v[0] = bf16_bits_to_f32(static_cast<uint16_t>(raw.x & 0xFFFFu));
-      v[1] = bf16_bits_to_f32(static_cast<uint16_t>(raw.x >> 16));
-      v[2] = bf16_bits_to_f32(static_cast<uint16_t>(raw.y & 0xFFFFu));
-      v[3] = bf16_bits_to_f32(static_cast<uint16_t>(raw.y >> 16));
-      if (SILU) {
-        const uint2 ru = *reinterpret_cast<const uint2*>(row + K + c);
-        v[0] = silu_mul_bf16_round(v[0], bf16_bits_to_f32(static_cast<uint16_t>(ru.x & 0xFFFFu)));
-        v[1] = silu_mul_bf16_round(v[1], bf16_bits_to_f32(static_cast<uint16_t>(ru.x >> 16)));
-        v[2] = silu_mul_bf16_round(v[2], bf16_bits_to_f32(static_cast<uint16_t>(ru.y & 0xFFFFu)));
-        v[3] = silu_mul_bf16_round(v[3], bf16_bits_to_f32(static_cast<uint16_t>(ru.y >> 16)));
-      }
-    } else {
+  const int hl = lane & 15;                      // lane within the half-warp
+  const int64_t hw0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
+  const int64_t nhw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 4;
+  for (int64_t base = hw0; base < total; base += nhw * kUnroll) {
+    float v[kUnroll][8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[i] = 0.0f;
-        if (c + i < K) {
-          v[i] = __bfloat162float(row[c + i]);
-          if (SILU) v[i] = silu_mul_bf16_round(v[i], __bfloat162float(row[K + c + i]));
-        }
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t item = base + u * nhw;
+      if (item < total) {
+        const int64_t m = item / Kb, g = item - m * Kb;
+        load8<SILU>(x + m * ld, g * 128 + hl * 8, K, vec_in, v[u]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[u][i] = 0.0f;
       }
     }
-    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const float sc = fmaxf(amax, 1e-10f) / 448.0f;
-    const uint16_t p01 = f32x2_to_e4m3x2(v[0] / sc, v[1] / sc);
-    const uint16_t p23 = f32x2_to_e4m3x2(v[2] / sc, v[3] / sc);
-    uint8_t* qrow = q + m * ldq;
-    if (c + 4 <= K && vec_out) {
-      *reinterpret_cast<uint32_t*>(qrow + c) = static_cast<uint32_t>(p01) | (static_cast<uint32_t>(p23) << 16);
-    } else {
-      const uint8_t b[4] = {static_cast<uint8_t>(p01 & 0xFF), static_cast<uint8_t>(p01 >> 8),
-                            static_cast<uint8_t>(p23 & 0xFF), static_cast<uint8_t>(p23 >> 8)};
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t item = base + u * nhw;
+      float amax = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (c + i < K) qrow[c + i] = b[i];
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[u][i]));
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      if (item >= total) continue;
+      const float sc = fmaxf(amax, 1e-10f) / 448.0f;
+      const int64_t m = item / Kb, g = item - m * Kb;
+      const int64_t c = g * 128 + hl * 8;
+      uint32_t w[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint16_t lo = f32x2_to_e4m3x2(v[u][4 * i] / sc, v[u][4 * i + 1] / sc);
+        const uint16_t hi = f32x2_to_e4m3x2(v[u][4 * i + 2] / sc, v[u][4 * i + 3] / sc);
+        w[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+      }
+      uint8_t* qrow = q + m * ldq;
+      if (vec_out && c + 8 <= K) {
+        *reinterpret_cast<uint2*>(qrow + c) = make_uint2(w[0], w[1]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (c + i < K) qrow[c + i] = static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
+      }
+      if (hl == 0) s[m * ssm + g * sskb] = sc;
     }
-    if (lane == 0) s[m * ssm + g * sskb] = sc;
   }
 }
 
@@ -159,11 +193,12 @@ int act_quant_common(bool silu, const void* x, int64_t M, int64_t K, int64_t ld,
   int sms = 0;
   int rc = sm_count(&sms);
   if (rc != BFP8_OK) return rc;
-  const int vec_in = (reinterpret_cast<uintptr_t>(x) % 8 == 0) && (ld % 4 == 0) && (K % 4 == 0);
-  const int vec_out = (reinterpret_cast<uintptr_t>(q) % 4 == 0) && (ldq % 4 == 0);
+  const int vec_in = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (ld % 8 == 0) && (K % 8 == 0);
+  const int vec_out = (reinterpret_cast<uintptr_t>(q) % 8 == 0) && (ldq % 8 == 0);
   const int64_t items = M * Kb;
-  const int64_t want = (items + (kThreads / 32) - 1) / (kThreads / 32);
-  const int64_t cap = static_cast<int64_t>(sms) * 16;
+  const int64_t per_block = (kThreads / 16) * kUnroll;   // groups one block covers per pass
+  const int64_t want = (items + per_block - 1) / per_block;
+  const int64_t cap = static_cast<int64_t>(sms) * 8;
   const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (silu)

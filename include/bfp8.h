@@ -175,6 +175,10 @@ typedef struct {
 } bfp8_members;
 
 /* ---- a3-a5, a8: W8A8 block-scaled projection (tcgen05 / TMEM) ----------- */
+/* Workspace bytes that let bfp8_linear_w8a8 split tiles along K (stream-K)
+ * on the current device; 0 on bad arguments. */
+size_t bfp8_linear_w8a8_workspace(int64_t M, int64_t N, int64_t K, const bfp8_members* members);
+
 /*
  * bfp8_linear_w8a8 -- y = dequant(q_a) . dequant(W)^T.
  *   [Module w8a8_prefill, arithmetic paragraph: per-token 1x128 activation
@@ -191,13 +195,22 @@ typedef struct {
  *   w_scale  [sum_i ceil(N_i/128), ceil(K/128)] row-major, w_scale_dtype BF16 or F32
  *   y_bf16   [M, N] BF16, row stride ldy >= N (elements)
  *   members  member table (host), NULL for one member
+ *   workspace, ws_bytes  optional device scratch, caller-owned and 256-byte
+ *            aligned. With at least bfp8_linear_w8a8_workspace() bytes, the
+ *            kernel balances work by cutting the (tiles x K-blocks) work into
+ *            equal ranges per SM (stream-K). Split tiles exchange FP32
+ *            partials here, and the last CTA sums them in a fixed order, so
+ *            the result is deterministic. NULL (or too small) means whole
+ *            tiles per SM. The call clears the tile counters it uses; two
+ *            calls that share a workspace must not overlap on the GPU.
  * Requirements: K % 16 == 0 (TMA row pitch); q_a, w_e4m3 16-byte aligned;
  * y_bf16 16-byte aligned and ldy % 8 == 0. M == 0 is a no-op.
  */
 int bfp8_linear_w8a8(const void* q_a, const float* s_a, int64_t s_stride_m, int64_t s_stride_kb,
                      const void* w_e4m3, const void* w_scale, int32_t w_scale_dtype,
                      int64_t M, int64_t N, int64_t K, void* y_bf16, int64_t ldy,
-                     const bfp8_members* members, void* stream);
+                     const bfp8_members* members, void* workspace, size_t ws_bytes,
+                     void* stream);
 
 /* ---- a6: W8A16 block-scaled projection ---------------------------------- */
 /*
@@ -288,12 +301,17 @@ int bfp8_gemv_decode_noalloc(const void* x_bf16, int64_t ldx, const void* w_e4m3
  *              values outside [0, total_M] and never reads or writes outside
  *              the tensors.
  *   y_bf16     [total_M, N] BF16, row stride ldy
+ *   workspace, ws_bytes  optional stream-K scratch, as bfp8_linear_w8a8, sized
+ *              by bfp8_grouped_linear_workspace() (an upper bound, because
+ *              the tile count is only known on the device)
  * Requirements: 1 <= G <= 1024; K % 16 == 0; alignments as bfp8_linear_w8a8.
  */
+size_t bfp8_grouped_linear_workspace(int64_t total_M, int32_t G, int64_t N, int64_t K);
 int bfp8_grouped_linear(const void* q_a, const float* s_a, int64_t s_stride_m, int64_t s_stride_kb,
                         const void* w_e4m3, const void* w_scale, int32_t w_scale_dtype,
                         const int32_t* offsets_dev, int32_t G, int64_t total_M, int64_t N,
-                        int64_t K, void* y_bf16, int64_t ldy, void* stream);
+                        int64_t K, void* y_bf16, int64_t ldy, void* workspace, size_t ws_bytes,
+                        void* stream);
 
 /* ---- diagnostics ---------------------------------------------------------- */
 /*

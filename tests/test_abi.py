@@ -53,14 +53,14 @@ def test_argument_errors_without_gpu(bfp8):
     # negative sizes / null pointers are refused before any CUDA call
     assert lib.bfp8_act_quant_group(None, -1, 4, 4, None, 4, None, 1, 1, None) == inval
     assert lib.bfp8_act_quant_group(None, 0, 4, 4, None, 4, None, 1, 1, None) == 0   # empty: no-op
-    assert lib.bfp8_linear_w8a8(None, None, 1, 1, None, None, 3, 4, 8, 16, None, 8, None, None) == inval
-    assert lib.bfp8_linear_w8a8(None, None, 1, 1, None, None, 3, 0, 8, 16, None, 8, None, None) == 0
+    assert lib.bfp8_linear_w8a8(None, None, 1, 1, None, None, 3, 4, 8, 16, None, 8, None, None, 0, None) == inval
+    assert lib.bfp8_linear_w8a8(None, None, 1, 1, None, None, 3, 0, 8, 16, None, 8, None, None, 0, None) == 0
     assert lib.bfp8_gemv_decode(None, 16, None, None, 3, 17, 8, 16, None, 8, None, None, 0, None) == inval
-    assert lib.bfp8_grouped_linear(None, None, 1, 1, None, None, 3, None, 0, 8, 8, 16, None, 8, None) == inval
+    assert lib.bfp8_grouped_linear(None, None, 1, 1, None, None, 3, None, 0, 8, 8, 16, None, 8, None, 0, None) == inval
     # a weight-scale dtype other than BF16/F32 is refused by name
     p = ctypes.c_void_p(16)
-    assert lib.bfp8_linear_w8a8(p, p, 1, 1, p, p, 4, 4, 8, 16, p, 8, None, None) == 8
+    assert lib.bfp8_linear_w8a8(p, p, 1, 1, p, p, 4, 4, 8, 16, p, 8, None, None, 0, None) == 8
     # members that do not partition N
     rows = (ctypes.c_int64 * 2)(3, 3)
     mem = bfp8.bfp8_members(2, rows)
-    assert lib.bfp8_linear_w8a8(p, p, 1, 1, p, p, 3, 4, 8, 16, p, 8, ctypes.byref(mem), None) == 11
+    assert lib.bfp8_linear_w8a8(p, p, 1, 1, p, p, 3, 4, 8, 16, p, 8, ctypes.byref(mem), None, 0, None) == 11

@@ -29,10 +29,12 @@ def test_dense_ffn_chain(bfp8, cuda_device):
     qh = torch.empty(M, I, dtype=torch.uint8, device=dev)
     sh = torch.empty(M, I // 128, dtype=torch.float32, device=dev)
     y = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    ws1 = torch.empty(bfp8.bfp8_linear_w8a8_workspace(M, 2 * I, H, [I, I]), dtype=torch.uint8, device=dev)
+    ws2 = torch.empty(bfp8.bfp8_linear_w8a8_workspace(M, H, I), dtype=torch.uint8, device=dev)
     bfp8.bfp8_act_quant_group(x, qa, sa)
-    bfp8.bfp8_linear_w8a8(qa, sa, wgu, swgu, gu, member_rows=[I, I])
+    bfp8.bfp8_linear_w8a8(qa, sa, wgu, swgu, gu, member_rows=[I, I], workspace=ws1)
     bfp8.bfp8_silu_mul_act_quant(gu, qh, sh)
-    bfp8.bfp8_linear_w8a8(qh, sh, wd, swd, y)
+    bfp8.bfp8_linear_w8a8(qh, sh, wd, swd, y, workspace=ws2)
     torch.cuda.synchronize()
     assert bfp8.bfp8_device_status() == 0
 

@@ -22,9 +22,13 @@ from oracle import quant as Q
 pytestmark = pytest.mark.gpu
 
 
-def _w8a8(bfp8, dev, qa, sa, q, s, members=None, mn_major=False, ldy_pad=0):
+def _w8a8(bfp8, dev, qa, sa, q, s, members=None, mn_major=False, ldy_pad=0, stream_k=True):
     M, K = qa.shape
     N = q.shape[0]
+    ws = None
+    if stream_k:
+        ws = torch.empty(bfp8.bfp8_linear_w8a8_workspace(M, N, K, members), dtype=torch.uint8,
+                         device=dev)
     a = to_dev_u8(qa, dev)
     if mn_major:
         sa_d = torch.from_numpy(np.ascontiguousarray(sa.T)).to(dev)
@@ -35,7 +39,7 @@ def _w8a8(bfp8, dev, qa, sa, q, s, members=None, mn_major=False, ldy_pad=0):
     ybuf = torch.full((M, N + ldy_pad), -7.0, dtype=torch.bfloat16, device=dev)
     y = ybuf[:, :N]
     bfp8.bfp8_linear_w8a8(a, sa_d, to_dev_u8(q, dev), scale_to_dev(s, dev), y,
-                          member_rows=members, **sa_kw)
+                          member_rows=members, workspace=ws, **sa_kw)
     torch.cuda.synchronize()
     assert bfp8.bfp8_device_status() == 0
     if ldy_pad:
@@ -73,13 +77,34 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("stream_k", [True, False], ids=["stream_k", "whole_tiles"])
 @pytest.mark.parametrize("M,N,K,members,sdt", SMALL)
-def test_w8a8_small(bfp8, cuda_device, M, N, K, members, sdt):
+def test_w8a8_small(bfp8, cuda_device, M, N, K, members, sdt, stream_k):
     xb, q, s = _problem(M * 31 + N * 7 + K, M, N, K, members, sdt)
     qa, sa = Q.act_quant_group(xb)
-    y = _w8a8(bfp8, cuda_device, qa, sa, q, s, members)
+    y = _w8a8(bfp8, cuda_device, qa, sa, q, s, members, stream_k=stream_k)
     ref = L.linear_w8a8(qa, sa, q, s, members)
     assert_close(gpu_bf16_to_f64(y), ref, f"w8a8 {M}x{N}x{K}")
+
+
+def test_w8a8_stream_k_deterministic(bfp8, cuda_device):
+    """Split tiles are summed in a fixed order: repeated calls give identical bytes,
+    and the workspace counters come back clean for the next call."""
+    xb, q, s = _problem(77, 300, 1024, 4096)
+    qa, sa = Q.act_quant_group(xb)
+    dev = cuda_device
+    a, sad = to_dev_u8(qa, dev), torch.from_numpy(sa).to(dev)
+    w, swd = to_dev_u8(q, dev), scale_to_dev(s, dev)
+    ws = torch.empty(bfp8.bfp8_linear_w8a8_workspace(300, 1024, 4096), dtype=torch.uint8, device=dev)
+    ys = []
+    for _ in range(3):
+        y = torch.empty(300, 1024, dtype=torch.bfloat16, device=dev)
+        bfp8.bfp8_linear_w8a8(a, sad, w, swd, y, workspace=ws)
+        ys.append(y)
+    torch.cuda.synchronize()
+    assert torch.equal(ys[0].view(torch.int16), ys[1].view(torch.int16))
+    assert torch.equal(ys[0].view(torch.int16), ys[2].view(torch.int16))
+    assert_close(gpu_bf16_to_f64(ys[0]), L.linear_w8a8(qa, sa, q, s), "stream-K")
 
 
 def test_w8a8_mn_major_scales_and_padded_output(bfp8, cuda_device):

@@ -19,13 +19,17 @@ from oracle import quant as Q
 pytestmark = pytest.mark.gpu
 
 
-def _grouped(bfp8, dev, qa, sa, qw, sw, offsets):
-    T = qa.shape[0]
-    N = qw.shape[1]
+def _grouped(bfp8, dev, qa, sa, qw, sw, offsets, stream_k=True):
+    T, K = qa.shape
+    G, N = qw.shape[0], qw.shape[1]
     y = torch.full((T, N), float("nan"), dtype=torch.bfloat16, device=dev)
     off = torch.from_numpy(np.asarray(offsets, dtype=np.int32)).to(dev)
+    ws = None
+    if stream_k:
+        ws = torch.empty(bfp8.bfp8_grouped_linear_workspace(T, G, N, K), dtype=torch.uint8,
+                         device=dev)
     bfp8.bfp8_grouped_linear(to_dev_u8(qa, dev), torch.from_numpy(sa).to(dev), to_dev_u8(qw, dev),
-                             scale_to_dev(sw, dev), off, y)
+                             scale_to_dev(sw, dev), off, y, workspace=ws)
     torch.cuda.synchronize()
     assert bfp8.bfp8_device_status() == 0
     return y
@@ -37,14 +41,15 @@ def _stack_quant(w):
     return np.stack(qs), np.stack(ss)
 
 
-def test_grouped_small_with_empty_experts(bfp8, cuda_device):
+@pytest.mark.parametrize("stream_k", [True, False], ids=["stream_k", "whole_tiles"])
+def test_grouped_small_with_empty_experts(bfp8, cuda_device, stream_k):
     offsets = [0, 3, 3, 200, 330, 331, 331]
     G, N, K = 6, 384, 256
     g = synth.generator(41)
     qw, sw = _stack_quant(synth.weight_stack_f32(g, G, N, K).numpy())
     xb = bits16(synth.activations_bf16(g, offsets[-1], K, outlier="entries", frac=0.01, factor=20.0))
     qa, sa = Q.act_quant_group(xb)
-    y = gpu_bf16_to_f64(_grouped(bfp8, cuda_device, qa, sa, qw, sw, offsets))
+    y = gpu_bf16_to_f64(_grouped(bfp8, cuda_device, qa, sa, qw, sw, offsets, stream_k))
     assert_close(y, L.grouped_linear_w8a8(qa, sa, qw, sw, offsets), "grouped small")
 
 
