@@ -82,29 +82,76 @@ def barrier(dist_mod) -> None:
         dist_mod.barrier()
 
 
-class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+THROTTLE_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+def parse_clock_samples(lines, t_begin=None, t_end=None) -> dict:
+    """Summarise nvidia-smi CLOCK_FIELDS rows (csv, noheader, nounits): median SM
+    clock, max SM clock, median power and every throttle reason seen Active.
+    Rows stamped outside [t_begin, t_end] (epoch seconds) are dropped, so idle
+    samples around the timed region do not enter the median."""
+    import datetime
+
+    sm, smax, power, reasons, stamps = [], [], [], set(), 0
+    for line in lines:
+        r = [c.strip() for c in line.split(",")]
+        if len(r) < 10:
+            continue
+        try:
+            ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            stamps += 1
+        except ValueError:
+            ts = None
+        if ts is not None and t_begin is not None and not (t_begin <= ts <= t_end):
+            continue
+        try:
+            sm.append(float(r[2]))
+            smax.append(float(r[3]))
+        except ValueError:
+            continue
+        try:
+            power.append(float(r[4]))
+        except ValueError:
+            pass
+        for name, v in zip(THROTTLE_NAMES, r[6:10]):
+            if v.lower().startswith("active"):
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "power_w": round(statistics.median(power), 1) if power else None,
+            "reasons": sorted(reasons), "samples": len(sm)}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples, kept only while the timed
+    region runs (begin() / end() mark it)."""
 
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
         self.path = ROOT / "gpurun_out" / f"clocks_bench_{os.getpid()}.csv"
+        self.t_begin = self.t_end = None
 
     def start(self):
         try:
             self.path.parent.mkdir(exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={CLOCK_FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def begin(self):
+        self.t_begin = time.time()
+
+    def end(self):
+        self.t_end = time.time()
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -116,24 +163,7 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        rows = [r.split(",") for r in self.path.read_text().splitlines() if r.strip()]
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            r = [c.strip() for c in r]
-            if len(r) < 9:
-                continue
-            try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
-            except ValueError:
-                continue
-            for name, v in zip(names, r[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return parse_clock_samples(self.path.read_text().splitlines(), self.t_begin, self.t_end)
 
 
 # --------------------------------------------------------------------------- our arm
@@ -207,11 +237,13 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    clocks.begin()
     t0.record(stream)
     for _ in range(args.steps):
         step(x, record=True)
     t1.record(stream)
     torch.cuda.synchronize()
+    clocks.end()
     barrier(dist_mod)
     clk = clocks.stop()
     ms = t0.elapsed_time(t1) / args.steps
@@ -220,7 +252,7 @@ def run_ours(args, rank, world, local):
     gu_events.clear()
 
     # end to end through the public API: pinned host x -> device, chain, y -> pinned host
-    e2e_steps = max(3, min(args.steps, 50))
+    e2e_steps = max(3, min(args.steps, 1000))
     barrier(dist_mod)
     torch.cuda.synchronize()
     t0.record(stream)
@@ -285,7 +317,7 @@ def run_ours(args, rank, world, local):
         "decode": decode,
     }
     if not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(args.cpu_rows)
+        out["cpu_baseline"] = cpu_baseline(args.cpu_seconds, args.cpu_chunk)
     return out
 
 
@@ -484,8 +516,8 @@ def _oracle_inputs():
     return _ORACLE_INPUTS
 
 
-def _oracle_chain_sample(rows: int):
-    """The CPU oracle, as it stands, on `rows` tokens of the same chain.
+def _oracle_chain_sample(r0: int, rows: int):
+    """The CPU oracle, as it stands, on tokens [r0, r0 + rows) of the same chain.
     Returns (seconds, algorithmic flops of those rows)."""
     from oracle import formats as F
     from oracle import linear as L
@@ -493,12 +525,23 @@ def _oracle_chain_sample(rows: int):
 
     qgu, sgu, qd, sd, xb = _oracle_inputs()
     t0 = time.perf_counter()
-    qa, sa = Q.act_quant_group(xb[:rows])
+    qa, sa = Q.act_quant_group(xb[r0:r0 + rows])
     gu = L.linear_w8a8(qa, sa, qgu, sgu, [INTER, INTER])
     qh, sh = Q.silu_mul_act_quant(F.f64_to_bf16_bits(gu))
     L.linear_w8a8(qh, sh, qd, sd)
     dt = time.perf_counter() - t0
     return dt, 2 * rows * (2 * INTER * HID + HID * INTER)
+
+
+def _oracle_bounded(seconds: float, chunk: int):
+    """Chunks of `chunk` tokens through the oracle chain until `seconds` of CPU
+    work have run or all M_TOK tokens are done. Returns (seconds, flops, rows)."""
+    dt_sum, fl_sum, r0 = 0.0, 0, 0
+    while r0 < M_TOK and (r0 == 0 or dt_sum < seconds):
+        rows = min(chunk, M_TOK - r0)
+        dt, fl = _oracle_chain_sample(r0, rows)
+        dt_sum, fl_sum, r0 = dt_sum + dt, fl_sum + fl, r0 + rows
+    return dt_sum, fl_sum, r0
 
 
 def _cores() -> int:
@@ -508,36 +551,41 @@ def _cores() -> int:
         return os.cpu_count() or 1
 
 
-def cpu_baseline(rows: int) -> dict:
-    dt, flops = _oracle_chain_sample(rows)
+def _sample_text(rows: int, dt: float, chunk: int) -> str:
+    return (f"{rows} of the {M_TOK} tokens through the whole chain, in chunks of {chunk} "
+            f"(numpy float64, BLAS threads = host cores), {dt:.1f} s")
+
+
+def cpu_baseline(seconds: float, chunk: int) -> dict:
+    dt, flops, rows = _oracle_bounded(seconds, chunk)
     return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": _cores(),
-            "kind": "oracle",
-            "sample": f"{rows} of the 949 tokens through the whole chain (numpy float64; "
-                      f"BLAS threads = host cores), {dt:.1f} s"}
+            "kind": "oracle", "sample": _sample_text(rows, dt, chunk)}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    per_step = []
     _oracle_inputs()
-    # the oracle takes seconds per step: run at most 3 so the arm ends in minutes
+    # the oracle takes seconds per step: run at most 3 bounded samples so the arm
+    # ends in minutes
     steps = max(1, min(args.steps, 3))
+    dts, fls, rows = [], [], 0
     for _ in range(steps):
-        dt, flops = _oracle_chain_sample(args.cpu_rows)
-        per_step.append(dt)
-    ms = statistics.mean(per_step) * 1e3
-    value = flops / (ms * 1e-3) / 1e12
+        dt, fl, rows = _oracle_bounded(args.cpu_seconds, args.cpu_chunk)
+        dts.append(dt)
+        fls.append(fl)
+    ms = statistics.mean(dts) * 1e3
+    value = sum(fls) / sum(dts) / 1e12
     return {
         "impl": "reference",
         "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
         "steps": steps, "warmup": 0, "ms_per_step": round(ms, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": M_TOK, "hidden": HID, "intermediate": INTER,
-                   "sample_rows": args.cpu_rows, "parallelism": "host cores"},
+                   "sample_rows": rows, "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": _cores(),
                          "kind": "oracle",
-                         "sample": f"{args.cpu_rows} of the 949 tokens per step through the whole chain"},
+                         "sample": _sample_text(rows, statistics.mean(dts), args.cpu_chunk) + " per step"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -546,10 +594,12 @@ def run_reference(args, rank, world):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-rows", type=int, default=8)
+    ap.add_argument("--cpu-seconds", type=float, default=20.0,
+                    help="CPU work bound of one oracle sample")
+    ap.add_argument("--cpu-chunk", type=int, default=128, help="tokens per oracle call")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", default=None, help="run one launch of: " + ", ".join(PROFILE_CASES))
     ap.add_argument("--decode-m", type=int, default=16)

@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
           Tile tl;
           decode_tile<BN, CL, GROUPED>(p, s_off, s_pre, t, rank, tl);
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_sleep(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
             const uint32_t sA = base + stage * C::kStage;
             const uint32_t sB = sA + C::kABytes;
             mbar_arrive_expect_tx(full_bar(stage), C::kTmaBytes);
@@ -419,29 +419,41 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        int stage = 0, buf = 0;
-        uint32_t phase = 0, bphase = 0;
-        bool ok = true;
-        SegIter it = seg_begin(sk, total, p.Kb, cid, ncl);
-        int t, kb0, kb1;
-        while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
-          for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(tempty_bar(buf), bphase ^ 1u, abort_flag)) { ok = false; break; }
-            if (!mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
-            if (W8A16 && !mbar_wait(conv_bar(stage), phase, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
-            const uint32_t sA = base + stage * C::kStage;
+      // The whole warp runs the loop (barrier waits, addresses) converged and
+      // one elected lane issues the tcgen05 instructions and their commits; a
+      // lone-lane loop issues them several times slower.
+      int stage = 0, buf = 0;
+      uint32_t phase = 0, bphase = 0;
+      bool ok = true;
+      SegIter it = seg_begin(sk, total, p.Kb, cid, ncl);
+      int t, kb0, kb1;
+      while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!__all_sync(0xffffffffu, mbar_wait_sleep(tempty_bar(buf), bphase ^ 1u, abort_flag))) {
+            ok = false;
+            break;
+          }
+          if (!__all_sync(0xffffffffu, mbar_wait_sleep(full_bar(stage), phase, abort_flag))) {
+            ok = false;
+            break;
+          }
+          if (W8A16 && !__all_sync(0xffffffffu, mbar_wait_sleep(conv_bar(stage), phase, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
+          const uint32_t sA = base + stage * C::kStage;
+          if (elect_one()) {
             if (!W8A16) {
               const uint64_t da = smem_desc_sw128(sA);
               const uint64_t db = smem_desc_sw128(sA + C::kABytes);
-  #pragma unroll
+#pragma unroll
               for (int k = 0; k < BK / 32; ++k)  // K = 32 bytes per MMA: +2 in 16-byte units
                 umma_e4m3(d, da + 2u * k, db + 2u * k, C::kIdesc, k > 0 ? 1u : 0u);
             } else {
               const uint32_t sConv = sA + C::kABytes + C::kBRawBytes;
-  #pragma unroll
+#pragma unroll
               for (int k = 0; k < BK / 16; ++k) {  // K = 16 BF16 = 32 bytes per MMA
                 const int j = k >> 2, kk = k & 3;
                 const uint64_t da = smem_desc_sw128(sA + j * (BM * 128)) + 2u * kk;
@@ -454,14 +466,18 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
             else
               umma_commit(empty_bar(stage));
             umma_commit(tfull_bar(buf));
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-            if (++buf == C::kNumBufs) { buf = 0; bphase ^= 1u; }
           }
+          __syncwarp();
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++buf == C::kNumBufs) { buf = 0; bphase ^= 1u; }
         }
-        if (!ok) raise_abort(abort_flag);
-        umma_commit(drain_bar);
-        wait_bounded(drain_bar, 0, kDrainLimitNs);
       }
+      if (!ok) raise_abort(abort_flag);
+      // the elected lane is the same one every time (lane 0 of a converged
+      // warp), so this commit tracks every MMA the warp issued
+      if (elect_one()) umma_commit(drain_bar);
+      __syncwarp();
+      wait_bounded(drain_bar, 0, kDrainLimitNs);
     }
   } else if (warp < C::kEpiWarp0 + C::kEpiWarps) {
     if constexpr (C::kSplitRegs) warpgroup_reg_alloc<C::kEpiRegs>();

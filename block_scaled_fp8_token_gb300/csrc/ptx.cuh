@@ -69,6 +69,44 @@ BFP8_DEV bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort
   }
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not yet complete
+// sleeps in hardware until it completes or about `ns` nanoseconds pass, rather
+// than re-issuing the test. Used by the single-purpose control warps.
+BFP8_DEV bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait with hardware suspension between tests; same limits and result.
+BFP8_DEV bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+  constexpr uint32_t kHintNs = 2000;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait_hint(bar, parity, kHintNs)) return true;
+    if ((i & 7u) == 7u) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
+// One lane of the (fully converged) warp returns true: the lowest active lane.
+BFP8_DEV bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 BFP8_DEV void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
