@@ -41,6 +41,34 @@ WORKLOAD = ("dense-FFN prefill chain, W8A8 block-FP8: M=949 BF16 tokens (N(0,1),
             "weights N(0,0.02^2) with 128x128 BF16 scales")
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+# one ncu capture of the kernel, keyed by a digest of the kernel's sources at
+# capture time: a changed kernel reports null until it is captured again.
+NCU_TRAFFIC = {
+    "gemm_gate_up": {"bytes": 183_554_048 + 48_139_520, "sources": "2f217e2e79d9b5c4",
+                     "kernel_files": ("bfp8_internal.h", "gemm_sm103.cu", "ptx.cuh")},
+    "gemv_gate_up_m16": {"bytes": 180_726_272 + 4_950_784, "sources": "",
+                         "kernel_files": ("bfp8_internal.h", "gemv_decode.cu", "ptx.cuh")},
+}
+
+
+def _source_digest(files) -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in files:
+        h.update((ROOT / "block_scaled_fp8_token_gb300" / "csrc" / f).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(name: str):
+    """(bytes, note): the captured traffic if the kernel's sources are unchanged."""
+    e = NCU_TRAFFIC[name]
+    if e["sources"] and _source_digest(e["kernel_files"]) == e["sources"]:
+        return e["bytes"], f"ncu capture, sources {e['sources']}"
+    return None, "kernel changed since its ncu capture"
+
+
 def _peaks():
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
@@ -265,6 +293,7 @@ def run_ours(args, rank, world, local):
     e2e_ms = reduce_max(t0.elapsed_time(t1) / e2e_steps, dist_mod)
 
     decode = run_decode(bfp8, torch, dev, wgu, sgu, wdn, sdn, peaks)
+    workloads = None if args.no_workloads else run_workloads(bfp8, torch, dev, peaks)
     status = bfp8.bfp8_device_status()
     if status != 0:
         raise RuntimeError(f"device status {bfp8.bfp8_status_string(status)}")
@@ -301,7 +330,8 @@ def run_ours(args, rank, world, local):
             "peak": round(fp8_peak, 1),
             "unit": "TFLOP/s",
             "frac": round(achieved / fp8_peak, 4),
-            "traffic": None,
+            "traffic": ncu_traffic("gemm_gate_up")[0],
+            "traffic_note": ncu_traffic("gemm_gate_up")[1],
             "peak_source": f"{peaks['source']} bf16 burst {peaks['bf16']} x 2 (FP8:BF16 nominal ratio 4.5:2.25)",
             "launch_ms": round(gu_ms, 4),
         },
@@ -315,6 +345,7 @@ def run_ours(args, rank, world, local):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "decode": decode,
+        "workloads": workloads,
     }
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.cpu_seconds, args.cpu_chunk)
@@ -360,7 +391,8 @@ def run_decode(bfp8, torch, dev, wgu, sgu, wdn, sdn, peaks):
         res["shapes"][f"M={M}"] = row
     res["roofline"] = {"bound": "hbm", "kernel": "gemv_kernel (gate/up [34816,5120], M=16)",
                        "achieved": best["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                       "frac": best["frac_hbm"], "traffic": None,
+                       "frac": best["frac_hbm"], "traffic": ncu_traffic("gemv_gate_up_m16")[0],
+                       "traffic_note": ncu_traffic("gemv_gate_up_m16")[1],
                        "peak_source": f"{peaks['source']} copy bandwidth"}
     del flush
     return res
@@ -371,19 +403,11 @@ PROFILE_CASES = ("act_quant", "gate_up", "silu_quant", "down", "gemv_gate_up", "
                  "qkv", "o_proj", "moe_gate_up", "moe_down", "w8a16_gate_up")
 
 
-def run_profile(args, local):
-    """Set up one launch of the hot path and run it warmup + steps times on its
-    own: the target for ncu captures and for per-kernel timing of the other
-    workloads (attention projections, MoE experts). Prints one JSON line with
-    the CUDA-event time per launch and the algorithmic work."""
-    import torch
-
-    from block_scaled_fp8_token_gb300 import bfp8, synth
-
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    gen = synth.generator(0)
-    case = args.profile
+def setup_case(case, bfp8, torch, dev, gen, decode_m=16):
+    """Device buffers for one launch of the hot path on a synthetic workload.
+    Returns (launch, work, unit, bound): work is algorithmic FLOPs (TFLOP/s
+    cases) or bytes (GB/s cases) per launch."""
+    from block_scaled_fp8_token_gb300 import synth
 
     def qweight(N, K, G=None):
         if G is None:
@@ -406,7 +430,6 @@ def run_profile(args, local):
         bfp8.bfp8_act_quant_group(x, q, s)
         return x, q, s
 
-    work, unit = 0, "TFLOP/s"
     if case in ("act_quant", "silu_quant"):
         K = HID if case == "act_quant" else INTER
         width = K if case == "act_quant" else 2 * K
@@ -414,33 +437,32 @@ def run_profile(args, local):
         q = torch.empty(M_TOK, K, dtype=torch.uint8, device=dev)
         s = torch.empty(M_TOK, K // 128, dtype=torch.float32, device=dev)
         fn = bfp8.bfp8_act_quant_group if case == "act_quant" else bfp8.bfp8_silu_mul_act_quant
-        launch = lambda: fn(x, q, s)
-        work, unit = M_TOK * width * 2 + M_TOK * K + 4 * M_TOK * (K // 128), "GB/s"
-    elif case in ("gate_up", "down", "w8a16_gate_up"):
+        return (lambda: fn(x, q, s)), M_TOK * width * 2 + M_TOK * K + 4 * M_TOK * (K // 128), \
+            "GB/s", "hbm"
+    if case in ("gate_up", "down", "w8a16_gate_up"):
         N, K = (2 * INTER, HID) if case != "down" else (HID, INTER)
         members = [INTER, INTER] if case != "down" else None
         w, sw = qweight(N, K)
         x, qa, sa = qact(M_TOK, K)
         y = torch.empty(M_TOK, N, dtype=torch.bfloat16, device=dev)
         if case == "w8a16_gate_up":
-            launch = lambda: bfp8.bfp8_linear_w8a16(x, w, sw, y, member_rows=members)
-        else:
-            ws = torch.empty(bfp8.bfp8_linear_w8a8_workspace(M_TOK, N, K, members),
-                             dtype=torch.uint8, device=dev)
-            launch = lambda: bfp8.bfp8_linear_w8a8(qa, sa, w, sw, y, member_rows=members,
-                                                   workspace=ws)
-        work = 2 * M_TOK * N * K
-    elif case in ("gemv_gate_up", "gemv_down"):
+            return (lambda: bfp8.bfp8_linear_w8a16(x, w, sw, y, member_rows=members)), \
+                2 * M_TOK * N * K, "TFLOP/s", "tensor-bf16"
+        ws = torch.empty(bfp8.bfp8_linear_w8a8_workspace(M_TOK, N, K, members),
+                         dtype=torch.uint8, device=dev)
+        return (lambda: bfp8.bfp8_linear_w8a8(qa, sa, w, sw, y, member_rows=members,
+                                              workspace=ws)), 2 * M_TOK * N * K, "TFLOP/s", "tensor"
+    if case in ("gemv_gate_up", "gemv_down"):
         N, K = (2 * INTER, HID) if case == "gemv_gate_up" else (HID, INTER)
         members = [INTER, INTER] if case == "gemv_gate_up" else None
         w, sw = qweight(N, K)
-        M = args.decode_m
+        M = decode_m
         x = synth.decode_tokens(1, M, K).to(dev)
         y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         ws = torch.empty(bfp8.bfp8_gemv_decode_workspace(M, N, K), dtype=torch.uint8, device=dev)
-        launch = lambda: bfp8.bfp8_gemv_decode(x, w, sw, y, ws, member_rows=members)
-        work, unit = N * K + sw.numel() * 2 + 2 * M * K + 2 * M * N, "GB/s"
-    elif case in ("qkv", "o_proj"):
+        return (lambda: bfp8.bfp8_gemv_decode(x, w, sw, y, ws, member_rows=members)), \
+            N * K + sw.numel() * 2 + 2 * M * K + 2 * M * N, "GB/s", "hbm"
+    if case in ("qkv", "o_proj"):
         c = synth.ATTENTION_PROJ
         M = c["M"]
         N, K = (c["q"] + c["k"] + c["v"], c["hidden"]) if case == "qkv" else (c["hidden"], c["o_in"])
@@ -450,9 +472,9 @@ def run_profile(args, local):
         y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         ws = torch.empty(bfp8.bfp8_linear_w8a8_workspace(M, N, K, members), dtype=torch.uint8,
                          device=dev)
-        launch = lambda: bfp8.bfp8_linear_w8a8(qa, sa, w, sw, y, member_rows=members, workspace=ws)
-        work = 2 * M * N * K
-    elif case in ("moe_gate_up", "moe_down"):
+        return (lambda: bfp8.bfp8_linear_w8a8(qa, sa, w, sw, y, member_rows=members, workspace=ws)), \
+            2 * M * N * K, "TFLOP/s", "tensor"
+    if case in ("moe_gate_up", "moe_down"):
         c = synth.MOE_PREFILL
         T, E, k = c["tokens"], c["experts"], c["top_k"]
         N, K = (2 * c["inter"], c["hidden"]) if case == "moe_gate_up" else (c["hidden"], c["inter"])
@@ -466,31 +488,84 @@ def run_profile(args, local):
         y = torch.empty(T * k, N, dtype=torch.bfloat16, device=dev)
         ws = torch.empty(bfp8.bfp8_grouped_linear_workspace(T * k, E, N, K), dtype=torch.uint8,
                          device=dev)
-        launch = lambda: bfp8.bfp8_grouped_linear(qa, sa, w, sw, offsets, y, workspace=ws)
-        work = 2 * T * k * N * K
-    else:
-        raise SystemExit(f"unknown profile case {case}; one of {PROFILE_CASES}")
+        return (lambda: bfp8.bfp8_grouped_linear(qa, sa, w, sw, offsets, y, workspace=ws)), \
+            2 * T * k * N * K, "TFLOP/s", "tensor"
+    raise SystemExit(f"unknown profile case {case}; one of {PROFILE_CASES}")
+
+
+def time_back_to_back(torch, launch, steps: int) -> float:
+    """ms per launch over `steps` back-to-back launches between one pair of
+    events: per-launch events would time the host's launch rate for the short
+    kernels."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        launch()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_profile(args, local):
+    """Set up one launch of the hot path and run it warmup + steps times on its
+    own: the target for ncu captures and for per-kernel timing of the other
+    workloads (attention projections, MoE experts). Prints one JSON line with
+    the CUDA-event time per launch and the algorithmic work."""
+    import torch
+
+    from block_scaled_fp8_token_gb300 import bfp8, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    launch, work, unit, _ = setup_case(args.profile, bfp8, torch, dev, synth.generator(0),
+                                       args.decode_m)
     torch.cuda.synchronize()
     torch.cuda.empty_cache()   # keep only the launch's own buffers on the device
     for _ in range(args.warmup):
         launch()
     torch.cuda.synchronize()
-    times = []
-    for _ in range(args.steps):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        launch()
-        e1.record()
-        times.append((e0, e1))
-    torch.cuda.synchronize()
+    ms = time_back_to_back(torch, launch, args.steps) if args.steps else float("nan")
     if bfp8.bfp8_device_status() != 0:
         raise RuntimeError("device status not OK")
-    ms = statistics.median(a.elapsed_time(b) for a, b in times) if times else float("nan")
-    rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9) if times else None
-    print(json.dumps({"profile": case, "ms": round(ms, 5) if times else None,
+    rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9) if args.steps else None
+    print(json.dumps({"profile": args.profile, "ms": round(ms, 5) if args.steps else None,
                       "rate": round(rate, 1) if rate else None, "unit": unit,
                       "l2": "warm (back-to-back launches)"}), flush=True)
+
+
+WORKLOAD_CASES = ("qkv", "o_proj", "moe_gate_up", "moe_down", "w8a16_gate_up", "act_quant",
+                  "silu_quant")
+
+
+def run_workloads(bfp8, torch, dev, peaks, steps: int = 50) -> dict:
+    """Per-launch throughput of the hot path on the other workloads (attention
+    projections at M=4096, MoE experts over 65,536 routed rows, the W8A16 arm,
+    the two quantizers), each against its own roofline."""
+    from block_scaled_fp8_token_gb300 import synth
+
+    out = {"timing": f"mean of {steps} back-to-back launches after 3 warm-up "
+                     "launches (GEMM inputs exceed L2 except the quantizers')", "cases": {}}
+    for case in WORKLOAD_CASES:
+        launch, work, unit, bound = setup_case(case, bfp8, torch, dev, synth.generator(0))
+        for _ in range(3):
+            launch()
+        torch.cuda.synchronize()
+        ms = time_back_to_back(torch, launch, steps)
+        if unit == "TFLOP/s":
+            rate = work / (ms * 1e-3) / 1e12
+            peak = 2.0 * peaks["bf16"] if bound == "tensor" else peaks["bf16"]
+        else:
+            rate = work / (ms * 1e-3) / 1e9
+            peak = peaks["hbm_gbs"]
+        out["cases"][case] = {"ms": round(ms, 5), "rate": round(rate, 1), "unit": unit,
+                              "bound": bound, "peak": round(peak, 1),
+                              "frac": round(rate / peak, 4), "work_per_launch": work}
+        del launch
+        torch.cuda.empty_cache()
+    if bfp8.bfp8_device_status() != 0:
+        raise RuntimeError("device status not OK after the workload sweep")
+    return out
 
 
 # --------------------------------------------------------------------------- oracle arm
@@ -601,6 +676,8 @@ def main(argv=None):
                     help="CPU work bound of one oracle sample")
     ap.add_argument("--cpu-chunk", type=int, default=128, help="tokens per oracle call")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-launch sweep over the other workloads")
     ap.add_argument("--profile", default=None, help="run one launch of: " + ", ".join(PROFILE_CASES))
     ap.add_argument("--decode-m", type=int, default=16)
     args = ap.parse_args(argv)

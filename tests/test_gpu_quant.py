@@ -104,3 +104,46 @@ def test_silu_mul_act_quant(bfp8, cuda_device, M, I):
     deq = dec_e4m3(q) * sfull
     bound = 2 ** -4 * np.abs(h) * (1 + 2 ** -6) + sfull * 2 ** -9
     assert np.all(np.abs(deq - h) <= bound)
+
+
+def _near_midpoint_groups(seed=5, n_amax=3000, rel=2.0 ** -22, limit_rows=256):
+    """BF16 groups whose quotients x / s sit within ~2 FP32 ulps of an E4M3
+    rounding midpoint: the only inputs where a quotient off by one FP32 ulp
+    would change a code. Column 0 of each row holds the group maximum."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for _ in range(n_amax):
+        a_bits = np.uint16(rng.integers(0x3F00, 0x4480))     # amax in [0.5, 1024)
+        A = F.bf16_bits_to_f32(np.array([a_bits], np.uint16))[0]
+        s = np.float32(A) / np.float32(448.0)
+        xb = np.arange(1, int(a_bits) + 1, dtype=np.uint16)
+        q = F.bf16_bits_to_f32(xb).astype(np.float64) / np.float64(s)
+        e = np.floor(np.log2(np.maximum(q, 2.0 ** -6)))
+        unit = np.where(q >= 2.0 ** -6, 2.0 ** e / 16.0, 2.0 ** -10)   # half the E4M3 step
+        odd = np.floor(q / unit / 2.0) * 2.0 + 1.0                      # nearest odd multiple
+        odd = np.where(np.abs(q / unit - odd) > 1.0, odd + 2.0, odd)
+        mid = odd * unit
+        hit = np.abs(q - mid) <= rel * mid
+        cand = xb[hit]
+        if cand.size:
+            row = np.zeros(128, np.uint16)
+            row[0] = a_bits
+            take = cand[:127]
+            signs = rng.integers(0, 2, take.size).astype(np.uint16) << 15
+            row[1:1 + take.size] = take | signs
+            rows.append(row)
+        if len(rows) >= limit_rows:
+            break
+    return np.stack(rows)
+
+
+def test_act_quant_near_rounding_midpoints(bfp8, cuda_device):
+    """The per-group reciprocal + remainder-correction quotient must round
+    exactly like IEEE x / s on the inputs where that is hardest."""
+    xb = _near_midpoint_groups()
+    n_hard = int(np.count_nonzero(xb[:, 1:]))
+    assert n_hard >= 100, n_hard
+    q, s = _run_act_quant(bfp8, cuda_device, xb)
+    qr, sr = Q.act_quant_group(xb)
+    assert np.array_equal(s.view(np.uint32), sr.view(np.uint32))
+    assert np.array_equal(q, qr)
