@@ -4,8 +4,10 @@ One step = one pass of the dense-FFN W8A8 prefill chain, the workload the
 pages measure their prefill on (949 tokens of BF16 activations, hidden 5120,
 intermediate 17408):
     bfp8_act_quant_group(x)              [949, 5120]  -> E4M3 + 1x128 scales
-    bfp8_linear_w8a8(gate/up)            [34816, 5120] as two member-local grids
-    bfp8_silu_mul_act_quant              [949, 34816] -> E4M3 [949, 17408]
+    bfp8_linear_w8a8_silu_quant          gate/up [34816, 5120] (two member-local
+                                         grids) with SiLU(gate)*up and the 1x128
+                                         quantization of h in its epilogue
+                                         -> E4M3 [949, 17408] + scales
     bfp8_linear_w8a8(down)               [5120, 17408]
 The headline value is prefill TFLOP/s over the chain: 2*M*(N1*K1 + N2*K2)
 algorithmic FLOPs (true M, no padding) per step. The decode half of the
@@ -45,9 +47,9 @@ WORKLOAD = ("dense-FFN prefill chain, W8A8 block-FP8: M=949 BF16 tokens (N(0,1),
 # one ncu capture of the kernel, keyed by a digest of the kernel's sources at
 # capture time: a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
-    "gemm_gate_up": {"bytes": 183_554_048 + 48_139_520, "sources": "2f217e2e79d9b5c4",
-                     "kernel_files": ("bfp8_internal.h", "gemm_sm103.cu", "ptx.cuh")},
-    "gemv_gate_up_m16": {"bytes": 180_726_272 + 4_950_784, "sources": "",
+    "gemm_gate_up_silu_quant": {"bytes": 183_410_688 + 13_410_048, "sources": "076962e803ba1fdd",
+                                "kernel_files": ('act_math.cuh', 'bfp8_internal.h', 'gemm_sm103.cu', 'ptx.cuh')},
+    "gemv_gate_up_m16": {"bytes": 180_726_272 + 4_950_784, "sources": "21a2bf737bc3c3fe",
                          "kernel_files": ("bfp8_internal.h", "gemv_decode.cu", "ptx.cuh")},
 }
 
@@ -225,14 +227,12 @@ def run_ours(args, rank, world, local):
 
     qa = torch.empty(M_TOK, HID, dtype=torch.uint8, device=dev)
     sa = torch.empty(M_TOK, HID // 128, dtype=torch.float32, device=dev)
-    gu = torch.empty(M_TOK, 2 * INTER, dtype=torch.bfloat16, device=dev)
     qh = torch.empty(M_TOK, INTER, dtype=torch.uint8, device=dev)
     sh = torch.empty(M_TOK, INTER // 128, dtype=torch.float32, device=dev)
     y = torch.empty(M_TOK, HID, dtype=torch.bfloat16, device=dev)
     y_host = torch.empty(M_TOK, HID, dtype=torch.bfloat16).pin_memory()
     stream = torch.cuda.current_stream(dev)
-    members = [INTER, INTER]
-    ws_gu = torch.empty(bfp8.bfp8_linear_w8a8_workspace(M_TOK, 2 * INTER, HID, members),
+    ws_gu = torch.empty(bfp8.bfp8_linear_w8a8_silu_quant_workspace(M_TOK, INTER, HID),
                         dtype=torch.uint8, device=dev)
     ws_dn = torch.empty(bfp8.bfp8_linear_w8a8_workspace(M_TOK, HID, INTER), dtype=torch.uint8,
                         device=dev)
@@ -244,15 +244,14 @@ def run_ours(args, rank, world, local):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-        bfp8.bfp8_linear_w8a8(qa, sa, wgu, sgu, gu, member_rows=members, workspace=ws_gu,
-                              stream=stream)
+        bfp8.bfp8_linear_w8a8_silu_quant(qa, sa, wgu, sgu, qh, sh, workspace=ws_gu,
+                                         stream=stream)
         if record:
             e1.record(stream)
             gu_events.append((e0, e1))
-        bfp8.bfp8_silu_mul_act_quant(gu, qh, sh, stream=stream)
         bfp8.bfp8_linear_w8a8(qh, sh, wdn, sdn, y, workspace=ws_dn, stream=stream)
 
-    launches_per_step = 4
+    launches_per_step = 3
     for _ in range(args.warmup):
         step(x)
     torch.cuda.synchronize()
@@ -325,13 +324,13 @@ def run_ours(args, rank, world, local):
         },
         "roofline": {
             "bound": "tensor",
-            "kernel": "gemm_kernel<256,4,W8A8> (gate/up [34816,5120], M=949)",
+            "kernel": "gemm_kernel<256,4,W8A8,fused SiLU*up+quant> (gate/up [34816,5120], M=949)",
             "achieved": round(achieved, 1),
             "peak": round(fp8_peak, 1),
             "unit": "TFLOP/s",
             "frac": round(achieved / fp8_peak, 4),
-            "traffic": ncu_traffic("gemm_gate_up")[0],
-            "traffic_note": ncu_traffic("gemm_gate_up")[1],
+            "traffic": ncu_traffic("gemm_gate_up_silu_quant")[0],
+            "traffic_note": ncu_traffic("gemm_gate_up_silu_quant")[1],
             "peak_source": f"{peaks['source']} bf16 burst {peaks['bf16']} x 2 (FP8:BF16 nominal ratio 4.5:2.25)",
             "launch_ms": round(gu_ms, 4),
         },
@@ -399,7 +398,8 @@ def run_decode(bfp8, torch, dev, wgu, sgu, wdn, sdn, peaks):
 
 
 # --------------------------------------------------------------------------- single-launch mode
-PROFILE_CASES = ("act_quant", "gate_up", "silu_quant", "down", "gemv_gate_up", "gemv_down",
+PROFILE_CASES = ("act_quant", "gate_up", "gate_up_silu_quant", "silu_quant", "down",
+                 "moe_gate_up_silu_quant", "gemv_gate_up", "gemv_down",
                  "qkv", "o_proj", "moe_gate_up", "moe_down", "w8a16_gate_up")
 
 
@@ -452,6 +452,15 @@ def setup_case(case, bfp8, torch, dev, gen, decode_m=16):
                          dtype=torch.uint8, device=dev)
         return (lambda: bfp8.bfp8_linear_w8a8(qa, sa, w, sw, y, member_rows=members,
                                               workspace=ws)), 2 * M_TOK * N * K, "TFLOP/s", "tensor"
+    if case == "gate_up_silu_quant":
+        w, sw = qweight(2 * INTER, HID)
+        x, qa, sa = qact(M_TOK, HID)
+        qh = torch.empty(M_TOK, INTER, dtype=torch.uint8, device=dev)
+        sh = torch.empty(M_TOK, INTER // 128, dtype=torch.float32, device=dev)
+        ws = torch.empty(bfp8.bfp8_linear_w8a8_silu_quant_workspace(M_TOK, INTER, HID),
+                         dtype=torch.uint8, device=dev)
+        return (lambda: bfp8.bfp8_linear_w8a8_silu_quant(qa, sa, w, sw, qh, sh, workspace=ws)), \
+            2 * M_TOK * 2 * INTER * HID, "TFLOP/s", "tensor"
     if case in ("gemv_gate_up", "gemv_down"):
         N, K = (2 * INTER, HID) if case == "gemv_gate_up" else (HID, INTER)
         members = [INTER, INTER] if case == "gemv_gate_up" else None
@@ -474,10 +483,10 @@ def setup_case(case, bfp8, torch, dev, gen, decode_m=16):
                          device=dev)
         return (lambda: bfp8.bfp8_linear_w8a8(qa, sa, w, sw, y, member_rows=members, workspace=ws)), \
             2 * M * N * K, "TFLOP/s", "tensor"
-    if case in ("moe_gate_up", "moe_down"):
+    if case in ("moe_gate_up", "moe_down", "moe_gate_up_silu_quant"):
         c = synth.MOE_PREFILL
         T, E, k = c["tokens"], c["experts"], c["top_k"]
-        N, K = (2 * c["inter"], c["hidden"]) if case == "moe_gate_up" else (c["hidden"], c["inter"])
+        N, K = (c["hidden"], c["inter"]) if case == "moe_down" else (2 * c["inter"], c["hidden"])
         logits = synth.router_logits(gen, T, E).to(dev)
         top = torch.topk(torch.softmax(logits.double(), dim=1), k, dim=1).indices.reshape(-1)
         counts = torch.bincount(top, minlength=E)
@@ -485,6 +494,15 @@ def setup_case(case, bfp8, torch, dev, gen, decode_m=16):
         offsets[1:] = torch.cumsum(counts, 0).to(torch.int32)
         w, sw = qweight(N, K, G=E)
         x, qa, sa = qact(T * k, K)
+        if case == "moe_gate_up_silu_quant":
+            I = c["inter"]
+            qh = torch.empty(T * k, I, dtype=torch.uint8, device=dev)
+            sh = torch.empty(T * k, I // 128, dtype=torch.float32, device=dev)
+            ws = torch.empty(bfp8.bfp8_grouped_linear_silu_quant_workspace(T * k, E, I, K),
+                             dtype=torch.uint8, device=dev)
+            return (lambda: bfp8.bfp8_grouped_linear_silu_quant(qa, sa, w, sw, offsets, qh, sh,
+                                                                workspace=ws)), \
+                2 * T * k * N * K, "TFLOP/s", "tensor"
         y = torch.empty(T * k, N, dtype=torch.bfloat16, device=dev)
         ws = torch.empty(bfp8.bfp8_grouped_linear_workspace(T * k, E, N, K), dtype=torch.uint8,
                          device=dev)
@@ -534,8 +552,8 @@ def run_profile(args, local):
                       "l2": "warm (back-to-back launches)"}), flush=True)
 
 
-WORKLOAD_CASES = ("qkv", "o_proj", "moe_gate_up", "moe_down", "w8a16_gate_up", "act_quant",
-                  "silu_quant")
+WORKLOAD_CASES = ("gate_up", "qkv", "o_proj", "moe_gate_up_silu_quant", "moe_gate_up", "moe_down",
+                  "w8a16_gate_up", "act_quant", "silu_quant")
 
 
 def run_workloads(bfp8, torch, dev, peaks, steps: int = 50) -> dict:

@@ -83,6 +83,14 @@ _SIGS = {
     "bfp8_grouped_linear": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i32, _vp, _i32, _i64,
                                            _i64, _i64, _vp, _i64, _vp, _sz, _vp]),
     "bfp8_grouped_linear_workspace": (_sz, [_i64, _i32, _i64, _i64]),
+    "bfp8_linear_w8a8_silu_quant": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i32, _i64,
+                                                   _i64, _i64, _vp, _i64, _vp, _i64, _i64, _vp,
+                                                   _sz, _vp]),
+    "bfp8_linear_w8a8_silu_quant_workspace": (_sz, [_i64, _i64, _i64]),
+    "bfp8_grouped_linear_silu_quant": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i32, _vp,
+                                                      _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i64,
+                                                      _i64, _vp, _sz, _vp]),
+    "bfp8_grouped_linear_silu_quant_workspace": (_sz, [_i64, _i32, _i64, _i64]),
     "bfp8_device_status": (ctypes.c_int, [_vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -273,6 +281,53 @@ def bfp8_grouped_linear(q_a, s_a, w, w_scale, offsets, y, s_stride_m=None, s_str
                                     _scale_dtype(w_scale), _ptr(offsets), G, T, N, K, _ptr(y),
                                     y.stride(0), wsp, wsb, _stream(stream)),
            "bfp8_grouped_linear")
+
+
+def bfp8_linear_w8a8_silu_quant_workspace(M: int, I: int, K: int) -> int:
+    return int(_lib.bfp8_linear_w8a8_silu_quant_workspace(M, I, K))
+
+
+def bfp8_linear_w8a8_silu_quant(q_a, s_a, w, w_scale, q_h, s_h, s_stride_m=None,
+                                s_stride_kb=None, sh_stride_m=None, sh_stride_kb=None,
+                                workspace=None, stream=None) -> None:
+    """Gate/up projection (w = gate rows over up rows, [2I, K]) with SiLU(gate)*up
+    and the 1x128 quantization of h fused into its epilogue: q_h [M, I], s_h."""
+    M, K = q_a.shape
+    I = w.shape[0] // 2
+    ssm = s_a.stride(0) if s_stride_m is None else s_stride_m
+    sskb = s_a.stride(1) if s_stride_kb is None else s_stride_kb
+    hsm = s_h.stride(0) if sh_stride_m is None else sh_stride_m
+    hskb = s_h.stride(1) if sh_stride_kb is None else sh_stride_kb
+    wsp, wsb = _ws(workspace)
+    _check(_lib.bfp8_linear_w8a8_silu_quant(_ptr(q_a), _ptr(s_a), ssm, sskb, _ptr(w),
+                                            _ptr(w_scale), _scale_dtype(w_scale), M, I, K,
+                                            _ptr(q_h), q_h.stride(0), _ptr(s_h), hsm, hskb, wsp,
+                                            wsb, _stream(stream)),
+           "bfp8_linear_w8a8_silu_quant")
+
+
+def bfp8_grouped_linear_silu_quant_workspace(total_M: int, G: int, I: int, K: int) -> int:
+    return int(_lib.bfp8_grouped_linear_silu_quant_workspace(total_M, G, I, K))
+
+
+def bfp8_grouped_linear_silu_quant(q_a, s_a, w, w_scale, offsets, q_h, s_h, s_stride_m=None,
+                                   s_stride_kb=None, sh_stride_m=None, sh_stride_kb=None,
+                                   workspace=None, stream=None) -> None:
+    """Per-expert gate/up projection (w [G, 2I, K]) with the fused SiLU*up +
+    1x128 quant epilogue over the token-offset table."""
+    T, K = q_a.shape
+    G, I = w.shape[0], w.shape[1] // 2
+    ssm = s_a.stride(0) if s_stride_m is None else s_stride_m
+    sskb = s_a.stride(1) if s_stride_kb is None else s_stride_kb
+    hsm = s_h.stride(0) if sh_stride_m is None else sh_stride_m
+    hskb = s_h.stride(1) if sh_stride_kb is None else sh_stride_kb
+    wsp, wsb = _ws(workspace)
+    _check(_lib.bfp8_grouped_linear_silu_quant(_ptr(q_a), _ptr(s_a), ssm, sskb, _ptr(w),
+                                               _ptr(w_scale), _scale_dtype(w_scale),
+                                               _ptr(offsets), G, T, I, K, _ptr(q_h),
+                                               q_h.stride(0), _ptr(s_h), hsm, hskb, wsp, wsb,
+                                               _stream(stream)),
+           "bfp8_grouped_linear_silu_quant")
 
 
 def bfp8_device_status(stream=None) -> int:

@@ -368,6 +368,51 @@ int bfp8_grouped_linear(const void* q_a, const float* s_a, int64_t s_stride_m,
                              stream);
 }
 
+size_t bfp8_linear_w8a8_silu_quant_workspace(int64_t M, int64_t I, int64_t K) {
+  (void)K;
+  int sms = 0;
+  if (M <= 0 || I <= 0 || sm_count(&sms) != BFP8_OK) return 0;
+  return gemm_w8a8_swiglu_workspace_bytes(M, I, sms);
+}
+
+int bfp8_linear_w8a8_silu_quant(const void* q_a, const float* s_a, int64_t s_stride_m,
+                                int64_t s_stride_kb, const void* w_e4m3, const void* w_scale,
+                                int32_t w_scale_dtype, int64_t M, int64_t I, int64_t K,
+                                void* q_h, int64_t ldq, float* s_h, int64_t sh_stride_m,
+                                int64_t sh_stride_kb, void* workspace, size_t ws_bytes,
+                                void* stream) {
+  if (M < 0 || I <= 0 || K <= 0) return BFP8_ERR_INVALID_ARG;
+  if (M == 0) return BFP8_OK;
+  if (!q_a || !s_a || !w_e4m3 || !w_scale || !q_h || !s_h || ldq < I) return BFP8_ERR_INVALID_ARG;
+  if (w_scale_dtype != BFP8_DT_BF16 && w_scale_dtype != BFP8_DT_F32) return BFP8_ERR_SCALE_DTYPE;
+  return launch_gemm_w8a8_swiglu(q_a, s_a, s_stride_m, s_stride_kb, w_e4m3, w_scale,
+                                 w_scale_dtype, M, I, K, q_h, ldq, s_h, sh_stride_m,
+                                 sh_stride_kb, workspace, ws_bytes, stream);
+}
+
+size_t bfp8_grouped_linear_silu_quant_workspace(int64_t total_M, int32_t G, int64_t I, int64_t K) {
+  (void)K;
+  int sms = 0;
+  if (total_M <= 0 || G < 1 || I <= 0 || sm_count(&sms) != BFP8_OK) return 0;
+  return grouped_w8a8_swiglu_workspace_bytes(total_M, G, I, sms);
+}
+
+int bfp8_grouped_linear_silu_quant(const void* q_a, const float* s_a, int64_t s_stride_m,
+                                   int64_t s_stride_kb, const void* w_e4m3, const void* w_scale,
+                                   int32_t w_scale_dtype, const int32_t* offsets_dev, int32_t G,
+                                   int64_t total_M, int64_t I, int64_t K, void* q_h, int64_t ldq,
+                                   float* s_h, int64_t sh_stride_m, int64_t sh_stride_kb,
+                                   void* workspace, size_t ws_bytes, void* stream) {
+  if (G < 1 || G > 1024 || total_M < 0 || I <= 0 || K <= 0) return BFP8_ERR_INVALID_ARG;
+  if (total_M == 0) return BFP8_OK;
+  if (!q_a || !s_a || !w_e4m3 || !w_scale || !offsets_dev || !q_h || !s_h || ldq < I)
+    return BFP8_ERR_INVALID_ARG;
+  if (w_scale_dtype != BFP8_DT_BF16 && w_scale_dtype != BFP8_DT_F32) return BFP8_ERR_SCALE_DTYPE;
+  return launch_grouped_w8a8_swiglu(q_a, s_a, s_stride_m, s_stride_kb, w_e4m3, w_scale,
+                                    w_scale_dtype, offsets_dev, G, total_M, I, K, q_h, ldq, s_h,
+                                    sh_stride_m, sh_stride_kb, workspace, ws_bytes, stream);
+}
+
 int bfp8_device_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return BFP8_ERR_CUDA;

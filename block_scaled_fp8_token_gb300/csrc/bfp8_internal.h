@@ -51,6 +51,18 @@ int launch_gemm_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t s
                      const void* w, const void* w_scale, int32_t w_scale_dtype, int64_t M,
                      int64_t N, int64_t K, void* y, int64_t ldy, const MemberTable& mt,
                      void* workspace, size_t ws_bytes, void* stream);
+size_t gemm_w8a8_swiglu_workspace_bytes(int64_t M, int64_t I, int sms);
+size_t grouped_w8a8_swiglu_workspace_bytes(int64_t total_M, int32_t G, int64_t I, int sms);
+int launch_gemm_w8a8_swiglu(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
+                            const void* w, const void* w_scale, int32_t w_scale_dtype, int64_t M,
+                            int64_t I, int64_t K, void* q_h, int64_t ldq, float* s_h,
+                            int64_t sh_sm, int64_t sh_skb, void* workspace, size_t ws_bytes,
+                            void* stream);
+int launch_grouped_w8a8_swiglu(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
+                               const void* w, const void* w_scale, int32_t w_scale_dtype,
+                               const int32_t* offsets, int32_t G, int64_t total_M, int64_t I,
+                               int64_t K, void* q_h, int64_t ldq, float* s_h, int64_t sh_sm,
+                               int64_t sh_skb, void* workspace, size_t ws_bytes, void* stream);
 int launch_gemm_w8a16(const void* x, int64_t ldx, const void* w, const void* w_scale,
                       int32_t w_scale_dtype, int64_t M, int64_t N, int64_t K, void* y,
                       int64_t ldy, const MemberTable& mt, void* stream);

@@ -39,6 +39,7 @@
 
 #include "bfp8_internal.h"
 #include "ptx.cuh"
+#include "act_math.cuh"
 
 namespace bfp8 {
 
@@ -70,6 +71,14 @@ struct GemmParams {
   // grouped mode
   const int32_t* offsets;
   int32_t G, N, n_tiles;
+  // fused SiLU(gate)*up + 1x128 quant epilogue: W stacks the gate rows
+  // [0, I) over the up rows [I, 2I); the output is h's E4M3 codes and scales
+  uint8_t* q_h;
+  int64_t ldq;
+  float* s_h;
+  int64_t sh_sm, sh_skb;
+  int32_t up_row0;    // first up row of W (of each expert's W when grouped): I
+  int32_t up_sbase;   // first scale row of the up member's grid: ceil(I / 128)
   // stream-K: split tiles exchange FP32 partials through a caller workspace
   int32_t stream_k;
   int32_t* ws_counters;   // one arrival counter per tile, zero on entry
@@ -138,6 +147,7 @@ struct Tile {
   int32_t b_row0, expert;    // first weight row (expert-local when grouped)
   int32_t n_out0, n_valid;   // first output column, columns valid from it
   int32_t srow0, srow_last;  // scale row of the first 128 columns; member's last row
+  int32_t b_row0_up, srow_up;  // fused SiLU*up: first up row and its scale row
 };
 
 #ifndef BFP8_W8A8_CLUSTER
@@ -145,8 +155,12 @@ struct Tile {
 #endif
 constexpr int kW8A8Cluster = BFP8_W8A8_CLUSTER;
 
-template <int BN, int STAGES, bool W8A16, bool GROUPED>
+template <int BN, int STAGES, bool W8A16, bool GROUPED, bool SWIGLU = false>
 struct Cfg {
+  static_assert(!SWIGLU || (!W8A16 && BN == 256),
+                "the fused SiLU*up epilogue pairs 128 gate with 128 up columns of a W8A8 tile");
+  // output columns a tile covers: BN, or BN/2 when a tile holds gate and up halves
+  static constexpr int kOutCols = SWIGLU ? BN / 2 : BN;
   static constexpr int kEpiWarps = 8;
   static constexpr int kConvWarps = W8A16 ? 4 : 0;
   // W8A8: warpgroup 0 = producer, MMA and two idle warps; warpgroups 1-2 =
@@ -155,13 +169,15 @@ struct Cfg {
   static constexpr bool kSplitRegs = !W8A16;
   // W8A8 runs in 2-CTA clusters on adjacent M tiles: each CTA loads its own A
   // tile and half of the shared B tile, multicast to both CTAs.
-  static constexpr int kCluster = W8A16 ? 1 : kW8A8Cluster;
+  static constexpr int kCluster = (W8A16 || SWIGLU) ? 1 : kW8A8Cluster;
   static constexpr int kEpiWarp0 = kSplitRegs ? 4 : 2;
   static constexpr int kWarps = kEpiWarp0 + kEpiWarps + kConvWarps;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kLaunchRegs = 168;      // 65536 / 384 rounded down to a multiple of 8
-  static constexpr int kCtrlRegs = 64;
-  static constexpr int kEpiRegs = 216;
+  // The fused SiLU*up epilogue keeps a second scale factor live in the
+  // promotion loop, so it takes 8 more registers per epilogue thread.
+  static constexpr int kCtrlRegs = SWIGLU ? 48 : 64;
+  static constexpr int kEpiRegs = SWIGLU ? 224 : 216;
   static_assert(!kSplitRegs || kCtrlRegs * 128 + kEpiRegs * 256 <= kLaunchRegs * kThreads,
                 "register split must add up to the launch allocation");
   static constexpr int kEpiCols = BN / 2;
@@ -191,9 +207,12 @@ struct Cfg {
 };
 
 // Work item t covers CL adjacent M tiles (one per CTA of the cluster) of one
-// N tile; `rank` picks this CTA's M tile. A rank past the last M tile gets
-// m_valid <= 0: it still loads and multicasts its share of B, but stores nothing.
-template <int BN, int CL, bool GROUPED>
+// N tile of TW output columns; `rank` picks this CTA's M tile. A rank past the
+// last M tile gets m_valid <= 0: it still loads and multicasts its share of B,
+// but stores nothing. The up-half fields serve the fused SiLU*up epilogue,
+// whose tile of TW output columns reads TW gate rows and the TW matching up
+// rows of W.
+template <int TW, int CL, bool GROUPED>
 __device__ __forceinline__ void decode_tile(const GemmParams& p, const int* s_off,
                                             const int* s_pre, int t, int rank, Tile& tl) {
   if (!GROUPED) {
@@ -203,15 +222,17 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, const int* s_of
     int i = 0;
 #pragma unroll 1
     while (i + 1 < p.n_members && nt >= p.mem_tile0[i + 1]) ++i;
-    const int nl0 = (nt - p.mem_tile0[i]) * BN;
+    const int nl0 = (nt - p.mem_tile0[i]) * TW;
     tl.a_row0 = mt * BM;
     tl.m_valid = min(BM, p.M - tl.a_row0);
     tl.b_row0 = p.mem_n0[i] + nl0;
     tl.expert = 0;
     tl.n_out0 = tl.b_row0;
-    tl.n_valid = min(BN, p.mem_rows[i] - nl0);
+    tl.n_valid = min(TW, p.mem_rows[i] - nl0);
     tl.srow0 = p.mem_sbase[i] + nl0 / 128;
     tl.srow_last = p.mem_sbase[i] + (p.mem_rows[i] + 127) / 128 - 1;
+    tl.b_row0_up = p.up_row0 + nl0;
+    tl.srow_up = p.up_sbase + nl0 / 128;
   } else {
     int lo = 0, hi = p.G;  // invariant: s_pre[lo] <= t < s_pre[hi]
 #pragma unroll 1
@@ -228,12 +249,14 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, const int* s_of
     const int mt = (local - nt * units) * CL + rank;
     tl.a_row0 = row0 + mt * BM;
     tl.m_valid = min(BM, rows - mt * BM);
-    tl.b_row0 = nt * BN;
+    tl.b_row0 = nt * TW;
     tl.expert = e;
-    tl.n_out0 = nt * BN;
-    tl.n_valid = min(BN, p.N - nt * BN);
-    tl.srow0 = (nt * BN) / 128;
+    tl.n_out0 = nt * TW;
+    tl.n_valid = min(TW, p.N - nt * TW);
+    tl.srow0 = (nt * TW) / 128;
     tl.srow_last = (p.N + 127) / 128 - 1;
+    tl.b_row0_up = p.up_row0 + nt * TW;
+    tl.srow_up = p.up_sbase + (nt * TW) / 128;
   }
 }
 
@@ -296,16 +319,18 @@ BFP8_DEV void raise_abort(volatile int* abort_flag) {
   atomicExch(&g_gemm_err, static_cast<int>(BFP8_ERR_TIMEOUT));
 }
 
+BFP8_DEV float bf16_round(float a) { return __bfloat162float(__float2bfloat16_rn(a)); }
+
 BFP8_DEV uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int BN, int STAGES, bool W8A16, bool GROUPED>
-__global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
+template <int BN, int STAGES, bool W8A16, bool GROUPED, bool SWIGLU>
+__global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ GemmParams p) {
-  using C = Cfg<BN, STAGES, W8A16, GROUPED>;
+  using C = Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
@@ -382,7 +407,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
         int t, kb0, kb1;
         while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
           Tile tl;
-          decode_tile<BN, CL, GROUPED>(p, s_off, s_pre, t, rank, tl);
+          decode_tile<C::kOutCols, CL, GROUPED>(p, s_off, s_pre, t, rank, tl);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait_sleep(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
             const uint32_t sA = base + stage * C::kStage;
@@ -402,6 +427,16 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
                 tma_load_3d_mc(sB + half, &tmB, kb * BK, brow, tl.expert, full_bar(stage), 0x3);
               else
                 tma_load_2d_mc(sB + half, &tmB, kb * BK, brow, full_bar(stage), 0x3);
+            } else if constexpr (SWIGLU) {
+              // gate rows into B rows [0, BN/2), the matching up rows into [BN/2, BN)
+              const uint32_t sBu = sB + (BN / 2) * 128u;
+              if (GROUPED) {
+                tma_load_3d(sB, &tmB, kb * BK, tl.b_row0, tl.expert, full_bar(stage));
+                tma_load_3d(sBu, &tmB, kb * BK, tl.b_row0_up, tl.expert, full_bar(stage));
+              } else {
+                tma_load_2d(sB, &tmB, kb * BK, tl.b_row0, full_bar(stage));
+                tma_load_2d(sBu, &tmB, kb * BK, tl.b_row0_up, full_bar(stage));
+              }
             } else if (GROUPED) {
               tma_load_3d(sB, &tmB, kb * BK, tl.b_row0, tl.expert, full_bar(stage));
             } else {
@@ -498,15 +533,23 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
     int t, kb0, kb1;
     while (next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
       Tile tl;
-      decode_tile<BN, CL, GROUPED>(p, s_off, s_pre, t, rank, tl);
+      decode_tile<C::kOutCols, CL, GROUPED>(p, s_off, s_pre, t, rank, tl);
       const bool row_ok = row_in_tile < tl.m_valid;
       const int64_t arow = static_cast<int64_t>(tl.a_row0) + row_in_tile;
-      const int srow = min(tl.srow0 + (h * C::kEpiCols) / 128, tl.srow_last);
-      const int64_t sw_idx = (GROUPED ? tl.expert * p.sw_expert_stride : 0) +
-                             static_cast<int64_t>(srow) * p.Kb;
+      // This warp's columns of the tile: 128 consecutive ones (one weight-scale
+      // block), or with the fused SiLU*up epilogue 64 gate columns and the
+      // 64 matching up columns, each half with its own member's scale row.
+      const int srow = SWIGLU ? tl.srow0 : min(tl.srow0 + (h * C::kEpiCols) / 128, tl.srow_last);
+      const int64_t sw_base = GROUPED ? tl.expert * p.sw_expert_stride : 0;
+      const int64_t sw_idx = sw_base + static_cast<int64_t>(srow) * p.Kb;
+      const int64_t sw_idx_up = sw_base + static_cast<int64_t>(tl.srow_up) * p.Kb;
       const float* sa_row = p.s_a + (row_ok ? arow * p.sa_sm : 0);
-      auto factor = [&](int kb) -> float {
-        const float sw = p.sw_f32 ? __ldg(sw32 + sw_idx + kb) : bf16_bits_to_f32(__ldg(sw16 + sw_idx + kb));
+      auto wscale = [&](int64_t idx) -> float {
+        return p.sw_f32 ? __ldg(sw32 + idx) : bf16_bits_to_f32(__ldg(sw16 + idx));
+      };
+      // promotion factor s_a[m,kb] * s_w[row,kb] (s_w alone for W8A16)
+      auto factor = [&](int64_t idx, int kb) -> float {
+        const float sw = wscale(idx + kb);
         if (W8A16) return sw;
         const float sa = row_ok ? __ldg(sa_row + kb * p.sa_skb) : 0.0f;
         return sa * sw;
@@ -515,26 +558,34 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
       float2 acc[C::kEpiCols / 2];
 #pragma unroll
       for (int i = 0; i < C::kEpiCols / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
-      float f_next = factor(kb0);
+      // factors of the next K-block are loaded one K-block ahead; the up
+      // half's factor exists only with the fused SiLU*up epilogue
+      float f_next = factor(sw_idx, kb0);
+      float fu_next = SWIGLU ? factor(sw_idx_up, kb0) : 0.0f;
       for (int kb = kb0; kb < kb1 && ok; ++kb) {
-        const float f = f_next;
+        const float f = f_next, fu = fu_next;
         const float2 f2 = make_float2(f, f);
-        if (kb + 1 < kb1) f_next = factor(kb + 1);
+        if (kb + 1 < kb1) {
+          f_next = factor(sw_idx, kb + 1);
+          if (SWIGLU) fu_next = factor(sw_idx_up, kb + 1);
+        }
         const bool w_ok = mbar_wait(tfull_bar(buf), bphase, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                               static_cast<uint32_t>(buf * BN + h * C::kEpiCols);
+        const uint32_t tcol0 = static_cast<uint32_t>(buf * BN + h * (SWIGLU ? 64 : C::kEpiCols));
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + tcol0;
         if constexpr (C::kSplitRegs) {
           // 64-column single-instruction loads (fewer tcgen05 instructions per
           // K-block than 32-column ones), then packed FP32x2 FMAs.
+          constexpr uint32_t kStep = SWIGLU ? BN / 2 : 64;
 #pragma unroll
           for (int c = 0; c < C::kEpiCols / 64; ++c) {
             float v[64];
-            tmem_ld64(taddr + 64u * c, v);
+            tmem_ld64(taddr + kStep * c, v);
+            const float2 fc = (SWIGLU && c == 1) ? make_float2(fu, fu) : f2;
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              acc[32 * c + j] = __ffma2_rn(make_float2(v[2 * j], v[2 * j + 1]), f2, acc[32 * c + j]);
+              acc[32 * c + j] = __ffma2_rn(make_float2(v[2 * j], v[2 * j + 1]), fc, acc[32 * c + j]);
           }
           tc_fence_before();
           __syncwarp();
@@ -603,6 +654,59 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
           }
         }
         if (ew == 0 && lane == 0) p.ws_counters[t] = 0;  // leave the workspace clean
+      }
+      if constexpr (SWIGLU) {
+        // Fused dense-FFN glue: h = bf16(silu(bf16(gate)) * bf16(up)), then the
+        // 1x128 quantization of h. A group is one row's 128 tile columns,
+        // split over this thread (64) and the thread of the other warpgroup
+        // with the same row; they swap maxima through shared memory. All
+        // epilogue warps reach both barriers whatever their `ok`.
+        float* xchg = reinterpret_cast<float*>(base_ptr + C::kOffStg);  // [2][BM] row maxima
+        const int col0 = h * 64;
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int cc = col0 + 2 * j;
+          float h0 = silu_mul_bf16_round(bf16_round(acc[j].x), bf16_round(acc[32 + j].x));
+          float h1 = silu_mul_bf16_round(bf16_round(acc[j].y), bf16_round(acc[32 + j].y));
+          if (cc >= tl.n_valid) h0 = 0.0f;
+          if (cc + 1 >= tl.n_valid) h1 = 0.0f;
+          acc[j] = make_float2(h0, h1);
+          amax = fmaxf(amax, fmaxf(fabsf(h0), fabsf(h1)));
+        }
+        xchg[h * BM + row_in_tile] = amax;
+        named_bar_sync(1, 32 * C::kEpiWarps);
+        amax = fmaxf(amax, xchg[(h ^ 1) * BM + row_in_tile]);
+        named_bar_sync(1, 32 * C::kEpiWarps);  // both read before the next tile rewrites them
+        if (ok && row_ok) {
+          const float sc = group_scale(amax);
+          const float rc = __frcp_rn(sc);
+          uint8_t* dst = p.q_h + arow * p.ldq + tl.n_out0 + col0;
+          const bool full = p.vec_store && col0 + 64 <= tl.n_valid;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {  // 16 codes at a time
+            uint32_t wq[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int j = 8 * i + 2 * k;
+              const uint16_t lo = f32x2_to_e4m3x2(div_by_scale(acc[j].x, sc, rc),
+                                                  div_by_scale(acc[j].y, sc, rc));
+              const uint16_t hi = f32x2_to_e4m3x2(div_by_scale(acc[j + 1].x, sc, rc),
+                                                  div_by_scale(acc[j + 1].y, sc, rc));
+              wq[k] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+            }
+            if (full) {
+              reinterpret_cast<uint4*>(dst)[i] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                if (col0 + 16 * i + e < tl.n_valid)
+                  dst[16 * i + e] = static_cast<uint8_t>(wq[e >> 2] >> (8 * (e & 3)));
+            }
+          }
+          if (h == 0) p.s_h[arow * p.sh_sm + (tl.n_out0 / 128) * p.sh_skb] = sc;
+        }
+        continue;
       }
       if (!ok) continue;
       // BF16 tile store: stage 32 rows x 32 columns through shared memory so
@@ -688,11 +792,11 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED>::kThreads, 1)
   }
 }
 
-template <int BN, int STAGES, bool W8A16, bool GROUPED>
+template <int BN, int STAGES, bool W8A16, bool GROUPED, bool SWIGLU = false>
 int launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int work_items,
            void* stream) {
-  using C = Cfg<BN, STAGES, W8A16, GROUPED>;
-  auto kernel = gemm_kernel<BN, STAGES, W8A16, GROUPED>;
+  using C = Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>;
+  auto kernel = gemm_kernel<BN, STAGES, W8A16, GROUPED, SWIGLU>;
   if constexpr (C::kSplitRegs) {
     // setmaxnreg.inc waits until the CTA's launch allocation can cover the
     // request, so the split is only safe if the kernel was built with exactly
@@ -914,6 +1018,112 @@ int launch_grouped_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_
   }
   // the work-item count is only known on the device: launch every resident cluster
   return launch<kBN8, kStages8, false, true>(ta, tb, p, 0x7FFFFFFF, stream);
+}
+
+size_t gemm_w8a8_swiglu_workspace_bytes(int64_t M, int64_t I, int sms) {
+  const int64_t m_tiles = (M + BM - 1) / BM;
+  return sk_workspace_bytes(m_tiles * ((I + 127) / 128), sms, kBN8);
+}
+
+size_t grouped_w8a8_swiglu_workspace_bytes(int64_t total_M, int32_t G, int64_t I, int sms) {
+  const int64_t tiles = ((total_M + BM - 1) / BM + G) * ((I + 127) / 128);
+  return sk_workspace_bytes(tiles, sms, kBN8);
+}
+
+namespace {
+
+// Shared part of the fused gate/up + SiLU*up + 1x128 quant launches.
+void fill_swiglu(GemmParams& p, int64_t I, void* q_h, int64_t ldq, float* s_h, int64_t sh_sm,
+                 int64_t sh_skb) {
+  p.q_h = static_cast<uint8_t*>(q_h);
+  p.ldq = ldq;
+  p.s_h = s_h;
+  p.sh_sm = sh_sm;
+  p.sh_skb = sh_skb;
+  p.up_row0 = static_cast<int32_t>(I);
+  p.up_sbase = static_cast<int32_t>((I + 127) / 128);
+  p.vec_store = (aligned16(q_h) && ldq % 16 == 0) ? 1 : 0;
+}
+
+}  // namespace
+
+int launch_gemm_w8a8_swiglu(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
+                            const void* w, const void* w_scale, int32_t w_scale_dtype, int64_t M,
+                            int64_t I, int64_t K, void* q_h, int64_t ldq, float* s_h,
+                            int64_t sh_sm, int64_t sh_skb, void* workspace, size_t ws_bytes,
+                            void* stream) {
+  if (K % 16 != 0 || !aligned16(q_a) || !aligned16(w)) return BFP8_ERR_UNSUPPORTED;
+  if (!fits_i32(M) || !fits_i32(2 * I) || !fits_i32(K)) return BFP8_ERR_UNSUPPORTED;
+  if (sa_sm < 0 || sa_skb < 0 || sh_sm < 0 || sh_skb < 0) return BFP8_ERR_INVALID_ARG;
+  CUtensorMap ta, tb;
+  int rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_a, K, M, K, BK, BM,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != BFP8_OK) return rc;
+  // gate and up halves of a B tile are separate 128-row boxes
+  rc = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, 2 * I, K, BK, kBN8 / 2,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != BFP8_OK) return rc;
+  GemmParams p{};
+  p.M = static_cast<int32_t>(M);
+  p.K = static_cast<int32_t>(K);
+  p.Kb = static_cast<int32_t>((K + BK - 1) / BK);
+  p.s_a = s_a;
+  p.sa_sm = sa_sm;
+  p.sa_skb = sa_skb;
+  p.s_w = w_scale;
+  p.sw_f32 = w_scale_dtype == BFP8_DT_F32;
+  // tiles walk h's I columns 128 at a time: one member of I rows
+  MemberTable mt;
+  mt.count = 1;
+  mt.n0[0] = 0;
+  mt.rows[0] = I;
+  mt.sbase[0] = 0;
+  mt.scale_rows = (I + 127) / 128;
+  rc = fill_members(p, mt, kBN8 / 2, 1, M, nullptr, 0);
+  if (rc != BFP8_OK) return rc;
+  fill_swiglu(p, I, q_h, ldq, s_h, sh_sm, sh_skb);
+  rc = sk_setup(p, p.total_tiles, kBN8, workspace, ws_bytes, stream);
+  if (rc != BFP8_OK) return rc;
+  return launch<kBN8, kStages8, false, false, true>(ta, tb, p, p.total_tiles, stream);
+}
+
+int launch_grouped_w8a8_swiglu(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
+                               const void* w, const void* w_scale, int32_t w_scale_dtype,
+                               const int32_t* offsets, int32_t G, int64_t total_M, int64_t I,
+                               int64_t K, void* q_h, int64_t ldq, float* s_h, int64_t sh_sm,
+                               int64_t sh_skb, void* workspace, size_t ws_bytes, void* stream) {
+  if (K % 16 != 0 || !aligned16(q_a) || !aligned16(w)) return BFP8_ERR_UNSUPPORTED;
+  if (!fits_i32(total_M) || !fits_i32(2 * I) || !fits_i32(K)) return BFP8_ERR_UNSUPPORTED;
+  if (G < 1 || G > kMaxExperts) return BFP8_ERR_INVALID_ARG;
+  if (sa_sm < 0 || sa_skb < 0 || sh_sm < 0 || sh_skb < 0) return BFP8_ERR_INVALID_ARG;
+  CUtensorMap ta, tb;
+  int rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_a, K, total_M, K, BK, BM,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != BFP8_OK) return rc;
+  rc = make_tmap_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, 2 * I, G, K, 2 * I * K, BK,
+                    kBN8 / 2, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != BFP8_OK) return rc;
+  GemmParams p{};
+  p.M = static_cast<int32_t>(total_M);
+  p.K = static_cast<int32_t>(K);
+  p.Kb = static_cast<int32_t>((K + BK - 1) / BK);
+  p.s_a = s_a;
+  p.sa_sm = sa_sm;
+  p.sa_skb = sa_skb;
+  p.s_w = w_scale;
+  p.sw_f32 = w_scale_dtype == BFP8_DT_F32;
+  // each expert's grid stacks the gate member's rows over the up member's
+  p.sw_expert_stride = 2 * ((I + 127) / 128) * static_cast<int64_t>(p.Kb);
+  p.offsets = offsets;
+  p.G = G;
+  p.N = static_cast<int32_t>(I);
+  p.n_tiles = static_cast<int32_t>((I + 127) / 128);
+  p.n_members = 1;
+  fill_swiglu(p, I, q_h, ldq, s_h, sh_sm, sh_skb);
+  const int64_t tile_bound = ((total_M + BM - 1) / BM + G) * p.n_tiles;
+  rc = sk_setup(p, tile_bound, kBN8, workspace, ws_bytes, stream);
+  if (rc != BFP8_OK) return rc;
+  return launch<kBN8, kStages8, false, true, true>(ta, tb, p, 0x7FFFFFFF, stream);
 }
 
 int gemm_read_clear_error() {

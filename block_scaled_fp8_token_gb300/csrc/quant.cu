@@ -11,14 +11,11 @@
 // cvt.rn.satfinite.e4m3x2.f32 applied to the correctly rounded quotient x / s,
 // which makes the result bit-exact against the CPU definition. All 128
 // elements of a group share the divisor, so the quotient is formed from one
-// correctly rounded reciprocal y = RN(1/s) per group and a remainder
-// correction per element (Markstein's theorem: with y within half an ulp of
-// 1/s and q0 = RN(x*y) within one ulp of x/s, r = x - q0*s is exact under
-// FMA and RN(q0 + r*y) = RN(x/s)). The theorem assumes no underflow; a
-// quotient in the FP32 subnormal range is below 2^-126, far under half the
-// smallest E4M3 step (2^-10), so its code is 0 either way.
+// correctly rounded reciprocal per group and a remainder correction per
+// element (act_math.cuh).
 #include "bfp8_internal.h"
 #include "ptx.cuh"
+#include "act_math.cuh"
 
 namespace bfp8 {
 namespace {
@@ -26,21 +23,6 @@ namespace {
 using namespace dev;
 
 constexpr int kThreads = 256;
-
-// h = bf16(silu(g) * u). SiLU only feeds a BF16 rounding, so the fast
-// exponential and division (a few FP32 ulps) change h only where the product
-// sits within those ulps of a BF16 rounding boundary.
-__device__ __forceinline__ float silu_mul_bf16_round(float g, float u) {
-  const float s = __fdividef(g, 1.0f + __expf(-g));
-  return __bfloat162float(__float2bfloat16_rn(s * u));
-}
-
-// RN(x / s) given y = RN(1 / s): one remainder correction (Markstein).
-__device__ __forceinline__ float div_by_scale(float x, float s, float y) {
-  const float q0 = x * y;
-  const float r = fmaf(-q0, s, x);
-  return fmaf(r, y, q0);
-}
 
 // SILU == false: x is [M, K] with row stride ld; values are x[m, c].
 // SILU == true : x is [M, 2K] with row stride ld; values are
@@ -115,7 +97,7 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(
 #pragma unroll
       for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
       if (item >= total) continue;
-      const float sc = fmaxf(amax, 1e-10f) / 448.0f;
+      const float sc = group_scale(amax);
       const float rc = __frcp_rn(sc);
       const int64_t m = item / Kb, g = item - m * Kb;
       const int64_t c = g * 128 + hl * 8;

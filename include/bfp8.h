@@ -124,8 +124,8 @@ int bfp8_validate_grid(const bfp8_weight_desc* desc, char* msg, size_t msg_len);
  *    activation scales, as per_token_group_quant_fp8 computes them]
  * For token m and group g (columns [128g, min(128g+128, K))):
  *   amax = max|x|, s = max(amax, 1e-10f) / 448.0f, q = RNE_satfinite_e4m3(x / s)
- * with IEEE float32 division. This is bit-exact with the CPU oracle for finite
- * inputs.
+ * where s and x / s are the correctly rounded float32 quotients (IEEE
+ * division). This is bit-exact with the CPU oracle for finite inputs.
  *   x_bf16  [M, K] BF16, row stride ldx >= K (elements)
  *   q_e4m3  [M, K] E4M3 bytes, row stride ldq >= K (bytes)
  *   scales  float32, element (m, g) at scales[m*s_stride_m + g*s_stride_kb];
@@ -312,6 +312,56 @@ int bfp8_grouped_linear(const void* q_a, const float* s_a, int64_t s_stride_m, i
                         const int32_t* offsets_dev, int32_t G, int64_t total_M, int64_t N,
                         int64_t K, void* y_bf16, int64_t ldy, void* workspace, size_t ws_bytes,
                         void* stream);
+
+/* ---- a10 fused into the gate/up projection --------------------------------- */
+/*
+ * bfp8_linear_w8a8_silu_quant -- the dense-FFN gate/up projection with
+ * SiLU(gate)*up and the 1x128 quantization of h in its epilogue, so that the
+ * BF16 [M, 2I] gate/up output never reaches memory.
+ *   [Module w8a8_prefill, first paragraph: the gate/up/down GEMM arm]
+ * The result equals bfp8_linear_w8a8 with members {I, I} writing gu [M, 2I]
+ * in BF16, followed by bfp8_silu_mul_act_quant(gu):
+ *   g = bf16_rn(acc_gate), u = bf16_rn(acc_up), h = bf16_rn(silu(g) * u),
+ *   then per (token m, 128 columns of h): s = max(max|h|, 1e-10f) / 448,
+ *   q_h = RNE_satfinite_e4m3(h / s).
+ *   q_a, s_a, s_stride_*  as bfp8_linear_w8a8 (K columns)
+ *   w_e4m3   [2I, K] E4M3: the gate rows 0..I-1 stacked over the up rows
+ *            I..2I-1, row stride K bytes
+ *   w_scale  [2*ceil(I/128), ceil(K/128)]: the gate member's grid stacked over
+ *            the up member's (member-local origins), BF16 or F32
+ *   q_h      [M, I] E4M3, row stride ldq >= I bytes
+ *   s_h      float32 scales of h, (m, g) at s_h[m*sh_stride_m + g*sh_stride_kb]
+ *   workspace, ws_bytes  optional stream-K scratch as bfp8_linear_w8a8, sized
+ *            by bfp8_linear_w8a8_silu_quant_workspace()
+ * Requirements: K % 16 == 0; q_a and w_e4m3 16-byte aligned. M == 0 is a no-op.
+ */
+size_t bfp8_linear_w8a8_silu_quant_workspace(int64_t M, int64_t I, int64_t K);
+int bfp8_linear_w8a8_silu_quant(const void* q_a, const float* s_a, int64_t s_stride_m,
+                                int64_t s_stride_kb, const void* w_e4m3, const void* w_scale,
+                                int32_t w_scale_dtype, int64_t M, int64_t I, int64_t K,
+                                void* q_h, int64_t ldq, float* s_h, int64_t sh_stride_m,
+                                int64_t sh_stride_kb, void* workspace, size_t ws_bytes,
+                                void* stream);
+
+/*
+ * bfp8_grouped_linear_silu_quant -- the MoE expert gate/up projection with the
+ * same fused epilogue, over the token-offset table of bfp8_grouped_linear.
+ *   [Module w8a8_prefill, "WHY": the MoE expert path; first paragraph: the
+ *    gate/up/down arm]
+ *   w_e4m3   [G, 2I, K] E4M3 (each expert: gate rows over up rows)
+ *   w_scale  [G, 2*ceil(I/128), ceil(K/128)] (each expert: gate grid over up grid)
+ *   q_h      [total_M, I] E4M3, row stride ldq; s_h as above
+ *   other arguments, the workspace (sized by
+ *   bfp8_grouped_linear_silu_quant_workspace()) and requirements as
+ *   bfp8_grouped_linear.
+ */
+size_t bfp8_grouped_linear_silu_quant_workspace(int64_t total_M, int32_t G, int64_t I, int64_t K);
+int bfp8_grouped_linear_silu_quant(const void* q_a, const float* s_a, int64_t s_stride_m,
+                                   int64_t s_stride_kb, const void* w_e4m3, const void* w_scale,
+                                   int32_t w_scale_dtype, const int32_t* offsets_dev, int32_t G,
+                                   int64_t total_M, int64_t I, int64_t K, void* q_h, int64_t ldq,
+                                   float* s_h, int64_t sh_stride_m, int64_t sh_stride_kb,
+                                   void* workspace, size_t ws_bytes, void* stream);
 
 /* ---- diagnostics ---------------------------------------------------------- */
 /*
