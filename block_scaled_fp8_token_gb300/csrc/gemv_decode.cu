@@ -17,11 +17,18 @@
 //     tokens). 160 KB stays in flight per SM, which covers HBM latency.
 //   * Warps 1-8 work in four pairs. Unit i goes to pair i % 4, and each warp
 //     of the pair owns 64 of the 128 rows. A warp reads 16-byte chunks of its
-//     rows, decodes E4M3 -> BF16 in registers, and runs the legacy
-//     m16n8k16 BF16 MMA with tokens as the n dimension. It multiplies the
-//     per-K-block partial by that block's scale in FP32 registers. The
-//     permutation of K inside a 64-wide half is the same for both operands,
-//     so the sums are unchanged.
+//     rows and runs the legacy m16n8k16 MMA with tokens as the n dimension,
+//     on F16 operands:
+//       - E4M3 -> F16 is one exact conversion per two weights.
+//       - Each token's 128 BF16 values of the K-block are multiplied by a
+//         power of two 2^e chosen so that their maximum lies in [2^14, 2^15),
+//         then converted to F16. A BF16 significand (8 bits) fits F16's 11,
+//         so every value within 28 binades of its row's maximum is carried
+//         exactly, and every product x * w is formed exactly, as with BF16
+//         operands.
+//     The per-K-block FP32 partial is multiplied by 2^-e (exact) and by the
+//     block's weight scale. The permutation of K inside a 64-wide half is the
+//     same for both operands, so the sums are unchanged.
 //   * At the end of a row tile's segment, the four pairs' accumulators are
 //     summed through shared memory. A CTA that owns a whole row tile writes
 //     BF16 directly. Partial tiles go to the workspace, and the last CTA to
@@ -223,6 +230,36 @@ __global__ void __launch_bounds__(kThreads, 1)
               xf[half][tb][0] = v0.x; xf[half][tb][1] = v0.y; xf[half][tb][2] = v0.z; xf[half][tb][3] = v0.w;
               xf[half][tb][4] = v1.x; xf[half][tb][5] = v1.y; xf[half][tb][6] = v1.z; xf[half][tb][7] = v1.w;
             }
+          // BF16 -> F16 with a power of two per token: the quad of lanes
+          // holding token row 8*tb + g finds the row's max |x| exponent E,
+          // scales by 2^e, e = 141 - E (so the max lands in [2^14, 2^15)),
+          // and hands 2^-e to the lanes whose accumulator columns are that
+          // token. Non-negative BF16 patterns order like their values.
+          float xinv[NTB][2];
+#pragma unroll
+          for (int tb = 0; tb < NTB; ++tb) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+#pragma unroll
+              for (int j = 0; j < 8; ++j) m = __vmaxu2(m, xf[half][tb][j] & 0x7FFF7FFFu);
+            m = max(m & 0xFFFFu, m >> 16);
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            const int e = min(max(141 - static_cast<int>((m >> 7) & 0xFFu), -126), 126);
+            const float up = __int_as_float((e + 127) << 23);
+            const float dn = __int_as_float((127 - e) << 23);
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const uint32_t w = xf[half][tb][j];
+                xf[half][tb][j] = f32x2_to_f16x2(__uint_as_float(w << 16) * up,
+                                                 __uint_as_float(w & 0xFFFF0000u) * up);
+              }
+            xinv[tb][0] = __shfl_sync(0xffffffffu, dn, 8 * t);       // token 8*tb + 2t
+            xinv[tb][1] = __shfl_sync(0xffffffffu, dn, 8 * t + 4);   // token 8*tb + 2t + 1
+          }
 #pragma unroll
           for (int rg = 0; rg < 4; ++rg) {
             float part[NTB][4];
@@ -240,20 +277,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t whw[4] = {wh.x, wh.y, wh.z, wh.w};
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
-                uint32_t a0, a1, a2, a3;
-                e4m3x4_to_bf16x4(wlw[j], a0, a2);
-                e4m3x4_to_bf16x4(whw[j], a1, a3);
+                const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(wlw[j] & 0xFFFFu));
+                const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(wlw[j] >> 16));
+                const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(whw[j] & 0xFFFFu));
+                const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(whw[j] >> 16));
 #pragma unroll
                 for (int tb = 0; tb < NTB; ++tb)
-                  mma_bf16_16816(part[tb], a0, a1, a2, a3, xf[half][tb][2 * j], xf[half][tb][2 * j + 1]);
+                  mma_f16_16816(part[tb], a0, a1, a2, a3, xf[half][tb][2 * j], xf[half][tb][2 * j + 1]);
               }
             }
 #pragma unroll
             for (int tb = 0; tb < NTB; ++tb) {
-              acc[rg][tb][0] = fmaf(part[tb][0], sc[rg][0], acc[rg][tb][0]);
-              acc[rg][tb][1] = fmaf(part[tb][1], sc[rg][0], acc[rg][tb][1]);
-              acc[rg][tb][2] = fmaf(part[tb][2], sc[rg][1], acc[rg][tb][2]);
-              acc[rg][tb][3] = fmaf(part[tb][3], sc[rg][1], acc[rg][tb][3]);
+              // undo the token scale first (exact), then apply the block scale
+              acc[rg][tb][0] = fmaf(part[tb][0] * xinv[tb][0], sc[rg][0], acc[rg][tb][0]);
+              acc[rg][tb][1] = fmaf(part[tb][1] * xinv[tb][1], sc[rg][0], acc[rg][tb][1]);
+              acc[rg][tb][2] = fmaf(part[tb][2] * xinv[tb][0], sc[rg][1], acc[rg][tb][2]);
+              acc[rg][tb][3] = fmaf(part[tb][3] * xinv[tb][1], sc[rg][1], acc[rg][tb][3]);
             }
           }
           __syncwarp();
