@@ -352,36 +352,76 @@ def run_ours(args, rank, world, local):
 
 
 def run_decode(bfp8, torch, dev, wgu, sgu, wdn, sdn, peaks):
-    """Decode GEMV (M in {1, 4, 16}) on the same weights: weight GB/s, L2
-    flushed between timed launches."""
+    """Decode GEMV (M in {1, 4, 16}) on the same weights: weight GB/s. The timed
+    launches rotate over enough copies of the weights (>= 2x L2) that no
+    launch finds its weights in L2; nothing is written between launches."""
     from block_scaled_fp8_token_gb300 import synth
 
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    res = {"metric": "weight GB/s (decode GEMV, W8A16 arithmetic)", "unit": "GB/s",
-           "l2": "flushed (512 MB write) before every timed launch", "shapes": {}}
+    l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    res = {"metric": "weight GB/s (decode GEMV, W8A16 arithmetic)", "unit": "GB/s", "shapes": {}}
     stream = torch.cuda.current_stream(dev)
     best = None
+    copies = {}
+    for name, w, s in (("gate_up", wgu, sgu), ("down", wdn, sdn)):
+        n = max(2, -(-2 * l2 // w.numel()))
+        copies[name] = [(w, s)] + [(w.clone(), s.clone()) for _ in range(n - 1)]
+    res["l2"] = (f"inputs larger than L2: each timed launch reads the next of "
+                 f"{len(copies['gate_up'])} (gate/up) or {len(copies['down'])} (down) weight "
+                 f"copies, >= 2x the {l2 >> 20} MB L2; no flush writes")
     for M in (1, 4, 16):
         row = {}
-        for name, w, s, members in (("gate_up", wgu, sgu, [INTER, INTER]), ("down", wdn, sdn, None)):
-            N, K = w.shape
+        for name, members in (("gate_up", [INTER, INTER]), ("down", None)):
+            ring = copies[name]
+            N, K = ring[0][0].shape
             x = synth.decode_tokens(100 + M, M, K).to(dev)
             y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
             ws = torch.empty(bfp8.bfp8_gemv_decode_workspace(M, N, K), dtype=torch.uint8, device=dev)
-            for _ in range(3):
-                bfp8.bfp8_gemv_decode(x, w, s, y, ws, member_rows=members, stream=stream)
+            def call(j):
+                w, s = ring[j % len(ring)]
+                bfp8.bfp8_gemv_decode(x, w, s, y, ws, member_rows=members, stream=g_stream)
+
+            # a CUDA graph of launches rotating over the copies: GPU time with
+            # the gaps between kernels, without the host's launch cost
+            g_stream = torch.cuda.Stream(dev)
+            g_stream.wait_stream(stream)
+            with torch.cuda.stream(g_stream):
+                for j in range(3):
+                    call(j)
+            torch.cuda.synchronize()
+            n_launch = 4 * len(ring)
             times = []
-            for _ in range(20):
-                flush.zero_()
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                bfp8.bfp8_gemv_decode(x, w, s, y, ws, member_rows=members, stream=stream)
-                e1.record(stream)
+            try:
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=g_stream):
+                    for j in range(n_launch):
+                        call(j)
+                run = graph.replay
+                res.setdefault("timing", "CUDA graph of 4 x copies bfp8_gemv_decode calls "
+                                         "(split-token kernel + GEMV each), replayed 5 times; "
+                                         "us = median replay time / launches")
+            except RuntimeError as exc:  # capture refused: eager back-to-back launches
+                graph = None
+
+                def run():
+                    for j in range(n_launch):
+                        call(j)
+                res["timing"] = f"eager back-to-back launches (graph capture failed: {exc})"
+            with torch.cuda.stream(g_stream):
+                for _ in range(2):
+                    run()
                 torch.cuda.synchronize()
-                times.append(e0.elapsed_time(e1))
-            us = statistics.median(times) * 1e3
-            nbytes = N * K + s.numel() * 2 + M * K * 2 + M * N * 2
+                for r in range(5):
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(g_stream)
+                    run()
+                    e1.record(g_stream)
+                    times.append((e0, e1))
+            torch.cuda.synchronize()
+            del graph
+            us = statistics.median(a.elapsed_time(b) for a, b in times) * 1e3 / n_launch
+            s0 = ring[0][1]
+            nbytes = N * K + s0.numel() * 2 + M * K * 2 + M * N * 2
             gbs = nbytes / (us * 1e-6) / 1e9
             row[name] = {"us": round(us, 2), "bytes": nbytes, "GB/s": round(gbs, 1),
                          "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
@@ -393,7 +433,8 @@ def run_decode(bfp8, torch, dev, wgu, sgu, wdn, sdn, peaks):
                        "frac": best["frac_hbm"], "traffic": ncu_traffic("gemv_gate_up_m16")[0],
                        "traffic_note": ncu_traffic("gemv_gate_up_m16")[1],
                        "peak_source": f"{peaks['source']} copy bandwidth"}
-    del flush
+    del copies
+    torch.cuda.empty_cache()
     return res
 
 

@@ -2,38 +2,43 @@
 //
 //   y[m, n] = sum_kb s_w[r(n), kb] * sum_{k in kb} x[m, k] * e4m3(W[n, k]),  1 <= M <= 16
 //
-// W8A16 arithmetic: BF16 tokens, E4M3 weights decoded exactly, FP32
-// accumulation, block multipliers applied inside the reduction [Qwen
-// checkpoints with block FP8 weights, paragraph 2]. The GB10 design on the
-// pages is an unfused per-projection GEMV [Module w8a8_prefill, "Reachability"].
+// W8A16 arithmetic: BF16 tokens, E4M3 weights, FP32 accumulation, block
+// multipliers applied inside the reduction [Qwen checkpoints with block FP8
+// weights, paragraph 2]. The GB10 design on the pages is an unfused
+// per-projection GEMV [Module w8a8_prefill, "Reachability"].
 //
-// Design for GB300:
+// Design for GB300: the weights go from HBM to the tensor cores untouched.
 //   * Work unit = 128 weight rows x one 128-wide K-block (16 KB of E4M3).
 //     There are ceil(N/128) * ceil(K/128) units. They are split into equal
 //     contiguous ranges over one persistent CTA per SM (stream-K), so every
 //     SM streams the same number of bytes whatever N and K are.
-//   * Warp 0 streams units into an 8-deep ring with TMA (128-byte swizzle):
-//     the weight tile plus the matching 128-column slice of x (up to 16
-//     tokens). 160 KB stays in flight per SM, which covers HBM latency.
-//   * Warps 1-8 work in four pairs. Unit i goes to pair i % 4, and each warp
-//     of the pair owns 64 of the 128 rows. A warp reads 16-byte chunks of its
-//     rows and runs the legacy m16n8k16 MMA with tokens as the n dimension,
-//     on F16 operands:
-//       - E4M3 -> F16 is one exact conversion per two weights.
-//       - Each token's 128 BF16 values of the K-block are multiplied by a
-//         power of two 2^e chosen so that their maximum lies in [2^14, 2^15),
-//         then converted to F16. A BF16 significand (8 bits) fits F16's 11,
-//         so every value within 28 binades of its row's maximum is carried
-//         exactly, and every product x * w is formed exactly, as with BF16
-//         operands.
-//     The per-K-block FP32 partial is multiplied by 2^-e (exact) and by the
-//     block's weight scale. The permutation of K inside a 64-wide half is the
-//     same for both operands, so the sums are unchanged.
-//   * At the end of a row tile's segment, the four pairs' accumulators are
-//     summed through shared memory. A CTA that owns a whole row tile writes
-//     BF16 directly. Partial tiles go to the workspace, and the last CTA to
-//     arrive sums the partials in CTA order (deterministic) and writes y. No
-//     CTA ever waits on another.
+//   * A small kernel first turns the tokens into the MMA's B operand, once
+//     per K-block. Token m's 128 values are multiplied by a power of two 2^e
+//     that puts their maximum in [2^7, 2^8). Each scaled value v is written as
+//     two E4M3 terms, hi = e4m3(v) and lo = e4m3(v - hi), in rows m and 16 + m
+//     of a 32 x 128 byte tile; 2^-e goes to a small table. A BF16 significand
+//     has 8 bits, hi keeps 4 and the remainder needs at most 4, so
+//     hi + lo == v exactly for every value within 2^-10 of the maximum.
+//     Smaller values are carried to within 2^-10 in the scaled units, that
+//     is max|x| * 2^-18. The GEMV is launched behind it as a programmatic
+//     dependent launch: it starts streaming weights at once and waits for
+//     the token tiles (griddepcontrol.wait) only before it first needs them.
+//   * Warp 4 streams units into an 8-slot ring with TMA: the weight tile and
+//     the K-block's token tile, both with the 128-byte swizzle of the tcgen05
+//     K-major layout. Slots are filled and released in groups of kGroup
+//     consecutive units under one barrier: HBM delivers several 16 KB tiles
+//     per barrier round trip much faster than one.
+//   * Warp 5 issues four tcgen05.mma kind::f8f6f4 (M = 128 weight rows,
+//     N = 32, K = 32) per unit into one of eight 32-column TMEM buffers:
+//     exact E4M3 products, FP32 accumulation.
+//   * Warps 0-3 (one TMEM lane quarter each, one weight row per thread) add
+//     the hi and lo columns, undo 2^e (exact), apply the block's weight scale
+//     and accumulate the 16 token sums in FP32 registers.
+//   * A CTA that owns a whole row tile writes BF16 directly. Partial tiles
+//     go to the workspace. Warp 6 publishes each partial with one
+//     acquire-release atomic on the tile's counter while the epilogue goes
+//     on; the CTA that arrives last on a tile sums its partials in CTA order
+//     (deterministic) and writes y at the end. No CTA ever waits on another.
 #include <mutex>
 
 #include "bfp8_internal.h"
@@ -46,27 +51,36 @@ using namespace dev;
 
 __device__ int g_gemv_err;
 
-constexpr int kRows = 128;          // weight rows per unit
-constexpr int kStages = 8;          // must be a multiple of 4 (pairs own stages s, s+4)
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = 32 * (1 + kConsumerWarps);
-constexpr uint32_t kWBytes = kRows * 128;
-constexpr uint32_t kRedBytes = 4 * kRows * 16 * 4;
+constexpr int kRows = 128;           // weight rows per unit (the MMA's M)
+#ifndef BFP8_GEMV_GROUP
+#define BFP8_GEMV_GROUP 4
+#endif
+#ifndef BFP8_GEMV_SLOTS
+#define BFP8_GEMV_SLOTS 8
+#endif
+constexpr int kStages = BFP8_GEMV_SLOTS;  // unit slots in shared memory
+constexpr int kGroup = BFP8_GEMV_GROUP;  // consecutive units per fill / release
+constexpr int kGroups = kStages / kGroup;
+constexpr int kTBufs = 8;            // TMEM partial buffers, 32 columns each
+constexpr int kThreads = 224;        // warps 0-3 epilogue, 4 producer, 5 MMA, 6 publisher
+constexpr int kProducerWarp = 4, kMmaWarp = 5, kPublisherWarp = 6;
+constexpr int kBarPartial = 2, kBarFinal = 3;  // named barriers: epilogue + publisher
+constexpr uint32_t kTmemCols = kTBufs * 32;
+constexpr uint32_t kWBytes = kRows * 128;            // E4M3 weight tile
+constexpr uint32_t kXTile = 32 * 128;                // token tile: hi rows 0-15, lo rows 16-31
+constexpr uint32_t kOffXTile = kWBytes;
+constexpr uint32_t kStage = kWBytes + kXTile;
+constexpr uint32_t kTmaBytes = kStage;
+constexpr uint32_t kOffBar = kStages * kStage;
+constexpr uint32_t kNumBars = 2 * kGroups + 2 * kTBufs + 1;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag, last flags [2]
+constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;
+static_assert(kThreads == 32 * (kPublisherWarp + 1), "one warp per role after the epilogue");
+constexpr uint32_t kIdesc = idesc_e4m3(kRows, 32);
 constexpr unsigned long long kDrainLimitNs = 100000000ull;
-
-template <int NTB>
-struct GCfg {
-  static constexpr int kMB = 8 * NTB;                        // token rows per x half-tile
-  static constexpr uint32_t kXHalf = kMB * 128;
-  static constexpr uint32_t kStage = kWBytes + 2 * kXHalf;   // multiple of 1024
-  static constexpr uint32_t kTmaBytes = kStage;
-  static constexpr uint32_t kOffRed = kStages * kStage;
-  static constexpr uint32_t kOffBar = kOffRed + kRedBytes;
-  static constexpr uint32_t kOffMisc = kOffBar + 2 * kStages * 8;
-  static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;
-  static_assert(kStage % 1024 == 0, "stages must keep 1024-byte alignment");
-  static_assert(kSmemBytes <= 232448, "shared memory budget");
-};
+static_assert(kStage % 1024 == 0 && kOffXTile % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(kStages % kGroup == 0, "slot groups must tile the ring");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct GemvParams {
   int32_t M, N, K, Kb, RT;
@@ -80,6 +94,7 @@ struct GemvParams {
   int64_t ldy;
   int32_t* counters;  // [RT], zero at kernel start
   float* partials;    // [grid][2][128][16]
+  const float* xinv;  // [Kb][16]: 2^-e of each token's K-block
 };
 
 BFP8_DEV int64_t unit_begin(const GemvParams& p, int64_t c) { return (c * p.U) / p.grid; }
@@ -115,285 +130,440 @@ BFP8_DEV void raise_abort(volatile int* abort_flag) {
   atomicExch(&g_gemv_err, static_cast<int>(BFP8_ERR_TIMEOUT));
 }
 
-template <int NTB>
+BFP8_DEV float2 f16x2_bits_to_f32x2(uint32_t h) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+BFP8_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+BFP8_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// One CTA per K-block, 64 threads: thread t handles token t / 4 and the 32
+// values [32*(t%4), +32) of the block. Writes the hi/lo E4M3 rows of the
+// block's 32 x 128 token tile (row-major; TMA applies the swizzle on load)
+// and 2^-e per token. Tokens past M get zero rows.
+// It also clears the GEMV's split-tile counters; the GEMV touches them only
+// after its griddepcontrol.wait.
+__global__ void __launch_bounds__(64) gemv_split_tokens_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t ldx, int32_t M, int32_t K,
+    uint8_t* __restrict__ xtile, float* __restrict__ xinv, int32_t* __restrict__ counters,
+    int32_t n_counters) {
+  pdl_launch_dependents();  // let the GEMV start streaming weights now
+  const int kb = blockIdx.x;
+  for (int i = kb * 64 + threadIdx.x; i < n_counters; i += gridDim.x * 64) counters[i] = 0;
+  const int tok = threadIdx.x >> 2, q4 = threadIdx.x & 3;
+  const int c0 = kb * 128 + 32 * q4;
+  uint32_t xw[16];
+  if (tok < M && c0 + 32 <= K) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(tok) * ldx + c0);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 v = src[c];
+      xw[4 * c] = v.x; xw[4 * c + 1] = v.y; xw[4 * c + 2] = v.z; xw[4 * c + 3] = v.w;
+    }
+  } else {
+    const uint16_t* xr = reinterpret_cast<const uint16_t*>(x) + static_cast<int64_t>(tok) * ldx;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t lo = (tok < M && c0 + 2 * j < K) ? xr[c0 + 2 * j] : 0u;
+      const uint32_t hi = (tok < M && c0 + 2 * j + 1 < K) ? xr[c0 + 2 * j + 1] : 0u;
+      xw[j] = lo | (hi << 16);
+    }
+  }
+  // the row's max |x| (non-negative BF16 patterns order like their values)
+  uint32_t m = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) m = __vmaxu2(m, xw[j] & 0x7FFF7FFFu);
+  m = max(m & 0xFFFFu, m >> 16);
+  m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+  const int e = min(max(134 - static_cast<int>((m >> 7) & 0xFFu), -126), 126);
+  const float up = __int_as_float((e + 127) << 23);
+  uint32_t hw[8], lw[8];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float v0 = __uint_as_float(xw[j] << 16) * up;
+    const float v1 = __uint_as_float(xw[j] & 0xFFFF0000u) * up;
+    const uint16_t hi = f32x2_to_e4m3x2(v0, v1);
+    const float2 hf = f16x2_bits_to_f32x2(e4m3x2_to_f16x2(hi));
+    const uint16_t lo = f32x2_to_e4m3x2(v0 - hf.x, v1 - hf.y);
+    if (j & 1) {
+      hw[j >> 1] |= static_cast<uint32_t>(hi) << 16;
+      lw[j >> 1] |= static_cast<uint32_t>(lo) << 16;
+    } else {
+      hw[j >> 1] = hi;
+      lw[j >> 1] = lo;
+    }
+  }
+  uint4* dh = reinterpret_cast<uint4*>(xtile + (static_cast<int64_t>(kb) * 32 + tok) * 128 + 32 * q4);
+  uint4* dl = reinterpret_cast<uint4*>(xtile + (static_cast<int64_t>(kb) * 32 + 16 + tok) * 128 + 32 * q4);
+  dh[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  dh[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+  dl[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  dl[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+  if (q4 == 0) xinv[kb * 16 + tok] = __int_as_float((127 - e) << 23);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                 const __grid_constant__ GemvParams p) {
-  using C = GCfg<NTB>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - raw_u32);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t bar0 = base + C::kOffBar;
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::kOffMisc);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(base_ptr + C::kOffMisc + 4);
-  float* red = reinterpret_cast<float*>(base_ptr + C::kOffRed);
+  const uint32_t bar0 = base + kOffBar;
+  auto full_bar = [&](int g) { return bar0 + 8u * g; };
+  auto empty_bar = [&](int g) { return bar0 + 8u * (kGroups + g); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kGroups + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kGroups + kTBufs + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kGroups + 2 * kTBufs);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + kOffMisc + 4);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(base_ptr + kOffMisc + 8);
 
   const int64_t ub = unit_begin(p, blockIdx.x);
   const int64_t ue = unit_begin(p, blockIdx.x + 1);
+  const int64_t nu = ue - ub;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 2);
+  // The producer thread sets up the barriers and starts the first group's
+  // weight loads before the CTA-wide sync, so HBM is busy from the start.
+  auto unit_rt_kb = [&](int64_t u, int& rt, int& kb) {
+    rt = static_cast<int>(u / p.Kb);
+    kb = static_cast<int>(u - static_cast<int64_t>(rt) * p.Kb);
+  };
+  const int64_t n_first = min(static_cast<int64_t>(kStages), nu);  // units of the ring's first pass
+  if (warp == kProducerWarp && lane == 0) {
+    for (int g = 0; g < kGroups; ++g) {
+      mbar_init(full_bar(g), 1);
+      mbar_init(empty_bar(g), 1);
     }
+    for (int b = 0; b < kTBufs; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 4);
+    }
+    mbar_init(drain_bar, 1);
     *abort_flag = 0;
     mbar_fence_init();
-  }
-  if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
+    for (int64_t i0 = 0; i0 < n_first; i0 += kGroup) {
+      const int g = static_cast<int>(i0 / kGroup);
+      const int n_in = static_cast<int>(min(static_cast<int64_t>(kGroup), nu - i0));
+      mbar_arrive_expect_tx(full_bar(g), kTmaBytes * n_in);
+      for (int j = 0; j < n_in; ++j) {
+        int rt, kb;
+        unit_rt_kb(ub + i0 + j, rt, kb);
+        tma_load_2d(base + (i0 + j) * kStage, &tmW, kb * 128, rt * kRows, full_bar(g));
+      }
+    }
   }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t armed = 0, armed_phase = 0;
       bool ok = true;
-      for (int64_t i = 0; ub + i < ue; ++i) {
-        const int s = static_cast<int>(i % kStages);
-        const uint32_t ph = static_cast<uint32_t>((i / kStages) & 1);
-        if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) { ok = false; break; }
-        const int64_t u = ub + i;
-        const int rt = static_cast<int>(u / p.Kb);
-        const int kb = static_cast<int>(u - static_cast<int64_t>(rt) * p.Kb);
-        const uint32_t sW = base + s * C::kStage;
-        const uint32_t sX = sW + kWBytes;
-        mbar_arrive_expect_tx(full_bar(s), C::kTmaBytes);
-        tma_load_2d(sW, &tmW, kb * 128, rt * kRows, full_bar(s));
-        tma_load_2d(sX, &tmX, kb * 128, 0, full_bar(s));
-        tma_load_2d(sX + C::kXHalf, &tmX, kb * 128 + 64, 0, full_bar(s));
-        armed |= 1u << s;
-        armed_phase = (armed_phase & ~(1u << s)) | (ph << s);
+      bool tokens_ready = false;
+      for (int64_t i0 = 0; i0 < nu; i0 += kGroup) {
+        const int g = static_cast<int>((i0 / kGroup) % kGroups);
+        const uint32_t ph = static_cast<uint32_t>((i0 / kStages) & 1);
+        const int n_in = static_cast<int>(min(static_cast<int64_t>(kGroup), nu - i0));
+        if (i0 >= n_first) {  // the first pass's weight loads went out before the CTA sync
+          if (!mbar_wait_sleep(empty_bar(g), ph ^ 1u, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(full_bar(g), kTmaBytes * n_in);
+          for (int j = 0; j < n_in; ++j) {
+            int rt, kb;
+            unit_rt_kb(ub + i0 + j, rt, kb);
+            tma_load_2d(base + (g * kGroup + j) * kStage, &tmW, kb * 128, rt * kRows, full_bar(g));
+          }
+        }
+        // the token tiles come from the split kernel this grid depends on
+        if (!tokens_ready) {
+          pdl_wait();
+          tokens_ready = true;
+        }
+        for (int j = 0; j < n_in; ++j) {
+          const int64_t u = ub + i0 + j;
+          const int kb = static_cast<int>(u % p.Kb);
+          tma_load_2d(base + (g * kGroup + j) * kStage + kOffXTile, &tmX, 0, kb * 32, full_bar(g));
+        }
+        armed |= 1u << g;
+        armed_phase = (armed_phase & ~(1u << g)) | (ph << g);
       }
       if (!ok) raise_abort(abort_flag);
-      for (int s = 0; s < kStages; ++s)
-        if ((armed >> s) & 1u) wait_bounded(full_bar(s), (armed_phase >> s) & 1u, kDrainLimitNs);
+      // no copy may still be landing in shared memory when the CTA exits
+      for (int g = 0; g < kGroups; ++g)
+        if ((armed >> g) & 1u) wait_bounded(full_bar(g), (armed_phase >> g) & 1u, kDrainLimitNs);
     }
-  } else {
-    // ------------------------------------------------------------ consumers
-    const int cw = warp - 1;
-    const int pair = cw >> 1, hw = cw & 1;
-    const int g = lane >> 2, t = lane & 3;
-    const int ct = threadIdx.x - 32;  // 0..255
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    // Converged warp; one elected lane issues the MMAs and their commits.
+    bool ok = true;
+    for (int64_t i = 0; i < nu; ++i) {
+      const int s = static_cast<int>(i % kStages);
+      const uint32_t ph = static_cast<uint32_t>((i / kStages) & 1);
+      const int b = static_cast<int>(i % kTBufs);
+      const uint32_t bph = static_cast<uint32_t>((i / kTBufs) & 1);
+      if (!__all_sync(0xffffffffu, mbar_wait_sleep(tempty_bar(b), bph ^ 1u, abort_flag))) {
+        ok = false;
+        break;
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait_sleep(full_bar(s / kGroup), ph, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sW = base + s * kStage;
+      if (elect_one()) {
+        const uint64_t da = smem_desc_sw128(sW);
+        const uint64_t db = smem_desc_sw128(sW + kOffXTile);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // K = 32 bytes per MMA: +2 in 16-byte units
+          umma_e4m3(tmem_base + static_cast<uint32_t>(b * 32), da + 2u * k, db + 2u * k, kIdesc,
+                    k > 0 ? 1u : 0u);
+        umma_commit(tfull_bar(b));
+        if (s % kGroup == kGroup - 1 || i == nu - 1)  // the group's last unit frees its slots
+          umma_commit(empty_bar(s / kGroup));
+      }
+      __syncwarp();
+    }
+    if (!ok) raise_abort(abort_flag);
+    if (elect_one()) umma_commit(drain_bar);
+    __syncwarp();
+    wait_bounded(drain_bar, 0, kDrainLimitNs);
+  } else if (warp < kProducerWarp) {
+    // ------------------------------------------------------------ promotion + output
+    pdl_wait();  // the token scales come from the split kernel
+    const int q = warp;                  // warps 0-3: TMEM lane quarter
+    const int row = 32 * q + lane;       // weight row within the unit's tile
+    const int et = threadIdx.x;          // 0..127
     bool ok = true;
     int64_t u = ub;
     while (u < ue) {
       const int rt = static_cast<int>(u / p.Kb);
       const int64_t tile_u0 = static_cast<int64_t>(rt) * p.Kb;
       const int64_t seg_end = min(ue, tile_u0 + p.Kb);
-      const int64_t i0 = u - ub, i1 = seg_end - ub;
-      int64_t srow_idx[4][2];
-#pragma unroll
-      for (int rg = 0; rg < 4; ++rg)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-          srow_idx[rg][hh] =
-              static_cast<int64_t>(scale_row_of(p, rt * kRows + 64 * hw + 16 * rg + g + 8 * hh)) * p.Kb;
-      float acc[4][NTB][4];
-#pragma unroll
-      for (int rg = 0; rg < 4; ++rg)
-#pragma unroll
-        for (int tb = 0; tb < NTB; ++tb)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) acc[rg][tb][c] = 0.0f;
-
-      if (ok) {
-        for (int64_t i = i0 + ((pair - i0 % 4 + 4) % 4); i < i1; i += 4) {
-          const int s = static_cast<int>(i % kStages);
-          const uint32_t ph = static_cast<uint32_t>((i / kStages) & 1);
-          const int kb = static_cast<int>(ub + i - tile_u0);
-          float sc[4][2];
-#pragma unroll
-          for (int rg = 0; rg < 4; ++rg)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) sc[rg][hh] = load_scale(p, srow_idx[rg][hh] + kb);
-          const bool w_ok = mbar_wait(full_bar(s), ph, abort_flag);
-          if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
-          const uint32_t sW = base + s * C::kStage;
-          const uint32_t sX = sW + kWBytes;
-          // x fragments: token row r = 8*tb + g, 16 values at K offset 16*t of each half
-          uint32_t xf[2][NTB][8];
-#pragma unroll
-          for (int half = 0; half < 2; ++half)
-#pragma unroll
-            for (int tb = 0; tb < NTB; ++tb) {
-              const int r = 8 * tb + g;
-              const uint32_t rowa = sX + half * C::kXHalf + r * 128;
-              const uint4 v0 = lds128(rowa + (static_cast<uint32_t>((2 * t) ^ (r & 7)) << 4));
-              const uint4 v1 = lds128(rowa + (static_cast<uint32_t>((2 * t + 1) ^ (r & 7)) << 4));
-              xf[half][tb][0] = v0.x; xf[half][tb][1] = v0.y; xf[half][tb][2] = v0.z; xf[half][tb][3] = v0.w;
-              xf[half][tb][4] = v1.x; xf[half][tb][5] = v1.y; xf[half][tb][6] = v1.z; xf[half][tb][7] = v1.w;
-            }
-          // BF16 -> F16 with a power of two per token: the quad of lanes
-          // holding token row 8*tb + g finds the row's max |x| exponent E,
-          // scales by 2^e, e = 141 - E (so the max lands in [2^14, 2^15)),
-          // and hands 2^-e to the lanes whose accumulator columns are that
-          // token. Non-negative BF16 patterns order like their values.
-          float xinv[NTB][2];
-#pragma unroll
-          for (int tb = 0; tb < NTB; ++tb) {
-            uint32_t m = 0;
-#pragma unroll
-            for (int half = 0; half < 2; ++half)
-#pragma unroll
-              for (int j = 0; j < 8; ++j) m = __vmaxu2(m, xf[half][tb][j] & 0x7FFF7FFFu);
-            m = max(m & 0xFFFFu, m >> 16);
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            const int e = min(max(141 - static_cast<int>((m >> 7) & 0xFFu), -126), 126);
-            const float up = __int_as_float((e + 127) << 23);
-            const float dn = __int_as_float((127 - e) << 23);
-#pragma unroll
-            for (int half = 0; half < 2; ++half)
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const uint32_t w = xf[half][tb][j];
-                xf[half][tb][j] = f32x2_to_f16x2(__uint_as_float(w << 16) * up,
-                                                 __uint_as_float(w & 0xFFFF0000u) * up);
-              }
-            xinv[tb][0] = __shfl_sync(0xffffffffu, dn, 8 * t);       // token 8*tb + 2t
-            xinv[tb][1] = __shfl_sync(0xffffffffu, dn, 8 * t + 4);   // token 8*tb + 2t + 1
-          }
-#pragma unroll
-          for (int rg = 0; rg < 4; ++rg) {
-            float part[NTB][4];
-#pragma unroll
-            for (int tb = 0; tb < NTB; ++tb)
-#pragma unroll
-              for (int c = 0; c < 4; ++c) part[tb][c] = 0.0f;
-            const int r_lo = 64 * hw + 16 * rg + g;
-            const int r_hi = r_lo + 8;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              const uint4 wl = lds128(sW + r_lo * 128 + (static_cast<uint32_t>((4 * half + t) ^ (r_lo & 7)) << 4));
-              const uint4 wh = lds128(sW + r_hi * 128 + (static_cast<uint32_t>((4 * half + t) ^ (r_hi & 7)) << 4));
-              const uint32_t wlw[4] = {wl.x, wl.y, wl.z, wl.w};
-              const uint32_t whw[4] = {wh.x, wh.y, wh.z, wh.w};
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(wlw[j] & 0xFFFFu));
-                const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(wlw[j] >> 16));
-                const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(whw[j] & 0xFFFFu));
-                const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(whw[j] >> 16));
-#pragma unroll
-                for (int tb = 0; tb < NTB; ++tb)
-                  mma_f16_16816(part[tb], a0, a1, a2, a3, xf[half][tb][2 * j], xf[half][tb][2 * j + 1]);
-              }
-            }
-#pragma unroll
-            for (int tb = 0; tb < NTB; ++tb) {
-              // undo the token scale first (exact), then apply the block scale
-              acc[rg][tb][0] = fmaf(part[tb][0] * xinv[tb][0], sc[rg][0], acc[rg][tb][0]);
-              acc[rg][tb][1] = fmaf(part[tb][1] * xinv[tb][1], sc[rg][0], acc[rg][tb][1]);
-              acc[rg][tb][2] = fmaf(part[tb][2] * xinv[tb][0], sc[rg][1], acc[rg][tb][2]);
-              acc[rg][tb][3] = fmaf(part[tb][3] * xinv[tb][1], sc[rg][1], acc[rg][tb][3]);
-            }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(empty_bar(s));
-        }
-      }
-      // ---- segment reduction over the four pairs
-#pragma unroll
-      for (int rg = 0; rg < 4; ++rg)
-#pragma unroll
-        for (int tb = 0; tb < NTB; ++tb) {
-          const int r_lo = 64 * hw + 16 * rg + g;
-          const int tok = 8 * tb + 2 * t;
-          float* lo = red + ((pair * kRows + r_lo) * 16 + tok);
-          float* hi = red + ((pair * kRows + r_lo + 8) * 16 + tok);
-          *reinterpret_cast<float2*>(lo) = make_float2(acc[rg][tb][0], acc[rg][tb][1]);
-          *reinterpret_cast<float2*>(hi) = make_float2(acc[rg][tb][2], acc[rg][tb][3]);
-        }
-      named_bar_sync(1, 32 * kConsumerWarps);
-      const int row = ct >> 1;
-      const int tk0 = (ct & 1) * 8;
-      float v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = 0.0f;
-#pragma unroll
-      for (int pr = 0; pr < 4; ++pr) {
-        const float4* src = reinterpret_cast<const float4*>(red + ((pr * kRows + row) * 16 + tk0));
-        const float4 a = src[0], b = src[1];
-        v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
-        v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
-      }
       const int n = rt * kRows + row;
+      const int64_t srow_idx = static_cast<int64_t>(scale_row_of(p, n)) * p.Kb;
+      float acc[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+      if (ok) {
+        // Units go in pairs whose TMEM buffers are adjacent (first buffer
+        // even): one 64-column load and one wait serve both.
+        int64_t uu = u;
+        while (uu < seg_end) {
+          const int64_t i = uu - ub;
+          const int b = static_cast<int>(i % kTBufs);
+          const bool pair = ((b & 1) == 0) && (uu + 1 < seg_end);
+          const int kb = static_cast<int>(uu - tile_u0);
+          const float sw0 = load_scale(p, srow_idx + kb);
+          const float sw1 = pair ? load_scale(p, srow_idx + kb + 1) : 0.0f;
+          float4 xa[4], xb[4];
+          const float4* xi4 = reinterpret_cast<const float4*>(p.xinv + kb * 16);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) xa[j] = __ldg(xi4 + j);
+          if (pair) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) xb[j] = __ldg(xi4 + 4 + j);
+          }
+          bool w = mbar_wait(tfull_bar(b), static_cast<uint32_t>((i / kTBufs) & 1), abort_flag);
+          if (pair && w)
+            w = mbar_wait(tfull_bar(b + 1), static_cast<uint32_t>(((i + 1) / kTBufs) & 1), abort_flag);
+          if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * 32);
+          float v[64];
+          if (pair) {
+            tmem_ld64(taddr, v);
+          } else {
+            float v1[32];
+            tmem_ld32(taddr, v1);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = v1[j];
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(tempty_bar(b));
+            if (pair) mbar_arrive(tempty_bar(b + 1));
+          }
+          const float xi0[16] = {xa[0].x, xa[0].y, xa[0].z, xa[0].w, xa[1].x, xa[1].y, xa[1].z, xa[1].w,
+                                 xa[2].x, xa[2].y, xa[2].z, xa[2].w, xa[3].x, xa[3].y, xa[3].z, xa[3].w};
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[j] = fmaf((v[j] + v[16 + j]) * xi0[j], sw0, acc[j]);
+          if (pair) {
+            const float xi1[16] = {xb[0].x, xb[0].y, xb[0].z, xb[0].w, xb[1].x, xb[1].y, xb[1].z, xb[1].w,
+                                   xb[2].x, xb[2].y, xb[2].z, xb[2].w, xb[3].x, xb[3].y, xb[3].z, xb[3].w};
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = fmaf((v[32 + j] + v[48 + j]) * xi1[j], sw1, acc[j]);
+          }
+          uu += pair ? 2 : 1;
+        }
+      }
+      // ---- output: whole tile, or a partial for the last CTA to sum
       const bool whole = (u == tile_u0) && (seg_end == tile_u0 + p.Kb);
       if (whole) {
-        if (n < p.N)
+        if (ok && n < p.N)
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (tk0 + j < p.M) p.y[static_cast<int64_t>(tk0 + j) * p.ldy + n] = __float2bfloat16_rn(v[j]);
+          for (int j = 0; j < 16; ++j)
+            if (j < p.M) p.y[static_cast<int64_t>(j) * p.ldy + n] = __float2bfloat16_rn(acc[j]);
       } else {
         const int slot = (u == ub) ? 0 : 1;
-        float* dst = p.partials + ((static_cast<int64_t>(blockIdx.x) * 2 + slot) * kRows + row) * 16 + tk0;
-        reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
-        reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
-        __threadfence();
-        named_bar_sync(1, 32 * kConsumerWarps);
-        const int64_t c_first = cta_of_unit(p, tile_u0);
-        const int64_t c_last = cta_of_unit(p, tile_u0 + p.Kb - 1);
-        if (ct == 0) {
-          const int old = atomicAdd(p.counters + rt, 1);
-          *last_flag = (old == static_cast<int>(c_last - c_first)) ? 1 : 0;
-        }
-        named_bar_sync(1, 32 * kConsumerWarps);
-        if (*last_flag) {
-          __threadfence();
-          float s[8];
+        float4* dst = reinterpret_cast<float4*>(
+            p.partials + ((static_cast<int64_t>(blockIdx.x) * 2 + slot) * kRows + row) * 16);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) s[j] = 0.0f;
-          for (int64_t c = c_first; c <= c_last; ++c) {
-            const int sl = (unit_begin(p, c) >= tile_u0) ? 0 : 1;
-            const float4* srcp = reinterpret_cast<const float4*>(
-                p.partials + ((c * 2 + sl) * kRows + row) * 16 + tk0);
-            const float4 a = __ldcg(srcp), b = __ldcg(srcp + 1);
-            s[0] += a.x; s[1] += a.y; s[2] += a.z; s[3] += a.w;
-            s[4] += b.x; s[5] += b.y; s[6] += b.z; s[7] += b.w;
-          }
-          if (n < p.N)
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (tk0 + j < p.M) p.y[static_cast<int64_t>(tk0 + j) * p.ldy + n] = __float2bfloat16_rn(s[j]);
-          if (ct == 0) p.counters[rt] = 0;
-        }
+        for (int j = 0; j < 4; ++j) dst[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+        // hand the arrival to the publisher warp and go on with the next segment
+        named_bar_sync(kBarPartial, 160);
       }
-      named_bar_sync(1, 32 * kConsumerWarps);
       u = seg_end;
     }
+    // ---- fixups: tiles this CTA arrived at last, summed in CTA order
+    named_bar_sync(kBarFinal, 160);
+    for (int k = 0; k < 2; ++k) {
+      const int last_tile = last_flag[k];  // tile index + 1, or 0
+      if (last_tile == 0) continue;
+      const int rt = last_tile - 1;
+      const int64_t tile_u0 = static_cast<int64_t>(rt) * p.Kb;
+      const int64_t c_first = cta_of_unit(p, tile_u0);
+      const int64_t c_last = cta_of_unit(p, tile_u0 + p.Kb - 1);
+      const int n = rt * kRows + row;
+      float sum[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) sum[j] = 0.0f;
+      // up to 4 contributors at a time so their loads overlap
+      for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
+        float4 part[4][4];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const int64_t c = c0 + cc;
+          if (c <= c_last) {
+            const int sl = (unit_begin(p, c) >= tile_u0) ? 0 : 1;
+            const float4* srcp = reinterpret_cast<const float4*>(
+                p.partials + ((c * 2 + sl) * kRows + row) * 16);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) part[cc][j] = __ldcg(srcp + j);
+          }
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          if (c0 + cc <= c_last) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              sum[4 * j] += part[cc][j].x; sum[4 * j + 1] += part[cc][j].y;
+              sum[4 * j + 2] += part[cc][j].z; sum[4 * j + 3] += part[cc][j].w;
+            }
+          }
+        }
+      }
+      if (n < p.N)
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (j < p.M) p.y[static_cast<int64_t>(j) * p.ldy + n] = __float2bfloat16_rn(sum[j]);
+      if (et == 0) p.counters[rt] = 0;  // leave the workspace clean
+    }
     if (!ok) raise_abort(abort_flag);
+  } else if (warp == kPublisherWarp) {
+    // ------------------------------------------------------------ arrivals
+    // For each split tile of this CTA (at most two: the first and the last
+    // segment), once the epilogue has written its partial: one acquire-release
+    // atomic on the tile's counter publishes the partial (cumulative release
+    // after the barrier) and tells whether this CTA arrived last; if so it
+    // also makes the other CTAs' partials visible here (acquire).
+    int k = 0;
+    int64_t u = ub;
+    while (u < ue) {
+      const int rt = static_cast<int>(u / p.Kb);
+      const int64_t tile_u0 = static_cast<int64_t>(rt) * p.Kb;
+      const int64_t seg_end = min(ue, tile_u0 + p.Kb);
+      const bool whole = (u == tile_u0) && (seg_end == tile_u0 + p.Kb);
+      if (!whole) {
+        named_bar_sync(kBarPartial, 160);
+        if (lane == 0) {
+          int last_arrival = 0;
+          if (!*abort_flag) {
+            const int64_t c_first = cta_of_unit(p, tile_u0);
+            const int64_t c_last = cta_of_unit(p, tile_u0 + p.Kb - 1);
+            const int old = atomic_add_acq_rel_gpu(p.counters + rt, 1);
+            last_arrival = (old == static_cast<int>(c_last - c_first)) ? rt + 1 : 0;
+          }
+          last_flag[k] = last_arrival;
+        }
+        ++k;
+      }
+      u = seg_end;
+    }
+    if (lane == 0)
+      for (; k < 2; ++k) last_flag[k] = 0;
+    __syncwarp();
+    named_bar_sync(kBarFinal, 160);
   }
+  tc_fence_before();
   __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
 }
 
-template <int NTB>
-int launch_t(const CUtensorMap& tw, const CUtensorMap& tx, const GemvParams& p, void* stream) {
-  using C = GCfg<NTB>;
-  auto kernel = gemv_kernel<NTB>;
-  int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel), C::kSmemBytes);
+// The split kernel, then the GEMV as its programmatic dependent.
+int launch_kernels(const void* x, int64_t ldx, uint8_t* xtile, float* xinv, const CUtensorMap& tw,
+                   const CUtensorMap& tx, const GemvParams& p, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  gemv_split_tokens_kernel<<<p.Kb, 64, 0, st>>>(static_cast<const __nv_bfloat16*>(x), ldx, p.M,
+                                                p.K, xtile, xinv, p.counters, p.RT);
+  int rc = check_launch();
   if (rc != BFP8_OK) return rc;
-  kernel<<<p.grid, kThreads, C::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(tw, tx, p);
+  rc = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel), kSmemBytes);
+  if (rc != BFP8_OK) return rc;
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, gemv_kernel, tw, tx, p) != cudaSuccess) return BFP8_ERR_CUDA;
   return check_launch();
 }
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
+// Workspace: [RT] tile counters | [sms][2][128][16] FP32 partial tiles |
+// [Kb][32][128] E4M3 token tiles | [Kb][16] token scales, each part 256-byte aligned.
+struct WsLayout {
+  size_t partials, xtile, xinv, total;
+};
+WsLayout ws_layout(int64_t N, int64_t K, int sms) {
+  const int64_t RT = (N + kRows - 1) / kRows;
+  const int64_t Kb = (K + 127) / 128;
+  WsLayout l;
+  l.partials = align256(static_cast<size_t>(RT) * 4);
+  l.xtile = l.partials + align256(static_cast<size_t>(sms) * 2 * kRows * 16 * sizeof(float));
+  l.xinv = l.xtile + align256(static_cast<size_t>(Kb) * kXTile);
+  l.total = l.xinv + align256(static_cast<size_t>(Kb) * 16 * sizeof(float));
+  return l;
+}
+
 }  // namespace
 
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K, int sms) {
   (void)M;
-  (void)K;
-  if (N <= 0 || sms <= 0) return 0;
-  const int64_t RT = (N + kRows - 1) / kRows;
-  return align256(static_cast<size_t>(RT) * 4) +
-         static_cast<size_t>(sms) * 2 * kRows * 16 * sizeof(float);
+  if (N <= 0 || K <= 0 || sms <= 0) return 0;
+  return ws_layout(N, K, sms).total;
 }
 
 int launch_gemv(const void* x, int64_t ldx, const void* w, const void* w_scale,
@@ -427,22 +597,22 @@ int launch_gemv(const void* x, int64_t ldx, const void* w, const void* w_scale,
   }
   p.y = static_cast<__nv_bfloat16*>(y);
   p.ldy = ldy;
-  p.counters = static_cast<int32_t*>(workspace);
-  p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                        align256(static_cast<size_t>(p.RT) * 4));
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, static_cast<size_t>(p.RT) * 4, st) != cudaSuccess)
-    return BFP8_ERR_CUDA;
-  const int ntb = M <= 8 ? 1 : 2;
-  const uint32_t mb = 8u * ntb;
+  const WsLayout l = ws_layout(N, K, sms);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.counters = reinterpret_cast<int32_t*>(ws);
+  p.partials = reinterpret_cast<float*>(ws + l.partials);
+  uint8_t* xtile = ws + l.xtile;
+  float* xinv = reinterpret_cast<float*>(ws + l.xinv);
+  p.xinv = xinv;
   CUtensorMap tw, tx;
   rc = make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, K, 128, kRows,
                     CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != BFP8_OK) return rc;
-  rc = make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, ldx * 2, 64, mb,
-                    CU_TENSOR_MAP_SWIZZLE_128B);
+  // the split kernel's token tiles, one 32-row box per K-block
+  rc = make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xtile, 128, static_cast<uint64_t>(p.Kb) * 32,
+                    128, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != BFP8_OK) return rc;
-  return ntb == 1 ? launch_t<1>(tw, tx, p, stream) : launch_t<2>(tw, tx, p, stream);
+  return launch_kernels(x, ldx, xtile, xinv, tw, tx, p, stream);
 }
 
 // ---------------------------------------------------------------------------

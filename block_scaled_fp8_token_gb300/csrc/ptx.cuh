@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -34,6 +35,11 @@ BFP8_DEV void mbar_init(uint32_t bar, uint32_t count) {
 // Make initialised barriers visible to the async proxy (TMA, tensor cores).
 BFP8_DEV void mbar_fence_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Make this thread's ordinary shared-memory writes visible to the async proxy
+// (the tensor cores reading an operand tile the threads wrote).
+BFP8_DEV void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 BFP8_DEV void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
@@ -94,6 +100,19 @@ BFP8_DEV bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const volatile int*
       if (globaltimer() - t0 > kWaitLimitNs) return false;
     }
   }
+}
+
+// atomicAdd with acquire-release semantics at GPU scope: writes ordered
+// before it (including other threads' writes ordered by a CTA barrier) are
+// visible to whoever observes the new value, and what the observed value
+// published is visible after it.
+BFP8_DEV int atomic_add_acq_rel_gpu(int* addr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(addr), "r"(v)
+               : "memory");
+  return old;
 }
 
 // One lane of the (fully converged) warp returns true: the lowest active lane.

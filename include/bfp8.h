@@ -233,16 +233,25 @@ int bfp8_linear_w8a16(const void* x_bf16, int64_t ldx, const void* w_e4m3, const
  * bfp8_gemv_decode -- the memory-bound small-M projection (W8A16 arithmetic).
  *   [Module w8a8_prefill, "Reachability": the GB10 decode path is an unfused
  *    per-projection GEMV]
- * Streams W once with 16-byte loads. Each 16x16 fragment is decoded E4M3->BF16
- * in registers, multiplied on the tensor cores and scaled per 128-K block in
- * FP32 registers. Split-K partial sums are reduced in a fixed order through
- * `workspace`, so results are deterministic.
+ * W streams from HBM to the tensor cores untouched (TMA, tcgen05 E4M3 MMAs,
+ * FP32 accumulation in tensor memory, the per-128-K block scale applied in
+ * FP32 registers). A small kernel launched first writes each token's
+ * 128-column blocks as two E4M3 terms hi + lo at a per-(token, block) power of
+ * two; hi + lo equals the BF16 value exactly for every entry within 2^-10 of
+ * the block's max |x|, and smaller entries are carried to within max|x| * 2^-18.
+ * The GEMV runs behind it as a programmatic dependent launch. Split-K partial
+ * sums are reduced in a fixed order through `workspace`, so results are
+ * deterministic.
  *   x_bf16 [M, K] BF16, row stride ldx (ldx % 8 == 0, 16-byte aligned), 1 <= M <= 16
- *   w_e4m3 [N, K], w_scale grid as bfp8_linear_w8a8 (K % 16 == 0)
+ *   w_e4m3 [N, K], w_scale grid as bfp8_linear_w8a8 (K % 16 == 0); E4M3 NaN
+ *          codes (0x7F, 0xFF) give NaN outputs
  *   y_bf16 [M, N] BF16, row stride ldy (elements)
  *   workspace  device scratch of at least bfp8_gemv_decode_workspace(M,N,K)
- *              bytes, caller-owned. Its contents need not be initialised. Two
- *              calls that share one workspace must not overlap on the GPU.
+ *              bytes, caller-owned, 256-byte aligned. Its contents need not be
+ *              initialised. Two calls that share one workspace must not
+ *              overlap on the GPU.
+ * The call is two kernel launches on `stream` and can be captured in a CUDA
+ * graph.
  */
 int bfp8_gemv_decode(const void* x_bf16, int64_t ldx, const void* w_e4m3, const void* w_scale,
                      int32_t w_scale_dtype, int64_t M, int64_t N, int64_t K,
