@@ -369,7 +369,7 @@ def run_decode(bfp8, torch, dev, wgu, sgu, wdn, sdn, peaks):
     res["l2"] = (f"inputs larger than L2: each timed launch reads the next of "
                  f"{len(copies['gate_up'])} (gate/up) or {len(copies['down'])} (down) weight "
                  f"copies, >= 2x the {l2 >> 20} MB L2; no flush writes")
-    for M in (1, 4, 16):
+    for arm, M in [("w8a16", 1), ("w8a16", 4), ("w8a16", 16), ("w8a8", 1), ("w8a8", 16)]:
         row = {}
         for name, members in (("gate_up", [INTER, INTER]), ("down", None)):
             ring = copies[name]
@@ -377,9 +377,17 @@ def run_decode(bfp8, torch, dev, wgu, sgu, wdn, sdn, peaks):
             x = synth.decode_tokens(100 + M, M, K).to(dev)
             y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
             ws = torch.empty(bfp8.bfp8_gemv_decode_workspace(M, N, K), dtype=torch.uint8, device=dev)
+            qa = torch.empty(M, K, dtype=torch.uint8, device=dev)
+            sa = torch.empty(M, K // 128, dtype=torch.float32, device=dev)
+            bfp8.bfp8_act_quant_group(x, qa, sa, stream=stream)
+
             def call(j):
                 w, s = ring[j % len(ring)]
-                bfp8.bfp8_gemv_decode(x, w, s, y, ws, member_rows=members, stream=g_stream)
+                if arm == "w8a8":
+                    bfp8.bfp8_gemv_decode_w8a8(qa, sa, w, s, y, ws, member_rows=members,
+                                               stream=g_stream)
+                else:
+                    bfp8.bfp8_gemv_decode(x, w, s, y, ws, member_rows=members, stream=g_stream)
 
             # a CUDA graph of launches rotating over the copies: GPU time with
             # the gaps between kernels, without the host's launch cost
@@ -426,9 +434,9 @@ def run_decode(bfp8, torch, dev, wgu, sgu, wdn, sdn, peaks):
             gbs = nbytes / (us * 1e-6) / 1e9
             row[name] = {"us": round(us, 2), "bytes": nbytes, "GB/s": round(gbs, 1),
                          "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
-            if name == "gate_up" and M == 16:
+            if name == "gate_up" and M == 16 and arm == "w8a16":
                 best = row[name]
-        res["shapes"][f"M={M}"] = row
+        res["shapes"][f"M={M}" if arm == "w8a16" else f"M={M} W8A8 (E4M3 tokens)"] = row
     res["roofline"] = {"bound": "hbm", "kernel": "gemv_kernel (gate/up [34816,5120], M=16)",
                        "achieved": best["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
                        "frac": best["frac_hbm"], "traffic": ncu_traffic("gemv_gate_up_m16")[0],

@@ -78,6 +78,9 @@ _SIGS = {
     "bfp8_gemv_decode": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _i64,
                                         ctypes.POINTER(bfp8_members), _vp, _sz, _vp]),
     "bfp8_gemv_decode_workspace": (_sz, [_i64, _i64, _i64]),
+    "bfp8_gemv_decode_w8a8": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i32, _i64, _i64,
+                                             _i64, _vp, _i64, ctypes.POINTER(bfp8_members), _vp,
+                                             _sz, _vp]),
     "bfp8_gemv_decode_noalloc": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _i64, _i64, _i64, _vp,
                                                 _i64, ctypes.POINTER(bfp8_members), _vp]),
     "bfp8_grouped_linear": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i32, _vp, _i32, _i64,
@@ -252,6 +255,22 @@ def bfp8_gemv_decode(x, w, w_scale, y, workspace, member_rows=None, stream=None)
                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _stream(stream)),
            "bfp8_gemv_decode")
+
+
+def bfp8_gemv_decode_w8a8(q_a, s_a, w, w_scale, y, workspace, member_rows=None, s_stride_m=None,
+                          s_stride_kb=None, stream=None) -> None:
+    """Decode GEMV (M <= 16) on E4M3 tokens with 1x128 scales (W8A8 arithmetic)."""
+    M, K = q_a.shape
+    N = w.shape[0]
+    ssm = s_a.stride(0) if s_stride_m is None else s_stride_m
+    sskb = s_a.stride(1) if s_stride_kb is None else s_stride_kb
+    mref, _keep = _members(member_rows)
+    _check(_lib.bfp8_gemv_decode_w8a8(_ptr(q_a), _ptr(s_a), ssm, sskb, _ptr(w), _ptr(w_scale),
+                                      _scale_dtype(w_scale), M, N, K, _ptr(y), y.stride(0), mref,
+                                      _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(),
+                                      _stream(stream)),
+           "bfp8_gemv_decode_w8a8")
 
 
 def bfp8_gemv_decode_noalloc(x, w, w_scale, y, member_rows=None, stream=None) -> None:

@@ -346,6 +346,21 @@ int bfp8_gemv_decode(const void* x_bf16, int64_t ldx, const void* w_e4m3, const 
                      workspace, ws_bytes, stream);
 }
 
+int bfp8_gemv_decode_w8a8(const void* q_a, const float* s_a, int64_t s_stride_m,
+                          int64_t s_stride_kb, const void* w_e4m3, const void* w_scale,
+                          int32_t w_scale_dtype, int64_t M, int64_t N, int64_t K, void* y_bf16,
+                          int64_t ldy, const bfp8_members* members, void* workspace,
+                          size_t ws_bytes, void* stream) {
+  if (M < 1 || M > 16 || N <= 0 || K <= 0) return BFP8_ERR_INVALID_ARG;
+  if (!q_a || !s_a || !w_e4m3 || !w_scale || !y_bf16 || ldy < N) return BFP8_ERR_INVALID_ARG;
+  if (w_scale_dtype != BFP8_DT_BF16 && w_scale_dtype != BFP8_DT_F32) return BFP8_ERR_SCALE_DTYPE;
+  MemberTable mt;
+  int rc = resolve_members(N, members, &mt);
+  if (rc != BFP8_OK) return rc;
+  return launch_gemv_w8a8(q_a, s_a, s_stride_m, s_stride_kb, w_e4m3, w_scale, w_scale_dtype, M,
+                          N, K, y_bf16, ldy, mt, workspace, ws_bytes, stream);
+}
+
 size_t bfp8_grouped_linear_workspace(int64_t total_M, int32_t G, int64_t N, int64_t K) {
   (void)K;
   int sms = 0;

@@ -76,6 +76,10 @@ size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K, int sms);
 int launch_gemv(const void* x, int64_t ldx, const void* w, const void* w_scale,
                 int32_t w_scale_dtype, int64_t M, int64_t N, int64_t K, void* y, int64_t ldy,
                 const MemberTable& mt, void* workspace, size_t ws_bytes, void* stream);
+int launch_gemv_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
+                     const void* w, const void* w_scale, int32_t w_scale_dtype, int64_t M,
+                     int64_t N, int64_t K, void* y, int64_t ldy, const MemberTable& mt,
+                     void* workspace, size_t ws_bytes, void* stream);
 
 // Device error words, one per translation unit with bounded waits: read and
 // clear. Return BFP8_OK, BFP8_ERR_TIMEOUT or BFP8_ERR_CUDA.

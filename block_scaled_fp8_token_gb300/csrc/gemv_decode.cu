@@ -70,13 +70,17 @@ constexpr uint32_t kWBytes = kRows * 128;            // E4M3 weight tile
 constexpr uint32_t kXTile = 32 * 128;                // token tile: hi rows 0-15, lo rows 16-31
 constexpr uint32_t kOffXTile = kWBytes;
 constexpr uint32_t kStage = kWBytes + kXTile;
-constexpr uint32_t kTmaBytes = kStage;
+// bytes TMA brings per unit: the weight tile and the token tile (32 hi/lo
+// rows for the W8A16 arm, 16 quantized token rows for the W8A8 arm)
+template <bool W8A8>
+constexpr uint32_t kTmaBytes = kWBytes + (W8A8 ? 16u * 128u : kXTile);
 constexpr uint32_t kOffBar = kStages * kStage;
 constexpr uint32_t kNumBars = 2 * kGroups + 2 * kTBufs + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag, last flags [2]
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kThreads == 32 * (kPublisherWarp + 1), "one warp per role after the epilogue");
-constexpr uint32_t kIdesc = idesc_e4m3(kRows, 32);
+template <bool W8A8>
+constexpr uint32_t kIdesc = idesc_e4m3(kRows, W8A8 ? 16 : 32);
 constexpr unsigned long long kDrainLimitNs = 100000000ull;
 static_assert(kStage % 1024 == 0 && kOffXTile % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(kStages % kGroup == 0, "slot groups must tile the ring");
@@ -94,7 +98,9 @@ struct GemvParams {
   int64_t ldy;
   int32_t* counters;  // [RT], zero at kernel start
   float* partials;    // [grid][2][128][16]
-  const float* xinv;  // [Kb][16]: 2^-e of each token's K-block
+  const float* xinv;  // [Kb][16]: 2^-e of each token's K-block (W8A16 arm)
+  const float* s_a;   // token scales (W8A8 arm): (m, kb) at s_a[m*sa_sm + kb*sa_skb]
+  int64_t sa_sm, sa_skb;
 };
 
 BFP8_DEV int64_t unit_begin(const GemvParams& p, int64_t c) { return (c * p.U) / p.grid; }
@@ -203,6 +209,18 @@ __global__ void __launch_bounds__(64) gemv_split_tokens_kernel(
   if (q4 == 0) xinv[kb * 16 + tok] = __int_as_float((127 - e) << 23);
 }
 
+// Clears the split-tile counters ahead of the W8A8 arm's GEMV, which runs as
+// its programmatic dependent and touches them only after griddepcontrol.wait.
+__global__ void __launch_bounds__(256) gemv_clear_counters_kernel(int32_t* __restrict__ counters,
+                                                                 int32_t n) {
+  pdl_launch_dependents();
+  for (int i = threadIdx.x; i < n; i += 256) counters[i] = 0;
+}
+
+// W8A8 == false: W8A16 arithmetic, tokens as split hi/lo tiles (tmX over
+// the split kernel's output). W8A8 == true: tokens already quantized to E4M3
+// with 1x128 scales (tmX over q_a [M, K], rows past M read as zeros).
+template <bool W8A8>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                 const __grid_constant__ GemvParams p) {
@@ -250,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t i0 = 0; i0 < n_first; i0 += kGroup) {
       const int g = static_cast<int>(i0 / kGroup);
       const int n_in = static_cast<int>(min(static_cast<int64_t>(kGroup), nu - i0));
-      mbar_arrive_expect_tx(full_bar(g), kTmaBytes * n_in);
+      mbar_arrive_expect_tx(full_bar(g), kTmaBytes<W8A8> * n_in);
       for (int j = 0; j < n_in; ++j) {
         int rt, kb;
         unit_rt_kb(ub + i0 + j, rt, kb);
@@ -279,22 +297,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n_in = static_cast<int>(min(static_cast<int64_t>(kGroup), nu - i0));
         if (i0 >= n_first) {  // the first pass's weight loads went out before the CTA sync
           if (!mbar_wait_sleep(empty_bar(g), ph ^ 1u, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(full_bar(g), kTmaBytes * n_in);
+          mbar_arrive_expect_tx(full_bar(g), kTmaBytes<W8A8> * n_in);
           for (int j = 0; j < n_in; ++j) {
             int rt, kb;
             unit_rt_kb(ub + i0 + j, rt, kb);
             tma_load_2d(base + (g * kGroup + j) * kStage, &tmW, kb * 128, rt * kRows, full_bar(g));
           }
         }
-        // the token tiles come from the split kernel this grid depends on
-        if (!tokens_ready) {
+        // the W8A16 arm's token tiles come from the split kernel this grid
+        // depends on; the W8A8 arm's tokens come from the caller
+        if (!W8A8 && !tokens_ready) {
           pdl_wait();
           tokens_ready = true;
         }
         for (int j = 0; j < n_in; ++j) {
           const int64_t u = ub + i0 + j;
           const int kb = static_cast<int>(u % p.Kb);
-          tma_load_2d(base + (g * kGroup + j) * kStage + kOffXTile, &tmX, 0, kb * 32, full_bar(g));
+          if (W8A8)
+            tma_load_2d(base + (g * kGroup + j) * kStage + kOffXTile, &tmX, kb * 128, 0, full_bar(g));
+          else
+            tma_load_2d(base + (g * kGroup + j) * kStage + kOffXTile, &tmX, 0, kb * 32, full_bar(g));
         }
         armed |= 1u << g;
         armed_phase = (armed_phase & ~(1u << g)) | (ph << g);
@@ -328,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t db = smem_desc_sw128(sW + kOffXTile);
 #pragma unroll
         for (int k = 0; k < 4; ++k)  // K = 32 bytes per MMA: +2 in 16-byte units
-          umma_e4m3(tmem_base + static_cast<uint32_t>(b * 32), da + 2u * k, db + 2u * k, kIdesc,
+          umma_e4m3(tmem_base + static_cast<uint32_t>(b * 32), da + 2u * k, db + 2u * k, kIdesc<W8A8>,
                     k > 0 ? 1u : 0u);
         umma_commit(tfull_bar(b));
         if (s % kGroup == kGroup - 1 || i == nu - 1)  // the group's last unit frees its slots
@@ -342,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     wait_bounded(drain_bar, 0, kDrainLimitNs);
   } else if (warp < kProducerWarp) {
     // ------------------------------------------------------------ promotion + output
-    pdl_wait();  // the token scales come from the split kernel
+    pdl_wait();  // the counters (and the W8A16 arm's token scales) come from the first kernel
     const int q = warp;                  // warps 0-3: TMEM lane quarter
     const int row = 32 * q + lane;       // weight row within the unit's tile
     const int et = threadIdx.x;          // 0..127
@@ -368,13 +390,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kb = static_cast<int>(uu - tile_u0);
           const float sw0 = load_scale(p, srow_idx + kb);
           const float sw1 = pair ? load_scale(p, srow_idx + kb + 1) : 0.0f;
-          float4 xa[4], xb[4];
-          const float4* xi4 = reinterpret_cast<const float4*>(p.xinv + kb * 16);
+          // per-token factors of the two K-blocks: 2^-e of the split (W8A16)
+          // or the 1x128 activation scale (W8A8)
+          float xi0[16], xi1[16];
+          if (W8A8) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) xa[j] = __ldg(xi4 + j);
-          if (pair) {
+            for (int j = 0; j < 16; ++j) {
+              xi0[j] = j < p.M ? __ldg(p.s_a + j * p.sa_sm + kb * p.sa_skb) : 0.0f;
+              xi1[j] = (pair && j < p.M) ? __ldg(p.s_a + j * p.sa_sm + (kb + 1) * p.sa_skb) : 0.0f;
+            }
+          } else {
+            const float4* xi4 = reinterpret_cast<const float4*>(p.xinv + kb * 16);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) xb[j] = __ldg(xi4 + 4 + j);
+            for (int j = 0; j < 4; ++j) {
+              const float4 a4 = __ldg(xi4 + j);
+              xi0[4 * j] = a4.x; xi0[4 * j + 1] = a4.y; xi0[4 * j + 2] = a4.z; xi0[4 * j + 3] = a4.w;
+            }
+            if (pair) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float4 a4 = __ldg(xi4 + 4 + j);
+                xi1[4 * j] = a4.x; xi1[4 * j + 1] = a4.y; xi1[4 * j + 2] = a4.z; xi1[4 * j + 3] = a4.w;
+              }
+            }
           }
           bool w = mbar_wait(tfull_bar(b), static_cast<uint32_t>((i / kTBufs) & 1), abort_flag);
           if (pair && w)
@@ -397,15 +435,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(tempty_bar(b));
             if (pair) mbar_arrive(tempty_bar(b + 1));
           }
-          const float xi0[16] = {xa[0].x, xa[0].y, xa[0].z, xa[0].w, xa[1].x, xa[1].y, xa[1].z, xa[1].w,
-                                 xa[2].x, xa[2].y, xa[2].z, xa[2].w, xa[3].x, xa[3].y, xa[3].z, xa[3].w};
+          // column j of a buffer is token j (W8A16: plus its lo term at 16 + j)
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc[j] = fmaf((v[j] + v[16 + j]) * xi0[j], sw0, acc[j]);
+          for (int j = 0; j < 16; ++j)
+            acc[j] = fmaf((W8A8 ? v[j] : v[j] + v[16 + j]) * xi0[j], sw0, acc[j]);
           if (pair) {
-            const float xi1[16] = {xb[0].x, xb[0].y, xb[0].z, xb[0].w, xb[1].x, xb[1].y, xb[1].z, xb[1].w,
-                                   xb[2].x, xb[2].y, xb[2].z, xb[2].w, xb[3].x, xb[3].y, xb[3].z, xb[3].w};
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = fmaf((v[32 + j] + v[48 + j]) * xi1[j], sw1, acc[j]);
+            for (int j = 0; j < 16; ++j)
+              acc[j] = fmaf((W8A8 ? v[32 + j] : v[32 + j] + v[48 + j]) * xi1[j], sw1, acc[j]);
           }
           uu += pair ? 2 : 1;
         }
@@ -524,7 +561,7 @@ int launch_kernels(const void* x, int64_t ldx, uint8_t* xtile, float* xinv, cons
                                                 p.K, xtile, xinv, p.counters, p.RT);
   int rc = check_launch();
   if (rc != BFP8_OK) return rc;
-  rc = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel), kSmemBytes);
+  rc = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel<false>), kSmemBytes);
   if (rc != BFP8_OK) return rc;
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[1];
@@ -536,7 +573,7 @@ int launch_kernels(const void* x, int64_t ldx, uint8_t* xtile, float* xinv, cons
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, gemv_kernel, tw, tx, p) != cudaSuccess) return BFP8_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, gemv_kernel<false>, tw, tx, p) != cudaSuccess) return BFP8_ERR_CUDA;
   return check_launch();
 }
 
@@ -566,12 +603,13 @@ size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K, int sms) {
   return ws_layout(N, K, sms).total;
 }
 
-int launch_gemv(const void* x, int64_t ldx, const void* w, const void* w_scale,
-                int32_t w_scale_dtype, int64_t M, int64_t N, int64_t K, void* y, int64_t ldy,
-                const MemberTable& mt, void* workspace, size_t ws_bytes, void* stream) {
-  if (K % 16 != 0 || ldx % 8 != 0) return BFP8_ERR_UNSUPPORTED;
-  if (reinterpret_cast<uintptr_t>(x) % 16 != 0 || reinterpret_cast<uintptr_t>(w) % 16 != 0)
-    return BFP8_ERR_UNSUPPORTED;
+namespace {
+
+// Parameters shared by both arms; checks the workspace and the geometry.
+int init_params(GemvParams& p, const void* w, const void* w_scale, int32_t w_scale_dtype,
+                int64_t M, int64_t N, int64_t K, void* y, int64_t ldy, const MemberTable& mt,
+                void* workspace, size_t ws_bytes, int* sms_out) {
+  if (K % 16 != 0 || reinterpret_cast<uintptr_t>(w) % 16 != 0) return BFP8_ERR_UNSUPPORTED;
   if (N > 0x7FFFFFFF || K > 0x7FFFFFFF) return BFP8_ERR_UNSUPPORTED;
   int sms = 0;
   int rc = sm_count(&sms);
@@ -579,7 +617,6 @@ int launch_gemv(const void* x, int64_t ldx, const void* w, const void* w_scale,
   const size_t need = gemv_workspace_bytes(M, N, K, sms);
   if (!workspace || ws_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
     return BFP8_ERR_INVALID_ARG;
-  GemvParams p{};
   p.M = static_cast<int32_t>(M);
   p.N = static_cast<int32_t>(N);
   p.K = static_cast<int32_t>(K);
@@ -601,9 +638,22 @@ int launch_gemv(const void* x, int64_t ldx, const void* w, const void* w_scale,
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.counters = reinterpret_cast<int32_t*>(ws);
   p.partials = reinterpret_cast<float*>(ws + l.partials);
-  uint8_t* xtile = ws + l.xtile;
-  float* xinv = reinterpret_cast<float*>(ws + l.xinv);
-  p.xinv = xinv;
+  p.xinv = reinterpret_cast<float*>(ws + l.xinv);
+  *sms_out = sms;
+  return BFP8_OK;
+}
+
+}  // namespace
+
+int launch_gemv(const void* x, int64_t ldx, const void* w, const void* w_scale,
+                int32_t w_scale_dtype, int64_t M, int64_t N, int64_t K, void* y, int64_t ldy,
+                const MemberTable& mt, void* workspace, size_t ws_bytes, void* stream) {
+  if (ldx % 8 != 0 || reinterpret_cast<uintptr_t>(x) % 16 != 0) return BFP8_ERR_UNSUPPORTED;
+  GemvParams p{};
+  int sms = 0;
+  int rc = init_params(p, w, w_scale, w_scale_dtype, M, N, K, y, ldy, mt, workspace, ws_bytes, &sms);
+  if (rc != BFP8_OK) return rc;
+  uint8_t* xtile = static_cast<uint8_t*>(workspace) + ws_layout(N, K, sms).xtile;
   CUtensorMap tw, tx;
   rc = make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, K, 128, kRows,
                     CU_TENSOR_MAP_SWIZZLE_128B);
@@ -612,7 +662,48 @@ int launch_gemv(const void* x, int64_t ldx, const void* w, const void* w_scale,
   rc = make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xtile, 128, static_cast<uint64_t>(p.Kb) * 32,
                     128, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != BFP8_OK) return rc;
-  return launch_kernels(x, ldx, xtile, xinv, tw, tx, p, stream);
+  return launch_kernels(x, ldx, xtile, const_cast<float*>(p.xinv), tw, tx, p, stream);
+}
+
+int launch_gemv_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
+                     const void* w, const void* w_scale, int32_t w_scale_dtype, int64_t M,
+                     int64_t N, int64_t K, void* y, int64_t ldy, const MemberTable& mt,
+                     void* workspace, size_t ws_bytes, void* stream) {
+  if (reinterpret_cast<uintptr_t>(q_a) % 16 != 0) return BFP8_ERR_UNSUPPORTED;
+  if (sa_sm < 0 || sa_skb < 0) return BFP8_ERR_INVALID_ARG;
+  GemvParams p{};
+  int sms = 0;
+  int rc = init_params(p, w, w_scale, w_scale_dtype, M, N, K, y, ldy, mt, workspace, ws_bytes, &sms);
+  if (rc != BFP8_OK) return rc;
+  p.s_a = s_a;
+  p.sa_sm = sa_sm;
+  p.sa_skb = sa_skb;
+  CUtensorMap tw, tx;
+  rc = make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, K, 128, kRows,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != BFP8_OK) return rc;
+  // the quantized tokens themselves: one 16-row box per K-block, rows past M zero
+  rc = make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_a, K, M, K, 128, 16,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != BFP8_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  gemv_clear_counters_kernel<<<1, 256, 0, st>>>(p.counters, p.RT);
+  rc = check_launch();
+  if (rc != BFP8_OK) return rc;
+  rc = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel<true>), kSmemBytes);
+  if (rc != BFP8_OK) return rc;
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, gemv_kernel<true>, tw, tx, p) != cudaSuccess) return BFP8_ERR_CUDA;
+  return check_launch();
 }
 
 // ---------------------------------------------------------------------------

@@ -261,6 +261,24 @@ int bfp8_gemv_decode(const void* x_bf16, int64_t ldx, const void* w_e4m3, const 
 /* Workspace bytes bfp8_gemv_decode needs on the current device (0 if none). */
 size_t bfp8_gemv_decode_workspace(int64_t M, int64_t N, int64_t K);
 
+/*
+ * bfp8_gemv_decode_w8a8 -- the same decode GEMV with E4M3 tokens: the W8A8
+ * arithmetic of bfp8_linear_w8a8 for M <= 16.
+ *   [Module w8a8_prefill, arithmetic paragraph: per-token 1x128 activation
+ *    scales times 128x128 weight scales, FP32 per K-block]
+ * y[m,n] = bf16_rn( sum_kb s_a[m,kb] * s_w[r(n),kb] * sum_{k in kb} e4m3(q_a[m,k]) * e4m3(W[n,k]) ).
+ * The quantized tokens go to the FP8 tensor cores as they are (no split).
+ *   q_a    [M, K] E4M3 from bfp8_act_quant_group, row stride K bytes, 16-byte aligned
+ *   s_a    float32 activation scales as bfp8_linear_w8a8
+ *   other arguments, the workspace (bfp8_gemv_decode_workspace bytes) and
+ *   requirements as bfp8_gemv_decode. One kernel launch.
+ */
+int bfp8_gemv_decode_w8a8(const void* q_a, const float* s_a, int64_t s_stride_m,
+                          int64_t s_stride_kb, const void* w_e4m3, const void* w_scale,
+                          int32_t w_scale_dtype, int64_t M, int64_t N, int64_t K, void* y_bf16,
+                          int64_t ldy, const bfp8_members* members, void* workspace,
+                          size_t ws_bytes, void* stream);
+
 /* ---- decode GEMV for callers that cannot allocate ------------------------- */
 /*
  * The pages have no counterpart for this entry point. It exists for callers

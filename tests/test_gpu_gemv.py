@@ -94,3 +94,47 @@ def test_gemv_deterministic_workspace_reuse(bfp8, cuda_device):
     torch.cuda.synchronize()
     assert torch.equal(ys[0].view(torch.int16), ys[1].view(torch.int16))
     assert torch.equal(ys[0].view(torch.int16), ys[2].view(torch.int16))
+
+
+# ---- the W8A8 arm: E4M3 tokens with 1x128 scales (bfp8_gemv_decode_w8a8)
+
+def _gemv_w8a8(bfp8, dev, qa, sa, q, s, members=None):
+    M, K = qa.shape
+    N = q.shape[0]
+    y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(bfp8.bfp8_gemv_decode_workspace(M, N, K), dtype=torch.uint8, device=dev)
+    bfp8.bfp8_gemv_decode_w8a8(to_dev_u8(qa, dev), torch.from_numpy(sa).to(dev), to_dev_u8(q, dev),
+                               scale_to_dev(s, dev), y, ws, member_rows=members)
+    torch.cuda.synchronize()
+    assert bfp8.bfp8_device_status() == 0
+    return y
+
+
+@pytest.mark.parametrize("M,N,K,members", [
+    (1, 192, 320, None), (3, 200, 320, None), (8, 130, 256, None), (9, 384, 640, None),
+    (16, 300, 1024, [100, 200]), (5, 1000, 2048, [500, 500]), (16, 256, 128, None),
+])
+def test_gemv_w8a8_small(bfp8, cuda_device, M, N, K, members):
+    g = synth.generator(M * 2000 + N + K)
+    w = synth.weight_f32(g, N, K).numpy()
+    xb = bits16(synth.activations_bf16(g, M, K, outlier="entries", frac=0.01, factor=20.0))
+    q, s = quantize_members(w, members)
+    from oracle import quant as Q
+    qa, sa = Q.act_quant_group(xb)
+    y = _gemv_w8a8(bfp8, cuda_device, qa, sa, q, s, members)
+    assert_close(gpu_bf16_to_f64(y), L.linear_w8a8(qa, sa, q, s, members), f"gemv w8a8 M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("which", ["gate_up", "down"])
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_gemv_w8a8_decode_workload(bfp8, cuda_device, which, M):
+    from oracle import quant as Q
+    qgu, sgu, qd, sd, _ = dense_ffn_weights(0)
+    q, s = (qgu, sgu) if which == "gate_up" else (qd, sd)
+    members = [17408, 17408] if which == "gate_up" else None
+    N, K = q.shape
+    qa, sa = Q.act_quant_group(bits16(synth.decode_tokens(200 + M, M, K)))
+    y = _gemv_w8a8(bfp8, cuda_device, qa, sa, q, s, members)
+    cols = sample_indices(N, 1500, seed=M + 7)
+    assert_close(gpu_bf16_to_f64(y)[:, cols], L.linear_w8a8(qa, sa, q, s, members, cols=cols),
+                 f"decode w8a8 {which} M={M}")
