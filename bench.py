@@ -47,10 +47,10 @@ WORKLOAD = ("dense-FFN prefill chain, W8A8 block-FP8: M=949 BF16 tokens (N(0,1),
 # one ncu capture of the kernel, keyed by a digest of the kernel's sources at
 # capture time: a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
-    "gemm_gate_up_silu_quant": {"bytes": 183_419_136 + 13_309_440, "sources": "1e82c15be072fd98",
+    "gemm_gate_up_silu_quant": {"bytes": 183_412_224 + 13_130_496, "sources": "f8178359f0174f71",
                                 "kernel_files": ("act_math.cuh", "bfp8_internal.h", "gemm_sm103.cu",
                                                  "ptx.cuh")},
-    "gemv_gate_up_m16": {"bytes": 180_574_208 + 4_713_472, "sources": "6a2dd28a22f5f4f0",
+    "gemv_gate_up_m16": {"bytes": 180_575_232 + 4_668_672, "sources": "eea1860b898c1175",
                          "kernel_files": ("bfp8_internal.h", "gemv_decode.cu", "ptx.cuh")},
 }
 
@@ -450,7 +450,28 @@ def run_decode(bfp8, torch, dev, wgu, sgu, wdn, sdn, peaks):
 # --------------------------------------------------------------------------- single-launch mode
 PROFILE_CASES = ("act_quant", "gate_up", "gate_up_silu_quant", "silu_quant", "down",
                  "moe_gate_up_silu_quant", "gemv_gate_up", "gemv_down",
-                 "qkv", "o_proj", "moe_gate_up", "moe_down", "w8a16_gate_up")
+                 "qkv", "o_proj", "moe_gate_up", "moe_down", "w8a16_gate_up",
+                 "moe_gather_quant", "moe_combine", "moe_layer")
+
+
+def _moe_routing(torch, gen, dev, c):
+    """Softmax top-k routing of synthetic logits on the device: the expert
+    offset table, the token of each expert-sorted row, the row of each
+    (token, slot) and the renormalized float32 weights."""
+    from block_scaled_fp8_token_gb300 import synth
+
+    T, E, k = c["tokens"], c["experts"], c["top_k"]
+    logits = synth.router_logits(gen, T, E).to(dev)
+    p, top = torch.topk(torch.softmax(logits.double(), dim=1), k, dim=1)
+    flat = top.reshape(-1)
+    offsets = torch.zeros(E + 1, dtype=torch.int32, device=dev)
+    offsets[1:] = torch.cumsum(torch.bincount(flat, minlength=E), 0).to(torch.int32)
+    perm = torch.argsort(flat, stable=True)
+    row_token = (perm // k).to(torch.int32)
+    row_of = torch.empty(T * k, dtype=torch.int32, device=dev)
+    row_of[perm] = torch.arange(T * k, dtype=torch.int32, device=dev)
+    weights = (p / p.sum(dim=1, keepdim=True)).float().contiguous()
+    return offsets, row_token, row_of.reshape(T, k), weights
 
 
 def setup_case(case, bfp8, torch, dev, gen, decode_m=16):
@@ -533,15 +554,44 @@ def setup_case(case, bfp8, torch, dev, gen, decode_m=16):
                          device=dev)
         return (lambda: bfp8.bfp8_linear_w8a8(qa, sa, w, sw, y, member_rows=members, workspace=ws)), \
             2 * M * N * K, "TFLOP/s", "tensor"
+    if case in ("moe_gather_quant", "moe_combine", "moe_layer"):
+        c = synth.MOE_PREFILL
+        T, E, k, H, I = c["tokens"], c["experts"], c["top_k"], c["hidden"], c["inter"]
+        R = T * k
+        offsets, row_token, row_of, weights = _moe_routing(torch, gen, dev, c)
+        if case == "moe_combine":
+            y = synth.activations_bf16(gen, R, H).to(dev)
+            out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+            return (lambda: bfp8.bfp8_moe_combine(y, row_of, weights, out)), \
+                R * H * 2 + R * 8 + T * H * 2, "GB/s", "hbm"
+        x = synth.activations_bf16(gen, T, H).to(dev)
+        qa = torch.empty(R, H, dtype=torch.uint8, device=dev)
+        sa = torch.empty(R, H // 128, dtype=torch.float32, device=dev)
+        if case == "moe_gather_quant":
+            return (lambda: bfp8.bfp8_moe_gather_act_quant(x, row_token, qa, sa)), \
+                T * H * 2 + R * 4 + R * H + R * (H // 128) * 4, "GB/s", "hbm"
+        wgu, sgu = qweight(2 * I, H, G=E)
+        wd, sd = qweight(H, I, G=E)
+        qh = torch.empty(R, I, dtype=torch.uint8, device=dev)
+        sh = torch.empty(R, I // 128, dtype=torch.float32, device=dev)
+        y = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        ws1 = torch.empty(bfp8.bfp8_grouped_linear_silu_quant_workspace(R, E, I, H),
+                          dtype=torch.uint8, device=dev)
+        ws2 = torch.empty(bfp8.bfp8_grouped_linear_workspace(R, E, H, I), dtype=torch.uint8,
+                          device=dev)
+
+        def layer():
+            bfp8.bfp8_moe_gather_act_quant(x, row_token, qa, sa)
+            bfp8.bfp8_grouped_linear_silu_quant(qa, sa, wgu, sgu, offsets, qh, sh, workspace=ws1)
+            bfp8.bfp8_grouped_linear(qh, sh, wd, sd, offsets, y, workspace=ws2)
+            bfp8.bfp8_moe_combine(y, row_of, weights, out)
+        return layer, 2 * R * (2 * I * H + H * I), "TFLOP/s", "tensor"
     if case in ("moe_gate_up", "moe_down", "moe_gate_up_silu_quant"):
         c = synth.MOE_PREFILL
         T, E, k = c["tokens"], c["experts"], c["top_k"]
         N, K = (c["hidden"], c["inter"]) if case == "moe_down" else (2 * c["inter"], c["hidden"])
-        logits = synth.router_logits(gen, T, E).to(dev)
-        top = torch.topk(torch.softmax(logits.double(), dim=1), k, dim=1).indices.reshape(-1)
-        counts = torch.bincount(top, minlength=E)
-        offsets = torch.zeros(E + 1, dtype=torch.int32, device=dev)
-        offsets[1:] = torch.cumsum(counts, 0).to(torch.int32)
+        offsets = _moe_routing(torch, gen, dev, c)[0]
         w, sw = qweight(N, K, G=E)
         x, qa, sa = qact(T * k, K)
         if case == "moe_gate_up_silu_quant":
@@ -603,7 +653,8 @@ def run_profile(args, local):
 
 
 WORKLOAD_CASES = ("gate_up", "qkv", "o_proj", "moe_gate_up_silu_quant", "moe_gate_up", "moe_down",
-                  "w8a16_gate_up", "act_quant", "silu_quant")
+                  "moe_layer", "w8a16_gate_up", "act_quant", "silu_quant", "moe_gather_quant",
+                  "moe_combine")
 
 
 def run_workloads(bfp8, torch, dev, peaks, steps: int = 50) -> dict:

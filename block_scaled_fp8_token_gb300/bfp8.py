@@ -94,6 +94,10 @@ _SIGS = {
                                                       _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i64,
                                                       _i64, _vp, _sz, _vp]),
     "bfp8_grouped_linear_silu_quant_workspace": (_sz, [_i64, _i32, _i64, _i64]),
+    "bfp8_moe_gather_act_quant": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp,
+                                                 _i64, _i64, _vp]),
+    "bfp8_moe_combine": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _i32, _vp, _i64,
+                                        _vp]),
     "bfp8_device_status": (ctypes.c_int, [_vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -347,6 +351,28 @@ def bfp8_grouped_linear_silu_quant(q_a, s_a, w, w_scale, offsets, q_h, s_h, s_st
                                                q_h.stride(0), _ptr(s_h), hsm, hskb, wsp, wsb,
                                                _stream(stream)),
            "bfp8_grouped_linear_silu_quant")
+
+
+def bfp8_moe_gather_act_quant(x, row_token, q, scales, s_stride_m=None, s_stride_kb=None,
+                              stream=None) -> None:
+    """q[r], scales[r] = 1x128 quantization of x[row_token[r]] (int32 on the device)."""
+    T, H = x.shape
+    R = row_token.shape[0]
+    ssm = scales.stride(0) if s_stride_m is None else s_stride_m
+    sskb = scales.stride(1) if s_stride_kb is None else s_stride_kb
+    _check(_lib.bfp8_moe_gather_act_quant(_ptr(x), T, H, x.stride(0), _ptr(row_token), R, _ptr(q),
+                                          q.stride(0), _ptr(scales), ssm, sskb, _stream(stream)),
+           "bfp8_moe_gather_act_quant")
+
+
+def bfp8_moe_combine(y, token_rows, token_weights, out, stream=None) -> None:
+    """out[t] = bf16(sum_j token_weights[t, j] * y[token_rows[t, j]]), slot order j."""
+    R, H = y.shape
+    T, topk = token_rows.shape
+    _check(_lib.bfp8_moe_combine(_ptr(y), R, H, y.stride(0), _ptr(token_rows),
+                                 _ptr(token_weights), T, topk, _ptr(out), out.stride(0),
+                                 _stream(stream)),
+           "bfp8_moe_combine")
 
 
 def bfp8_device_status(stream=None) -> int:

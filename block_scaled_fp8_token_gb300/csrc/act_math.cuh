@@ -18,8 +18,13 @@ __device__ __forceinline__ float silu_mul_bf16_round(float g, float u) {
   return __bfloat162float(__float2bfloat16_rn(s * u));
 }
 
-// The 1x128 scale of a group with maximum |x| = amax.
-__device__ __forceinline__ float group_scale(float amax) { return fmaxf(amax, 1e-10f) / 448.0f; }
+// The 1x128 scale of a group with maximum |x| = amax: the correctly rounded
+// max(amax, 1e-10f) / 448, formed as div_by_scale below with the correctly
+// rounded reciprocal of 448 (a constant), so no division is issued.
+__device__ __forceinline__ float div_by_scale(float x, float s, float y);
+__device__ __forceinline__ float group_scale(float amax) {
+  return div_by_scale(fmaxf(amax, 1e-10f), 448.0f, 1.0f / 448.0f);
+}
 
 // RN(x / s) given y = RN(1 / s): one remainder correction. Markstein's
 // theorem: with y within half an ulp of 1/s and q0 = RN(x*y) within one ulp
@@ -31,6 +36,14 @@ __device__ __forceinline__ float div_by_scale(float x, float s, float y) {
   const float q0 = x * y;
   const float r = fmaf(-q0, s, x);
   return fmaf(r, y, q0);
+}
+
+// div_by_scale on two values at once (packed FP32 operations, the same
+// roundings per lane): ns = (-s, -s), y = (RN(1/s), RN(1/s)).
+__device__ __forceinline__ float2 div_by_scale2(float2 x, float2 ns, float2 y) {
+  const float2 q0 = __fmul2_rn(x, y);
+  const float2 r = __ffma2_rn(q0, ns, x);
+  return __ffma2_rn(r, y, q0);
 }
 
 }  // namespace dev

@@ -280,6 +280,21 @@ int bfp8_silu_mul_act_quant(const void* gu_bf16, int64_t M, int64_t I, int64_t l
                                    s_stride_kb, stream);
 }
 
+int bfp8_moe_gather_act_quant(const void* x_bf16, int64_t T, int64_t H, int64_t ldx,
+                              const int32_t* row_token, int64_t R, void* q_e4m3, int64_t ldq,
+                              float* scales, int64_t s_stride_m, int64_t s_stride_kb,
+                              void* stream) {
+  return launch_moe_gather_act_quant(x_bf16, T, H, ldx, row_token, R, q_e4m3, ldq, scales,
+                                     s_stride_m, s_stride_kb, stream);
+}
+
+int bfp8_moe_combine(const void* y_bf16, int64_t R, int64_t H, int64_t ldy,
+                     const int32_t* token_rows, const float* token_weights, int64_t T,
+                     int32_t topk, void* out_bf16, int64_t ldo, void* stream) {
+  return launch_moe_combine(y_bf16, R, H, ldy, token_rows, token_weights, T, topk, out_bf16, ldo,
+                            stream);
+}
+
 int bfp8_quantize_weight_block(const float* w, int64_t N, int64_t K, int64_t ldw, void* q,
                                int64_t ldq, void* scale, int32_t scale_dtype, void* stream) {
   return launch_weight_quant(w, N, K, ldw, q, ldq, scale, scale_dtype, stream);

@@ -42,6 +42,12 @@ int launch_act_quant(const void* x, int64_t M, int64_t K, int64_t ldx, void* q, 
                      float* s, int64_t ssm, int64_t sskb, void* stream);
 int launch_silu_mul_act_quant(const void* gu, int64_t M, int64_t I, int64_t ld, void* q,
                               int64_t ldq, float* s, int64_t ssm, int64_t sskb, void* stream);
+int launch_moe_gather_act_quant(const void* x, int64_t T, int64_t H, int64_t ldx,
+                                const int32_t* row_token, int64_t R, void* q, int64_t ldq,
+                                float* s, int64_t ssm, int64_t sskb, void* stream);
+int launch_moe_combine(const void* y, int64_t R, int64_t H, int64_t ldy, const int32_t* token_rows,
+                       const float* token_weights, int64_t T, int32_t topk, void* out, int64_t ldo,
+                       void* stream);
 int launch_weight_quant(const float* w, int64_t N, int64_t K, int64_t ldw, void* q, int64_t ldq,
                         void* scale, int32_t scale_dtype, void* stream);
 

@@ -24,101 +24,139 @@ using namespace dev;
 
 constexpr int kThreads = 256;
 
-// SILU == false: x is [M, K] with row stride ld; values are x[m, c].
-// SILU == true : x is [M, 2K] with row stride ld; values are
-//                bf16(silu(x[m, c]) * x[m, K + c]).
-// A half-warp owns one (token, 128-column group): each lane holds 8 consecutive
-// elements (one 16-byte load), the group maximum is a 4-step shuffle within the
-// half-warp, and each half-warp keeps kUnroll groups in flight.
-constexpr int kUnroll = 2;
+// A quad of lanes owns one (token, 128-column group). Lane ql of the quad holds
+// the 8-column chunks that start at 32 i + 8 ql (i = 0..3), so each 16-byte
+// load of a quad covers 64 contiguous bytes and each 8-byte store 32. The
+// per-group work (the maximum over the quad, the scale, its reciprocal, the
+// scale store, the index update) is spread over 32 elements per lane.
+constexpr int kQuad = 4;
+constexpr int kChunks = 4;
 
-template <bool SILU>
-__device__ __forceinline__ void load8(const __nv_bfloat16* row, int64_t c, int64_t K, bool vec,
-                                      float (&v)[8]) {
+// row[c .. c+8) as four bf16x2 words, zero past K.
+__device__ __forceinline__ void load_chunk(const __nv_bfloat16* row, int64_t c, int64_t K,
+                                           bool vec, uint32_t (&w)[4]) {
   if (vec && c + 8 <= K) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(row + c);
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[2 * i] = bf16_bits_to_f32(static_cast<uint16_t>(w[i] & 0xFFFFu));
-      v[2 * i + 1] = bf16_bits_to_f32(static_cast<uint16_t>(w[i] >> 16));
-    }
-    if (SILU) {
-      const uint4 ru = *reinterpret_cast<const uint4*>(row + K + c);
-      const uint32_t u[4] = {ru.x, ru.y, ru.z, ru.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[2 * i] = silu_mul_bf16_round(v[2 * i], bf16_bits_to_f32(static_cast<uint16_t>(u[i] & 0xFFFFu)));
-        v[2 * i + 1] = silu_mul_bf16_round(v[2 * i + 1], bf16_bits_to_f32(static_cast<uint16_t>(u[i] >> 16)));
-      }
-    }
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(row + c));
+    w[0] = raw.x;
+    w[1] = raw.y;
+    w[2] = raw.z;
+    w[3] = raw.w;
   } else {
+    const uint16_t* r16 = reinterpret_cast<const uint16_t*>(row);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      v[i] = 0.0f;
-      if (c + i < K) {
-        v[i] = __bfloat162float(row[c + i]);
-        if (SILU) v[i] = silu_mul_bf16_round(v[i], __bfloat162float(row[K + c + i]));
-      }
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t lo = c + 2 * j < K ? r16[c + 2 * j] : 0u;
+      const uint32_t hi = c + 2 * j + 1 < K ? r16[c + 2 * j + 1] : 0u;
+      w[j] = lo | (hi << 16);
     }
   }
 }
 
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// SILU == false: x is [M, K] with row stride ld; values are x[m, c].
+// SILU == true : x is [M, 2K] with row stride ld; values are
+//                bf16(silu(x[m, c]) * x[m, K + c]).
+// rows == nullptr: output row m quantizes input row m. Otherwise output row m
+// quantizes input row rows[m] (a gather, e.g. routed MoE rows); an index
+// outside [0, n_src) quantizes a zero row.
+// For finite inputs the codes and scales equal the CPU definition bit for bit:
+// the group maximum is exact (taken on the BF16 bit patterns of |x|, or on the
+// BF16-rounded h), and every quotient is the correctly rounded x / s.
 template <bool SILU>
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K, int64_t ld,
     uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s, int64_t ssm, int64_t sskb,
-    int vec_in, int vec_out) {
+    int vec_in, int vec_out, const int32_t* __restrict__ rows, int64_t n_src) {
   const int64_t Kb = (K + 127) / 128;
-  const int64_t total = M * Kb;
-  const int lane = threadIdx.x & 31;
-  const int hl = lane & 15;                      // lane within the half-warp
-  const int64_t hw0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
-  const int64_t nhw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 4;
-  for (int64_t base = hw0; base < total; base += nhw * kUnroll) {
-    float v[kUnroll][8];
+  const int ql = threadIdx.x & (kQuad - 1);
+  const int64_t quad = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / kQuad;
+  const int64_t nquad = static_cast<int64_t>(gridDim.x) * blockDim.x / kQuad;
+  // (m, g) of this quad's group, advanced by nquad groups per pass without a division
+  int64_t m = quad / Kb, g = quad - m * Kb;
+  const int64_t dm = nquad / Kb, dg = nquad - dm * Kb;
+  while (__any_sync(0xffffffffu, m < M)) {
+    const bool live = m < M;
+    const int64_t src = !live ? -1 : (rows ? static_cast<int64_t>(__ldg(rows + m)) : m);
+    const bool ok = src >= 0 && src < n_src;
+    const __nv_bfloat16* row = x + (ok ? src : 0) * ld;
+    const int64_t c0 = g * 128 + ql * 8;
+    uint32_t a[kChunks][4];
+    float h[SILU ? kChunks : 1][8];
+    float amax;
+    if constexpr (SILU) {
+      amax = 0.0f;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t item = base + u * nhw;
-      if (item < total) {
-        const int64_t m = item / Kb, g = item - m * Kb;
-        load8<SILU>(x + m * ld, g * 128 + hl * 8, K, vec_in, v[u]);
+      for (int i = 0; i < kChunks; ++i) {
+        uint32_t u[4] = {0u, 0u, 0u, 0u};
+        a[i][0] = a[i][1] = a[i][2] = a[i][3] = 0u;
+        if (ok) {
+          load_chunk(row, c0 + 32 * i, K, vec_in, a[i]);
+          load_chunk(row + K, c0 + 32 * i, K, vec_in, u);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          h[i][2 * j] = silu_mul_bf16_round(lo_bf16(a[i][j]), lo_bf16(u[j]));
+          h[i][2 * j + 1] = silu_mul_bf16_round(hi_bf16(a[i][j]), hi_bf16(u[j]));
+          amax = fmaxf(amax, fmaxf(fabsf(h[i][2 * j]), fabsf(h[i][2 * j + 1])));
+        }
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    } else {
+      uint32_t mx = 0u;
+#pragma unroll
+      for (int i = 0; i < kChunks; ++i) {
+        a[i][0] = a[i][1] = a[i][2] = a[i][3] = 0u;
+        if (ok) load_chunk(row, c0 + 32 * i, K, vec_in, a[i]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mx = max_u16x2(mx, a[i][j] & 0x7FFF7FFFu);
+      }
+      // |x| of a finite BF16 orders like its bit pattern with the sign cleared
+      uint32_t am = max(mx & 0xFFFFu, mx >> 16);
+      am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
+      am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
+      amax = __uint_as_float(am << 16);
+    }
+    const float sc = group_scale(amax);
+    const float rc = __frcp_rn(sc);
+    const float2 y2 = make_float2(rc, rc), ns2 = make_float2(-sc, -sc);
+    uint8_t* qrow = q + (live ? m : 0) * ldq;
+#pragma unroll
+    for (int i = 0; i < kChunks; ++i) {
+      uint16_t p[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 v = SILU ? make_float2(h[SILU ? i : 0][2 * j], h[SILU ? i : 0][2 * j + 1])
+                              : make_float2(lo_bf16(a[i][j]), hi_bf16(a[i][j]));
+        const float2 qv = div_by_scale2(v, ns2, y2);
+        p[j] = f32x2_to_e4m3x2(qv.x, qv.y);
+      }
+      const uint32_t w0 = static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[1]) << 16);
+      const uint32_t w1 = static_cast<uint32_t>(p[2]) | (static_cast<uint32_t>(p[3]) << 16);
+      const int64_t c = c0 + 32 * i;
+      if (!live) continue;
+      if (vec_out && c + 8 <= K) {
+        *reinterpret_cast<uint2*>(qrow + c) = make_uint2(w0, w1);
       } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[u][i] = 0.0f;
+        for (int e = 0; e < 8; ++e)
+          if (c + e < K) qrow[c + e] = static_cast<uint8_t>((e < 4 ? w0 : w1) >> (8 * (e & 3)));
       }
     }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t item = base + u * nhw;
-      float amax = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[u][i]));
-#pragma unroll
-      for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      if (item >= total) continue;
-      const float sc = group_scale(amax);
-      const float rc = __frcp_rn(sc);
-      const int64_t m = item / Kb, g = item - m * Kb;
-      const int64_t c = g * 128 + hl * 8;
-      uint32_t w[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const uint16_t lo = f32x2_to_e4m3x2(div_by_scale(v[u][4 * i], sc, rc),
-                                            div_by_scale(v[u][4 * i + 1], sc, rc));
-        const uint16_t hi = f32x2_to_e4m3x2(div_by_scale(v[u][4 * i + 2], sc, rc),
-                                            div_by_scale(v[u][4 * i + 3], sc, rc));
-        w[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-      }
-      uint8_t* qrow = q + m * ldq;
-      if (vec_out && c + 8 <= K) {
-        *reinterpret_cast<uint2*>(qrow + c) = make_uint2(w[0], w[1]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (c + i < K) qrow[c + i] = static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
-      }
-      if (hl == 0) s[m * ssm + g * sskb] = sc;
+    if (live && ql == 0) s[m * ssm + g * sskb] = sc;
+    m += dm;
+    g += dg;
+    if (g >= Kb) {
+      g -= Kb;
+      ++m;
     }
   }
 }
@@ -182,8 +220,110 @@ __global__ void __launch_bounds__(kThreads) weight_quant_kernel(
   }
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// out[t, c] = bf16( sum_j w[t, j] * y[rows[t, j], c] ), FP32 fused multiply-adds
+// in slot order j (deterministic). A row index outside [0, R) adds nothing.
+// Each thread owns 8 consecutive columns of one token; the slots are fetched
+// kSlotBatch at a time, all loads issued before the first multiply-add.
+constexpr int kSlotBatch = 8;
+
+__global__ void __launch_bounds__(kThreads) moe_combine_kernel(
+    const __nv_bfloat16* __restrict__ y, int64_t R, int64_t H, int64_t ldy,
+    const int32_t* __restrict__ rows, const float* __restrict__ w, int64_t T, int topk,
+    __nv_bfloat16* __restrict__ out, int64_t ldo, int vec) {
+  const int64_t hc = (H + 7) / 8;
+  const int64_t it0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t t = it0 / hc, cc = it0 - t * hc;
+  const int64_t dt = step / hc, dc = step - dt * hc;
+  for (; t < T; t += dt, cc += dc) {
+    if (cc >= hc) {
+      cc -= hc;
+      ++t;
+      if (t >= T) break;
+    }
+    const int64_t c = cc * 8;
+    const bool full = vec && c + 8 <= H;
+    float2 acc[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] = make_float2(0.0f, 0.0f);
+    const int32_t* rt = rows + t * topk;
+    const float* wt = w + t * topk;
+    for (int j0 = 0; j0 < topk; j0 += kSlotBatch) {
+      int64_t r[kSlotBatch];
+      float wj[kSlotBatch];
+      uint4 raw[kSlotBatch];
+#pragma unroll
+      for (int u = 0; u < kSlotBatch; ++u) {
+        const bool in = j0 + u < topk;
+        r[u] = in ? static_cast<int64_t>(__ldg(rt + j0 + u)) : -1;
+        wj[u] = in ? __ldg(wt + j0 + u) : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < kSlotBatch; ++u) {
+        raw[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (r[u] < 0 || r[u] >= R) continue;
+        const __nv_bfloat16* src = y + r[u] * ldy + c;
+        if (full) {
+          raw[u] = __ldg(reinterpret_cast<const uint4*>(src));
+        } else {
+          const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
+          uint32_t wd[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t lo = c + 2 * e < H ? s16[2 * e] : 0u;
+            const uint32_t hi = c + 2 * e + 1 < H ? s16[2 * e + 1] : 0u;
+            wd[e] = lo | (hi << 16);
+          }
+          raw[u] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kSlotBatch; ++u) {
+        if (r[u] < 0 || r[u] >= R) continue;
+        const float2 w2 = make_float2(wj[u], wj[u]);
+        const uint32_t wd[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          acc[e] = __ffma2_rn(w2, make_float2(lo_bf16(wd[e]), hi_bf16(wd[e])), acc[e]);
+      }
+    }
+    __nv_bfloat16* dst = out + t * ldo + c;
+    if (full) {
+      uint4 o;
+      o.x = pack_bf16x2(acc[0].x, acc[0].y);
+      o.y = pack_bf16x2(acc[1].x, acc[1].y);
+      o.z = pack_bf16x2(acc[2].x, acc[2].y);
+      o.w = pack_bf16x2(acc[3].x, acc[3].y);
+      *reinterpret_cast<uint4*>(dst) = o;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (c + e < H) dst[e] = __float2bfloat16_rn(e & 1 ? acc[e >> 1].y : acc[e >> 1].x);
+    }
+  }
+}
+
+// Blocks of kThreads that one SM keeps resident for `kernel` (at least 1):
+// the grid-stride kernels launch exactly one wave of them.
+template <typename Kernel>
+int resident_blocks(Kernel kernel) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, 0) != cudaSuccess ||
+      n < 1) {
+    cudaGetLastError();
+    n = 1;
+  }
+  return n;
+}
+
 int act_quant_common(bool silu, const void* x, int64_t M, int64_t K, int64_t ld, void* q,
-                     int64_t ldq, float* s, int64_t ssm, int64_t sskb, void* stream) {
+                     int64_t ldq, float* s, int64_t ssm, int64_t sskb, void* stream,
+                     const int32_t* rows = nullptr, int64_t n_src = 0) {
   if (M < 0 || K < 0) return BFP8_ERR_INVALID_ARG;
   if (M == 0 || K == 0) return BFP8_OK;
   if (!x || !q || !s) return BFP8_ERR_INVALID_ARG;
@@ -197,20 +337,22 @@ int act_quant_common(bool silu, const void* x, int64_t M, int64_t K, int64_t ld,
   if (rc != BFP8_OK) return rc;
   const int vec_in = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (ld % 8 == 0) && (K % 8 == 0);
   const int vec_out = (reinterpret_cast<uintptr_t>(q) % 8 == 0) && (ldq % 8 == 0);
+  static const int per_sm[2] = {resident_blocks(act_quant_kernel<false>),
+                                resident_blocks(act_quant_kernel<true>)};
   const int64_t items = M * Kb;
-  const int64_t per_block = (kThreads / 16) * kUnroll;   // groups one block covers per pass
+  const int64_t per_block = kThreads / kQuad;   // groups one block covers per pass
   const int64_t want = (items + per_block - 1) / per_block;
-  const int64_t cap = static_cast<int64_t>(sms) * 8;
+  const int64_t cap = static_cast<int64_t>(sms) * per_sm[silu ? 1 : 0];
   const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (silu)
     act_quant_kernel<true><<<blocks, kThreads, 0, st>>>(
         static_cast<const __nv_bfloat16*>(x), M, K, ld, static_cast<uint8_t*>(q), ldq, s, ssm,
-        sskb, vec_in, vec_out);
+        sskb, vec_in, vec_out, rows, rows ? n_src : M);
   else
     act_quant_kernel<false><<<blocks, kThreads, 0, st>>>(
         static_cast<const __nv_bfloat16*>(x), M, K, ld, static_cast<uint8_t*>(q), ldq, s, ssm,
-        sskb, vec_in, vec_out);
+        sskb, vec_in, vec_out, rows, rows ? n_src : M);
   return check_launch();
 }
 
@@ -224,6 +366,37 @@ int launch_act_quant(const void* x, int64_t M, int64_t K, int64_t ldx, void* q, 
 int launch_silu_mul_act_quant(const void* gu, int64_t M, int64_t I, int64_t ld, void* q,
                               int64_t ldq, float* s, int64_t ssm, int64_t sskb, void* stream) {
   return act_quant_common(true, gu, M, I, ld, q, ldq, s, ssm, sskb, stream);
+}
+
+int launch_moe_gather_act_quant(const void* x, int64_t T, int64_t H, int64_t ldx,
+                                const int32_t* row_token, int64_t R, void* q, int64_t ldq,
+                                float* s, int64_t ssm, int64_t sskb, void* stream) {
+  if (T < 0 || R < 0 || H < 0) return BFP8_ERR_INVALID_ARG;
+  if (R == 0 || H == 0) return BFP8_OK;
+  if (!row_token) return BFP8_ERR_INVALID_ARG;
+  return act_quant_common(false, x, R, H, ldx, q, ldq, s, ssm, sskb, stream, row_token, T);
+}
+
+int launch_moe_combine(const void* y, int64_t R, int64_t H, int64_t ldy, const int32_t* token_rows,
+                       const float* token_weights, int64_t T, int32_t topk, void* out, int64_t ldo,
+                       void* stream) {
+  if (R < 0 || H < 0 || T < 0 || topk < 1) return BFP8_ERR_INVALID_ARG;
+  if (T == 0 || H == 0) return BFP8_OK;
+  if (!y || !token_rows || !token_weights || !out || ldy < H || ldo < H) return BFP8_ERR_INVALID_ARG;
+  int sms = 0;
+  int rc = sm_count(&sms);
+  if (rc != BFP8_OK) return rc;
+  const int vec = (reinterpret_cast<uintptr_t>(y) % 16 == 0) && (ldy % 8 == 0) &&
+                  (reinterpret_cast<uintptr_t>(out) % 16 == 0) && (ldo % 8 == 0);
+  static const int per_sm = resident_blocks(moe_combine_kernel);
+  const int64_t items = T * ((H + 7) / 8);
+  const int64_t want = (items + kThreads - 1) / kThreads;
+  const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+  const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
+  moe_combine_kernel<<<blocks, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(y), R, H, ldy, token_rows, token_weights, T, topk,
+      static_cast<__nv_bfloat16*>(out), ldo, vec);
+  return check_launch();
 }
 
 int launch_weight_quant(const float* w, int64_t N, int64_t K, int64_t ldw, void* q, int64_t ldq,

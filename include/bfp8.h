@@ -390,6 +390,49 @@ int bfp8_grouped_linear_silu_quant(const void* q_a, const float* s_a, int64_t s_
                                    float* s_h, int64_t sh_stride_m, int64_t sh_stride_kb,
                                    void* workspace, size_t ws_bytes, void* stream);
 
+/* ---- the steps on either side of the grouped MoE projection -------------- */
+/*
+ * bfp8_moe_gather_act_quant -- permutation by expert fused with the per-token
+ * 1x128 activation quantization: routed row r of the expert-sorted buffer
+ * quantizes token row_token[r] of x.
+ *   [Module w8a8_prefill, "WHY": the MoE expert path on the block-scaled
+ *    prefill arm; arithmetic paragraph: per-token 1x128 FP32 activation scales]
+ * Each output row equals bfp8_act_quant_group of its source token row, so
+ * the E4M3 codes and scales are bit-exact with quantizing first and
+ * permuting after.
+ *   x_bf16     [T, H] BF16 tokens, row stride ldx >= H (elements)
+ *   row_token  device int32 [R]: the source token of each routed row; an
+ *              index outside [0, T) yields a zero row (codes 0, scale 1e-10f/448)
+ *   q_e4m3     [R, H] E4M3, row stride ldq >= H (bytes)
+ *   scales     float32, (r, g) at scales[r*s_stride_m + g*s_stride_kb]
+ * R == 0 or H == 0 is a no-op. Errors: INVALID_ARG for null pointers,
+ * negative sizes or ld < H.
+ */
+int bfp8_moe_gather_act_quant(const void* x_bf16, int64_t T, int64_t H, int64_t ldx,
+                              const int32_t* row_token, int64_t R, void* q_e4m3, int64_t ldq,
+                              float* scales, int64_t s_stride_m, int64_t s_stride_kb,
+                              void* stream);
+
+/*
+ * bfp8_moe_combine -- un-permute and weight the routed rows of the down
+ * projection back onto their tokens:
+ *   out[t, c] = bf16_rn( sum_{j=0}^{topk-1} w[t, j] * y[rows[t, j], c] )
+ * as float32 fused multiply-adds in slot order j = 0, 1, ... from 0, so the
+ * result is deterministic (no atomics).
+ *   [Module w8a8_prefill, "WHY": the MoE expert path; the weights are the
+ *    renormalized top-k router probabilities]
+ *   y_bf16         [R, H] BF16 routed rows (expert-sorted), row stride ldy >= H
+ *   token_rows     device int32 [T, topk]: the routed row of each (token, slot);
+ *                  an index outside [0, R) contributes nothing
+ *   token_weights  device float32 [T, topk]
+ *   out_bf16       [T, H] BF16, row stride ldo >= H; must not overlap y
+ * T == 0 or H == 0 is a no-op. Errors: INVALID_ARG for null pointers,
+ * negative sizes, topk < 1 or ld < H.
+ */
+int bfp8_moe_combine(const void* y_bf16, int64_t R, int64_t H, int64_t ldy,
+                     const int32_t* token_rows, const float* token_weights, int64_t T,
+                     int32_t topk, void* out_bf16, int64_t ldo, void* stream);
+
 /* ---- diagnostics ---------------------------------------------------------- */
 /*
  * bfp8_device_status -- synchronise `stream`, then read and clear the library's
