@@ -352,6 +352,48 @@ def run_ours(args, rank, world, local):
     return out
 
 
+def _graph_time(torch, dev, stream, call, n_launch):
+    """Median GPU time (us) per call(j), j = 0 .. n_launch-1, from a CUDA graph
+    of the n_launch calls replayed 5 times (eager back-to-back launches if the
+    capture is refused). call(j, g_stream) enqueues on g_stream."""
+    g_stream = torch.cuda.Stream(dev)
+    g_stream.wait_stream(stream)
+    with torch.cuda.stream(g_stream):
+        for j in range(3):
+            call(j, g_stream)
+    torch.cuda.synchronize()
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=g_stream):
+            for j in range(n_launch):
+                call(j, g_stream)
+        run = graph.replay
+        note = (f"CUDA graph of {n_launch} calls rotating over the weight copies, replayed 5 "
+                "times; us = median replay time / calls")
+    except RuntimeError as exc:  # capture refused: eager back-to-back launches
+        graph = None
+
+        def run():
+            for j in range(n_launch):
+                call(j, g_stream)
+        note = f"eager back-to-back launches (graph capture failed: {exc})"
+    times = []
+    with torch.cuda.stream(g_stream):
+        for _ in range(2):
+            run()
+        torch.cuda.synchronize()
+        for _ in range(5):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(g_stream)
+            run()
+            e1.record(g_stream)
+            times.append((e0, e1))
+    torch.cuda.synchronize()
+    del graph
+    return statistics.median(a.elapsed_time(b) for a, b in times) * 1e3 / n_launch, note
+
+
 def run_decode(bfp8, torch, dev, wgu, sgu, wdn, sdn, peaks):
     """Decode GEMV (M in {1, 4, 16}) on the same weights: weight GB/s. The timed
     launches rotate over enough copies of the weights (>= 2x L2) that no
@@ -381,7 +423,7 @@ def run_decode(bfp8, torch, dev, wgu, sgu, wdn, sdn, peaks):
             sa = torch.empty(M, K // 128, dtype=torch.float32, device=dev)
             bfp8.bfp8_act_quant_group(x, qa, sa, stream=stream)
 
-            def call(j):
+            def call(j, g_stream):
                 w, s = ring[j % len(ring)]
                 if arm == "w8a8":
                     bfp8.bfp8_gemv_decode_w8a8(qa, sa, w, s, y, ws, member_rows=members,
@@ -389,46 +431,8 @@ def run_decode(bfp8, torch, dev, wgu, sgu, wdn, sdn, peaks):
                 else:
                     bfp8.bfp8_gemv_decode(x, w, s, y, ws, member_rows=members, stream=g_stream)
 
-            # a CUDA graph of launches rotating over the copies: GPU time with
-            # the gaps between kernels, without the host's launch cost
-            g_stream = torch.cuda.Stream(dev)
-            g_stream.wait_stream(stream)
-            with torch.cuda.stream(g_stream):
-                for j in range(3):
-                    call(j)
-            torch.cuda.synchronize()
-            n_launch = 4 * len(ring)
-            times = []
-            try:
-                graph = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(graph, stream=g_stream):
-                    for j in range(n_launch):
-                        call(j)
-                run = graph.replay
-                res.setdefault("timing", "CUDA graph of 4 x copies bfp8_gemv_decode calls "
-                                         "(split-token kernel + GEMV each), replayed 5 times; "
-                                         "us = median replay time / launches")
-            except RuntimeError as exc:  # capture refused: eager back-to-back launches
-                graph = None
-
-                def run():
-                    for j in range(n_launch):
-                        call(j)
-                res["timing"] = f"eager back-to-back launches (graph capture failed: {exc})"
-            with torch.cuda.stream(g_stream):
-                for _ in range(2):
-                    run()
-                torch.cuda.synchronize()
-                for r in range(5):
-                    e0 = torch.cuda.Event(enable_timing=True)
-                    e1 = torch.cuda.Event(enable_timing=True)
-                    e0.record(g_stream)
-                    run()
-                    e1.record(g_stream)
-                    times.append((e0, e1))
-            torch.cuda.synchronize()
-            del graph
-            us = statistics.median(a.elapsed_time(b) for a, b in times) * 1e3 / n_launch
+            us, note = _graph_time(torch, dev, stream, call, 4 * len(ring))
+            res.setdefault("timing", note)
             s0 = ring[0][1]
             nbytes = N * K + s0.numel() * 2 + M * K * 2 + M * N * 2
             gbs = nbytes / (us * 1e-6) / 1e9
@@ -437,6 +441,29 @@ def run_decode(bfp8, torch, dev, wgu, sgu, wdn, sdn, peaks):
             if name == "gate_up" and M == 16 and arm == "w8a16":
                 best = row[name]
         res["shapes"][f"M={M}" if arm == "w8a16" else f"M={M} W8A8 (E4M3 tokens)"] = row
+    # the whole decode FFN step (gate/up GEMV -> SiLU*up -> down GEMV) as one call
+    res["step"] = {"what": "bfp8_decode_ffn: gate/up GEMV -> SiLU*up -> down GEMV, one call; "
+                           "bytes = both weights + scales + x + y", "shapes": {}}
+    gu_ring, dn_ring = copies["gate_up"], copies["down"]
+    for arm, M in [("w8a16", 1), ("w8a16", 16), ("w8a8", 1), ("w8a8", 16)]:
+        code = bfp8.BFP8_DECODE_W8A8 if arm == "w8a8" else bfp8.BFP8_DECODE_W8A16
+        x = synth.decode_tokens(500 + M, M, HID).to(dev)
+        y = torch.empty(M, HID, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(bfp8.bfp8_decode_ffn_workspace(M, HID, INTER, code), dtype=torch.uint8,
+                         device=dev)
+
+        def step(j, g_stream):
+            wg, sg = gu_ring[j % len(gu_ring)]
+            wd, sd = dn_ring[j % len(dn_ring)]
+            bfp8.bfp8_decode_ffn(x, wg, sg, wd, sd, y, ws, arith=code, stream=g_stream)
+        us, note = _graph_time(torch, dev, stream, step, 4 * max(len(gu_ring), len(dn_ring)))
+        nbytes = (wgu.numel() + wdn.numel() + 2 * (sgu.numel() + sdn.numel())
+                  + 2 * M * HID * 2)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res["step"]["shapes"][f"M={M} {arm.upper()}"] = {
+            "us": round(us, 2), "bytes": nbytes, "GB/s": round(gbs, 1),
+            "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+        res["step"].setdefault("timing", note)
     res["roofline"] = {"bound": "hbm", "kernel": "gemv_kernel (gate/up [34816,5120], M=16)",
                        "achieved": best["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
                        "frac": best["frac_hbm"], "traffic": ncu_traffic("gemv_gate_up_m16")[0],

@@ -94,6 +94,9 @@ _SIGS = {
                                                       _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i64,
                                                       _i64, _vp, _sz, _vp]),
     "bfp8_grouped_linear_silu_quant_workspace": (_sz, [_i64, _i32, _i64, _i64]),
+    "bfp8_decode_ffn": (ctypes.c_int, [_i32, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64,
+                                       _vp, _i64, _vp, _sz, _vp]),
+    "bfp8_decode_ffn_workspace": (_sz, [_i64, _i64, _i64, _i32]),
     "bfp8_moe_gather_act_quant": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp,
                                                  _i64, _i64, _vp]),
     "bfp8_moe_combine": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _i32, _vp, _i64,
@@ -351,6 +354,25 @@ def bfp8_grouped_linear_silu_quant(q_a, s_a, w, w_scale, offsets, q_h, s_h, s_st
                                                q_h.stride(0), _ptr(s_h), hsm, hskb, wsp, wsb,
                                                _stream(stream)),
            "bfp8_grouped_linear_silu_quant")
+
+
+BFP8_DECODE_W8A16, BFP8_DECODE_W8A8 = 0, 1
+
+
+def bfp8_decode_ffn_workspace(M: int, H: int, I: int, arith: int = BFP8_DECODE_W8A16) -> int:
+    return int(_lib.bfp8_decode_ffn_workspace(M, H, I, arith))
+
+
+def bfp8_decode_ffn(x, w_gate_up, s_gate_up, w_down, s_down, y, workspace,
+                    arith: int = BFP8_DECODE_W8A16, stream=None) -> None:
+    """One dense-FFN decode step: gate/up GEMV -> SiLU*up -> down GEMV."""
+    M, H = x.shape
+    I = w_down.shape[1]
+    _check(_lib.bfp8_decode_ffn(arith, _ptr(x), x.stride(0), _ptr(w_gate_up), _ptr(s_gate_up),
+                                _ptr(w_down), _ptr(s_down), _scale_dtype(s_gate_up), M, H, I,
+                                _ptr(y), y.stride(0), *_ws(workspace),
+                                _stream(stream)),
+           "bfp8_decode_ffn")
 
 
 def bfp8_moe_gather_act_quant(x, row_token, q, scales, s_stride_m=None, s_stride_kb=None,

@@ -280,6 +280,20 @@ int bfp8_silu_mul_act_quant(const void* gu_bf16, int64_t M, int64_t I, int64_t l
                                    s_stride_kb, stream);
 }
 
+size_t bfp8_decode_ffn_workspace(int64_t M, int64_t H, int64_t I, int32_t arith) {
+  int sms = 0;
+  if (sm_count(&sms) != BFP8_OK) return 0;
+  return decode_ffn_workspace_bytes(M, H, I, arith, sms);
+}
+
+int bfp8_decode_ffn(int32_t arith, const void* x_bf16, int64_t ldx, const void* w_gate_up,
+                    const void* s_gate_up, const void* w_down, const void* s_down,
+                    int32_t w_scale_dtype, int64_t M, int64_t H, int64_t I, void* y_bf16,
+                    int64_t ldy, void* workspace, size_t ws_bytes, void* stream) {
+  return launch_decode_ffn(arith, x_bf16, ldx, w_gate_up, s_gate_up, w_down, s_down,
+                           w_scale_dtype, M, H, I, y_bf16, ldy, workspace, ws_bytes, stream);
+}
+
 int bfp8_moe_gather_act_quant(const void* x_bf16, int64_t T, int64_t H, int64_t ldx,
                               const int32_t* row_token, int64_t R, void* q_e4m3, int64_t ldq,
                               float* scales, int64_t s_stride_m, int64_t s_stride_kb,

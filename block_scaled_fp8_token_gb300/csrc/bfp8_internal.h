@@ -81,11 +81,19 @@ int launch_grouped_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K, int sms);
 int launch_gemv(const void* x, int64_t ldx, const void* w, const void* w_scale,
                 int32_t w_scale_dtype, int64_t M, int64_t N, int64_t K, void* y, int64_t ldy,
-                const MemberTable& mt, void* workspace, size_t ws_bytes, void* stream);
+                const MemberTable& mt, void* workspace, size_t ws_bytes, void* stream,
+                bool silu = false);
 int launch_gemv_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
                      const void* w, const void* w_scale, int32_t w_scale_dtype, int64_t M,
                      int64_t N, int64_t K, void* y, int64_t ldy, const MemberTable& mt,
                      void* workspace, size_t ws_bytes, void* stream);
+
+// The dense-FFN decode step (gate/up GEMV -> SiLU*up -> down GEMV).
+size_t decode_ffn_workspace_bytes(int64_t M, int64_t H, int64_t I, int32_t arith, int sms);
+int launch_decode_ffn(int32_t arith, const void* x, int64_t ldx, const void* w_gu,
+                      const void* s_gu, const void* w_dn, const void* s_dn, int32_t w_scale_dtype,
+                      int64_t M, int64_t H, int64_t I, void* y, int64_t ldy, void* workspace,
+                      size_t ws_bytes, void* stream);
 
 // Device error words, one per translation unit with bounded waits: read and
 // clear. Return BFP8_OK, BFP8_ERR_TIMEOUT or BFP8_ERR_CUDA.

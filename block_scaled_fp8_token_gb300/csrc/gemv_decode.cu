@@ -43,6 +43,7 @@
 
 #include "bfp8_internal.h"
 #include "ptx.cuh"
+#include "act_math.cuh"
 
 namespace bfp8 {
 
@@ -149,6 +150,30 @@ BFP8_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // and 2^-e per token. Tokens past M get zero rows.
 // It also clears the GEMV's split-tile counters; the GEMV touches them only
 // after its griddepcontrol.wait.
+// SILU == true: x is a gate/up output [M, 2K] (gate columns 0..K-1, up columns
+// K..2K-1) and the tokens are h = bf16(silu(gate) * up), formed with the same
+// arithmetic as the SiLU*up quantizer.
+BFP8_DEV void load_token_words(const __nv_bfloat16* row, bool in_range, int c0, int K,
+                               uint32_t (&xw)[16]) {
+  if (in_range && c0 + 32 <= K) {
+    const uint4* src = reinterpret_cast<const uint4*>(row + c0);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 v = src[c];
+      xw[4 * c] = v.x; xw[4 * c + 1] = v.y; xw[4 * c + 2] = v.z; xw[4 * c + 3] = v.w;
+    }
+  } else {
+    const uint16_t* xr = reinterpret_cast<const uint16_t*>(row);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t lo = (in_range && c0 + 2 * j < K) ? xr[c0 + 2 * j] : 0u;
+      const uint32_t hi = (in_range && c0 + 2 * j + 1 < K) ? xr[c0 + 2 * j + 1] : 0u;
+      xw[j] = lo | (hi << 16);
+    }
+  }
+}
+
+template <bool SILU>
 __global__ void __launch_bounds__(64) gemv_split_tokens_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t ldx, int32_t M, int32_t K,
     uint8_t* __restrict__ xtile, float* __restrict__ xinv, int32_t* __restrict__ counters,
@@ -158,21 +183,18 @@ __global__ void __launch_bounds__(64) gemv_split_tokens_kernel(
   for (int i = kb * 64 + threadIdx.x; i < n_counters; i += gridDim.x * 64) counters[i] = 0;
   const int tok = threadIdx.x >> 2, q4 = threadIdx.x & 3;
   const int c0 = kb * 128 + 32 * q4;
+  const __nv_bfloat16* row = x + static_cast<int64_t>(tok < M ? tok : 0) * ldx;
   uint32_t xw[16];
-  if (tok < M && c0 + 32 <= K) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(tok) * ldx + c0);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint4 v = src[c];
-      xw[4 * c] = v.x; xw[4 * c + 1] = v.y; xw[4 * c + 2] = v.z; xw[4 * c + 3] = v.w;
-    }
-  } else {
-    const uint16_t* xr = reinterpret_cast<const uint16_t*>(x) + static_cast<int64_t>(tok) * ldx;
+  load_token_words(row, tok < M, c0, K, xw);
+  if constexpr (SILU) {
+    uint32_t uw[16];
+    load_token_words(row + K, tok < M, c0, K, uw);
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const uint32_t lo = (tok < M && c0 + 2 * j < K) ? xr[c0 + 2 * j] : 0u;
-      const uint32_t hi = (tok < M && c0 + 2 * j + 1 < K) ? xr[c0 + 2 * j + 1] : 0u;
-      xw[j] = lo | (hi << 16);
+      const float h0 = silu_mul_bf16_round(__uint_as_float(xw[j] << 16), __uint_as_float(uw[j] << 16));
+      const float h1 = silu_mul_bf16_round(__uint_as_float(xw[j] & 0xFFFF0000u),
+                                           __uint_as_float(uw[j] & 0xFFFF0000u));
+      xw[j] = (__float_as_uint(h0) >> 16) | (__float_as_uint(h1) & 0xFFFF0000u);
     }
   }
   // the row's max |x| (non-negative BF16 patterns order like their values)
@@ -555,10 +577,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // The split kernel, then the GEMV as its programmatic dependent.
 int launch_kernels(const void* x, int64_t ldx, uint8_t* xtile, float* xinv, const CUtensorMap& tw,
-                   const CUtensorMap& tx, const GemvParams& p, void* stream) {
+                   const CUtensorMap& tx, const GemvParams& p, void* stream, bool silu = false) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  gemv_split_tokens_kernel<<<p.Kb, 64, 0, st>>>(static_cast<const __nv_bfloat16*>(x), ldx, p.M,
-                                                p.K, xtile, xinv, p.counters, p.RT);
+  if (silu)
+    gemv_split_tokens_kernel<true><<<p.Kb, 64, 0, st>>>(static_cast<const __nv_bfloat16*>(x), ldx,
+                                                        p.M, p.K, xtile, xinv, p.counters, p.RT);
+  else
+    gemv_split_tokens_kernel<false><<<p.Kb, 64, 0, st>>>(static_cast<const __nv_bfloat16*>(x), ldx,
+                                                         p.M, p.K, xtile, xinv, p.counters, p.RT);
   int rc = check_launch();
   if (rc != BFP8_OK) return rc;
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel<false>), kSmemBytes);
@@ -647,8 +673,9 @@ int init_params(GemvParams& p, const void* w, const void* w_scale, int32_t w_sca
 
 int launch_gemv(const void* x, int64_t ldx, const void* w, const void* w_scale,
                 int32_t w_scale_dtype, int64_t M, int64_t N, int64_t K, void* y, int64_t ldy,
-                const MemberTable& mt, void* workspace, size_t ws_bytes, void* stream) {
+                const MemberTable& mt, void* workspace, size_t ws_bytes, void* stream, bool silu) {
   if (ldx % 8 != 0 || reinterpret_cast<uintptr_t>(x) % 16 != 0) return BFP8_ERR_UNSUPPORTED;
+  if (silu && K % 8 != 0) return BFP8_ERR_UNSUPPORTED;
   GemvParams p{};
   int sms = 0;
   int rc = init_params(p, w, w_scale, w_scale_dtype, M, N, K, y, ldy, mt, workspace, ws_bytes, &sms);
@@ -662,7 +689,7 @@ int launch_gemv(const void* x, int64_t ldx, const void* w, const void* w_scale,
   rc = make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xtile, 128, static_cast<uint64_t>(p.Kb) * 32,
                     128, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != BFP8_OK) return rc;
-  return launch_kernels(x, ldx, xtile, const_cast<float*>(p.xinv), tw, tx, p, stream);
+  return launch_kernels(x, ldx, xtile, const_cast<float*>(p.xinv), tw, tx, p, stream, silu);
 }
 
 int launch_gemv_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
@@ -704,6 +731,103 @@ int launch_gemv_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t s
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, gemv_kernel<true>, tw, tx, p) != cudaSuccess) return BFP8_ERR_CUDA;
   return check_launch();
+}
+
+// ---------------------------------------------------------------------------
+// The dense-FFN decode step: gate/up GEMV (members {I, I}) -> h = bf16(silu(g)*u)
+// -> down GEMV, every launch on one stream with no host synchronisation, so the
+// step can be captured in a CUDA graph.
+//   W8A16: split(x) -> GEMV(gate/up) -> split(SiLU*up of gu) -> GEMV(down), the
+//          SiLU*up formed inside the down GEMV's token split.
+//   W8A8:  1x128 quant(x) -> GEMV(gate/up) -> SiLU*up + 1x128 quant -> GEMV(down).
+// Workspace: the intermediates, then one GEMV scratch region that the two GEMVs
+// use in turn (the second GEMV's first kernel starts only after the first GEMV
+// has finished, and each GEMV touches its counters and partials only after its
+// programmatic-dependency wait).
+namespace {
+
+struct DecodeFfnLayout {
+  size_t qx, sx, gu, qh, sh, scratch, total;
+};
+
+DecodeFfnLayout decode_ffn_layout(int64_t M, int64_t H, int64_t I, int32_t arith, int sms) {
+  const int64_t Hb = (H + 127) / 128, Ib = (I + 127) / 128;
+  const bool w8a8 = arith == BFP8_DECODE_W8A8;
+  DecodeFfnLayout l{};
+  size_t off = 0;
+  l.qx = off;
+  off += w8a8 ? align256(static_cast<size_t>(M * H)) : 0;
+  l.sx = off;
+  off += w8a8 ? align256(static_cast<size_t>(M * Hb) * sizeof(float)) : 0;
+  l.gu = off;
+  off += align256(static_cast<size_t>(M * 2 * I) * 2);
+  l.qh = off;
+  off += w8a8 ? align256(static_cast<size_t>(M * I)) : 0;
+  l.sh = off;
+  off += w8a8 ? align256(static_cast<size_t>(M * Ib) * sizeof(float)) : 0;
+  l.scratch = off;
+  const size_t g1 = ws_layout(2 * I, H, sms).total, g2 = ws_layout(H, I, sms).total;
+  l.total = off + (g1 > g2 ? g1 : g2);
+  return l;
+}
+
+}  // namespace
+
+size_t decode_ffn_workspace_bytes(int64_t M, int64_t H, int64_t I, int32_t arith, int sms) {
+  if (M < 1 || M > 16 || H <= 0 || I <= 0 || sms <= 0) return 0;
+  if (arith != BFP8_DECODE_W8A16 && arith != BFP8_DECODE_W8A8) return 0;
+  return decode_ffn_layout(M, H, I, arith, sms).total;
+}
+
+int launch_decode_ffn(int32_t arith, const void* x, int64_t ldx, const void* w_gu,
+                      const void* s_gu, const void* w_dn, const void* s_dn, int32_t w_scale_dtype,
+                      int64_t M, int64_t H, int64_t I, void* y, int64_t ldy, void* workspace,
+                      size_t ws_bytes, void* stream) {
+  if (arith != BFP8_DECODE_W8A16 && arith != BFP8_DECODE_W8A8) return BFP8_ERR_INVALID_ARG;
+  if (!x || !w_gu || !s_gu || !w_dn || !s_dn || !y || !workspace) return BFP8_ERR_INVALID_ARG;
+  if (M < 1 || M > 16 || H <= 0 || I <= 0 || ldx < H || ldy < H) return BFP8_ERR_INVALID_ARG;
+  if (w_scale_dtype != BFP8_DT_BF16 && w_scale_dtype != BFP8_DT_F32) return BFP8_ERR_SCALE_DTYPE;
+  if (H % 16 != 0 || I % 16 != 0) return BFP8_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return BFP8_ERR_INVALID_ARG;
+  int sms = 0;
+  int rc = sm_count(&sms);
+  if (rc != BFP8_OK) return rc;
+  const DecodeFfnLayout l = decode_ffn_layout(M, H, I, arith, sms);
+  if (ws_bytes < l.total) return BFP8_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* gu = ws + l.gu;
+  void* scratch = ws + l.scratch;
+  const size_t scratch_bytes = ws_bytes - l.scratch;
+  const int64_t Hb = (H + 127) / 128, Ib = (I + 127) / 128;
+  MemberTable gu_mt, dn_mt;
+  const int64_t gu_rows[2] = {I, I};
+  bfp8_members gm;
+  gm.n_members = 2;
+  gm.member_rows = gu_rows;
+  rc = resolve_members(2 * I, &gm, &gu_mt);
+  if (rc != BFP8_OK) return rc;
+  rc = resolve_members(H, nullptr, &dn_mt);
+  if (rc != BFP8_OK) return rc;
+  if (arith == BFP8_DECODE_W8A16) {
+    rc = launch_gemv(x, ldx, w_gu, s_gu, w_scale_dtype, M, 2 * I, H, gu, 2 * I, gu_mt, scratch,
+                     scratch_bytes, stream);
+    if (rc != BFP8_OK) return rc;
+    return launch_gemv(gu, 2 * I, w_dn, s_dn, w_scale_dtype, M, H, I, y, ldy, dn_mt, scratch,
+                       scratch_bytes, stream, /*silu=*/true);
+  }
+  uint8_t* qx = ws + l.qx;
+  float* sx = reinterpret_cast<float*>(ws + l.sx);
+  uint8_t* qh = ws + l.qh;
+  float* sh = reinterpret_cast<float*>(ws + l.sh);
+  rc = launch_act_quant(x, M, H, ldx, qx, H, sx, Hb, 1, stream);
+  if (rc != BFP8_OK) return rc;
+  rc = launch_gemv_w8a8(qx, sx, Hb, 1, w_gu, s_gu, w_scale_dtype, M, 2 * I, H, gu, 2 * I, gu_mt,
+                        scratch, scratch_bytes, stream);
+  if (rc != BFP8_OK) return rc;
+  rc = launch_silu_mul_act_quant(gu, M, I, 2 * I, qh, I, sh, Ib, 1, stream);
+  if (rc != BFP8_OK) return rc;
+  return launch_gemv_w8a8(qh, sh, Ib, 1, w_dn, s_dn, w_scale_dtype, M, H, I, y, ldy, dn_mt,
+                          scratch, scratch_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------

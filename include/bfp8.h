@@ -279,6 +279,45 @@ int bfp8_gemv_decode_w8a8(const void* q_a, const float* s_a, int64_t s_stride_m,
                           int64_t ldy, const bfp8_members* members, void* workspace,
                           size_t ws_bytes, void* stream);
 
+/* ---- the dense-FFN decode step (graph-capturable) ------------------------ */
+/* Arithmetic of a decode step: the W8A16 GEMV of bfp8_gemv_decode, or the
+ * W8A8 GEMV of bfp8_gemv_decode_w8a8 behind 1x128 activation quantization. */
+enum bfp8_decode_arith { BFP8_DECODE_W8A16 = 0, BFP8_DECODE_W8A8 = 1 };
+
+/*
+ * bfp8_decode_ffn -- one dense-FFN decode step for M <= 16 tokens, as a
+ * chain of GEMVs on one stream:
+ *   gu = GEMV(x, W_gate_up) with members {I, I}        (BF16 [M, 2I])
+ *   h  = bf16_rn( silu(gu[:, :I]) * gu[:, I:] )        (as bfp8_silu_mul_act_quant)
+ *   y  = GEMV(h, W_down)                               (BF16 [M, H])
+ *   [Module w8a8_prefill, "Reachability": decode on GB10 runs one unfused
+ *    GEMV per projection; first paragraph: the gate/up/down arm]
+ * arith = BFP8_DECODE_W8A16: both GEMVs are bfp8_gemv_decode's arithmetic on
+ *   x and h (4 launches: each GEMV behind its token split; the SiLU*up is
+ *   formed inside the down GEMV's token split).
+ * arith = BFP8_DECODE_W8A8: x is quantized as bfp8_act_quant_group, the
+ *   gate/up GEMV is bfp8_gemv_decode_w8a8, h is quantized as
+ *   bfp8_silu_mul_act_quant, and the down GEMV is bfp8_gemv_decode_w8a8.
+ * The result equals that sequence of entry points byte for byte.
+ *   x_bf16     [M, H] BF16, row stride ldx (ldx % 8 == 0, 16-byte aligned)
+ *   w_gate_up  [2I, H] E4M3, gate rows over up rows; s_gate_up its
+ *              member-local grid [2*ceil(I/128), ceil(H/128)]
+ *   w_down     [H, I] E4M3; s_down its grid [ceil(H/128), ceil(I/128)]
+ *   w_scale_dtype  BFP8_DT_BF16 or BFP8_DT_F32, for both grids
+ *   y_bf16     [M, H] BF16, row stride ldy
+ *   workspace  at least bfp8_decode_ffn_workspace(M, H, I, arith) bytes,
+ *              256-byte aligned, caller-owned; holds the intermediates and
+ *              the GEMVs' split-K scratch. Calls sharing it must not overlap.
+ * Requirements: 1 <= M <= 16; H % 16 == 0 and I % 16 == 0.
+ * Every launch goes to `stream` and nothing synchronises with the host, so a
+ * step can be captured once in a CUDA graph and replayed.
+ */
+size_t bfp8_decode_ffn_workspace(int64_t M, int64_t H, int64_t I, int32_t arith);
+int bfp8_decode_ffn(int32_t arith, const void* x_bf16, int64_t ldx, const void* w_gate_up,
+                    const void* s_gate_up, const void* w_down, const void* s_down,
+                    int32_t w_scale_dtype, int64_t M, int64_t H, int64_t I, void* y_bf16,
+                    int64_t ldy, void* workspace, size_t ws_bytes, void* stream);
+
 /* ---- decode GEMV for callers that cannot allocate ------------------------- */
 /*
  * The pages have no counterpart for this entry point. It exists for callers

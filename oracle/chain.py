@@ -1,5 +1,5 @@
 """The dense-FFN glue as one step (gate/up projection, SiLU(gate)*up, 1x128
-quantization of h), double precision.
+quantization of h), and the whole dense-FFN decode step, double precision.
 
 Test infrastructure (CPU oracle); see the package docstring for who may use it.
 
@@ -19,8 +19,8 @@ from __future__ import annotations
 import numpy as np
 
 from .formats import f64_to_bf16_bits
-from .linear import linear_w8a8
-from .quant import silu_mul_act_quant
+from .linear import linear_w8a8, linear_w8a16
+from .quant import act_quant_group, silu_mul_act_quant, silu_mul_bf16
 
 
 def gate_up_silu_quant(q_a, s_a, q_w, s_w, rows=None):
@@ -47,3 +47,25 @@ def grouped_gate_up_silu_quant(q_a, s_a, q_w, s_w, offsets, rows=None):
         if sel.size:
             gu[sel] = linear_w8a8(q_a, s_a, q_w[e], s_w[e], [I, I], rows=ri[sel])
     return silu_mul_act_quant(f64_to_bf16_bits(gu))
+
+
+def decode_ffn(x_bits, q_gu, s_gu, q_d, s_d, arith="w8a16"):
+    """The dense-FFN decode step [Module w8a8_prefill, "Reachability": one
+    GEMV per projection at decode; first paragraph: the gate/up/down arm],
+    as the composition of its projections in their order:
+      w8a16: gu = bf16(W8A16 gate/up of x); h = bf16(silu(g)*u);
+             y  = W8A16 down of h
+      w8a8:  x quantized 1x128; gu = bf16(W8A8 gate/up); h = bf16(silu(g)*u)
+             quantized 1x128; y = W8A8 down
+    x_bits uint16 [M, H]; q_gu [2I, H] (gate rows over up rows) with its
+    member-local grid; q_d [H, I]. Returns float64 [M, H], y before its BF16
+    rounding."""
+    I = q_gu.shape[0] // 2
+    if arith == "w8a16":
+        gu = linear_w8a16(x_bits, q_gu, s_gu, [I, I])
+        return linear_w8a16(silu_mul_bf16(f64_to_bf16_bits(gu)), q_d, s_d)
+    if arith != "w8a8":
+        raise ValueError(arith)
+    q_a, s_a = act_quant_group(x_bits)
+    q_h, s_h = gate_up_silu_quant(q_a, s_a, q_gu, s_gu)
+    return linear_w8a8(q_h, s_h, q_d, s_d)

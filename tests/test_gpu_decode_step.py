@@ -1,0 +1,129 @@
+"""GPU parity: the dense-FFN decode step (bfp8_decode_ffn) at the dense-FFN
+decode shapes (hidden 5120, intermediate 17408; gate/up [34816, 5120], down
+[5120, 17408]) for M = 1, 4 and 16 tokens, in both arithmetics.
+
+* W8A8: the step must equal, byte for byte, the sequence of parity-tested
+  entry points it chains (act quant -> W8A8 GEMV -> SiLU*up quant -> W8A8
+  GEMV). End to end, a rare h code that rounds the other way is a
+  quantization-level difference, so each token meets the W8A8 accuracy gate
+  against the oracle's step (cosine >= 0.999, relative RMS <= 2%).
+* W8A16: stage by stage on bytes both sides share. The gate/up GEMV (the
+  public bfp8_gemv_decode, the same kernel the step runs) meets the GEMM
+  acceptance bound against the oracle; the step's y meets it against the
+  oracle's down projection of h formed from the GPU's own gate/up bytes.
+  End to end, BF16 gate/up values that round the other way (the GEMV carries
+  token entries far below their block's maximum to within 2^-17 of it) move
+  single h values by one BF16 ulp, a quantization-level difference, so each
+  token meets the same accuracy gate as W8A8.
+* Both: a CUDA graph captured around one step and replayed on new tokens
+  gives the same bytes as an eager step on those tokens, and M = 1 (smallest)
+  and M = 16 (the limit) both run.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_fp8_token_gb300 import synth
+from gpu_util import (assert_close, bits16, cos_rrms, dense_ffn_weights, gpu_bf16_to_f64,
+                      scale_to_dev, to_dev_bf16, to_dev_u8)
+from oracle import chain as CH
+from oracle import linear as L
+from oracle import quant as Q
+
+pytestmark = pytest.mark.gpu
+
+H, I = 5120, 17408
+
+
+@pytest.fixture(scope="module")
+def weights(cuda_device):
+    qgu, sgu, qd, sd, _ = dense_ffn_weights(0)
+    dev = cuda_device
+    host = (qgu, sgu, qd, sd)
+    return host, (to_dev_u8(qgu, dev), scale_to_dev(sgu, dev), to_dev_u8(qd, dev),
+                  scale_to_dev(sd, dev))
+
+
+def _step(bfp8, dev, x, w, arith):
+    M = x.shape[0]
+    y = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(bfp8.bfp8_decode_ffn_workspace(M, H, I, arith), dtype=torch.uint8, device=dev)
+    bfp8.bfp8_decode_ffn(x, *w, y, ws, arith=arith)
+    torch.cuda.synchronize()
+    assert bfp8.bfp8_device_status() == 0
+    return y
+
+
+def _chain_of_entry_points(bfp8, dev, x, w):
+    wgu, sgu, wd, sd = w
+    M = x.shape[0]
+    qa = torch.empty(M, H, dtype=torch.uint8, device=dev)
+    sa = torch.empty(M, H // 128, dtype=torch.float32, device=dev)
+    gu = torch.empty(M, 2 * I, dtype=torch.bfloat16, device=dev)
+    qh = torch.empty(M, I, dtype=torch.uint8, device=dev)
+    sh = torch.empty(M, I // 128, dtype=torch.float32, device=dev)
+    y = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(bfp8.bfp8_gemv_decode_workspace(M, 2 * I, H),
+                         bfp8.bfp8_gemv_decode_workspace(M, H, I)), dtype=torch.uint8, device=dev)
+    bfp8.bfp8_act_quant_group(x, qa, sa)
+    bfp8.bfp8_gemv_decode_w8a8(qa, sa, wgu, sgu, gu, ws, member_rows=[I, I])
+    bfp8.bfp8_silu_mul_act_quant(gu, qh, sh)
+    bfp8.bfp8_gemv_decode_w8a8(qh, sh, wd, sd, y, ws)
+    torch.cuda.synchronize()
+    return y
+
+
+@pytest.mark.parametrize("M", [1, 4, 16])
+@pytest.mark.parametrize("arith", ["w8a16", "w8a8"])
+def test_decode_step(bfp8, cuda_device, weights, arith, M):
+    dev = cuda_device
+    host, w = weights
+    code = bfp8.BFP8_DECODE_W8A8 if arith == "w8a8" else bfp8.BFP8_DECODE_W8A16
+    xb = bits16(synth.decode_tokens(300 + M, M, H))
+    x = to_dev_bf16(xb, dev)
+    y = _step(bfp8, dev, x, w, code)
+    ref = CH.decode_ffn(xb, *host, arith=arith)
+    got = gpu_bf16_to_f64(y)
+    if arith == "w8a16":
+        qgu, sgu, qd, sd = host
+        gu = torch.empty(M, 2 * I, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(bfp8.bfp8_gemv_decode_workspace(M, 2 * I, H), dtype=torch.uint8,
+                         device=dev)
+        bfp8.bfp8_gemv_decode(x, w[0], w[1], gu, ws, member_rows=[I, I])
+        torch.cuda.synchronize()
+        assert_close(gpu_bf16_to_f64(gu), L.linear_w8a16(xb, qgu, sgu, [I, I]),
+                     f"decode step gate/up M={M}")
+        h_of_gpu_gu = Q.silu_mul_bf16(bits16(gu))
+        assert_close(got, L.linear_w8a16(h_of_gpu_gu, qd, sd), f"decode step down M={M}")
+    else:
+        assert torch.equal(y.view(torch.int16), _chain_of_entry_points(bfp8, dev, x, w).view(torch.int16))
+    for m in range(M):
+        cos, rrms = cos_rrms(got[m], ref[m])
+        assert cos >= 0.999 and rrms <= 0.02, (m, cos, rrms)
+
+
+@pytest.mark.parametrize("arith", ["w8a16", "w8a8"])
+def test_decode_step_in_a_cuda_graph(bfp8, cuda_device, weights, arith):
+    dev = cuda_device
+    _, w = weights
+    code = bfp8.BFP8_DECODE_W8A8 if arith == "w8a8" else bfp8.BFP8_DECODE_W8A16
+    M = 16
+    x = to_dev_bf16(bits16(synth.decode_tokens(401, M, H)), dev)
+    y = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(bfp8.bfp8_decode_ffn_workspace(M, H, I, code), dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        bfp8.bfp8_decode_ffn(x, *w, y, ws, arith=code)     # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        bfp8.bfp8_decode_ffn(x, *w, y, ws, arith=code)
+    for seed in (402, 403):
+        x.copy_(to_dev_bf16(bits16(synth.decode_tokens(seed, M, H)), dev))
+        g.replay()
+        torch.cuda.synchronize()
+        eager = _step(bfp8, dev, x.clone(), w, code)
+        assert torch.equal(y.view(torch.int16), eager.view(torch.int16)), seed
