@@ -56,6 +56,7 @@ class bfp8_weight_desc(ctypes.Structure):
         ("declared_block", ctypes.c_int32 * 2),
         ("n_members", ctypes.c_int32),
         ("member_rows", ctypes.POINTER(ctypes.c_int64)),
+        ("tensor_scale_dtype", ctypes.c_int32),
     ]
 
 
@@ -138,14 +139,16 @@ def _stream(stream) -> int:
     return stream.cuda_stream
 
 
+BFP8_SCALE_PER_TENSOR = 0x100
+
+
 def _scale_dtype(t: torch.Tensor) -> int:
-    if t.dtype == torch.bfloat16:
-        return BFP8_DT_BF16
-    if t.dtype == torch.float32:
-        return BFP8_DT_F32
-    if t.dtype == torch.float16:
-        return BFP8_DT_F16
-    return BFP8_DT_NONE
+    """The dtype code of a scale tensor. A block grid has rank 2 (rank 3 for
+    experts); a scale of rank 0 or 1 (one multiplier, or one per expert) is a
+    per-tensor scale and carries BFP8_SCALE_PER_TENSOR."""
+    code = {torch.bfloat16: BFP8_DT_BF16, torch.float32: BFP8_DT_F32,
+            torch.float16: BFP8_DT_F16}.get(t.dtype, BFP8_DT_NONE)
+    return code | BFP8_SCALE_PER_TENSOR if code and t.dim() <= 1 else code
 
 
 def _members(member_rows):
@@ -166,7 +169,7 @@ def bfp8_validate_grid(desc: bfp8_weight_desc, msg_len: int = 256) -> tuple[int,
 def make_weight_desc(weight_dtype: int, weight_shape, scale_dtype: int = BFP8_DT_NONE,
                      scale_shape=None, has_row_scale: bool = False,
                      declared_quant_fp8: bool = True, declared_block=(128, 128),
-                     member_rows=None):
+                     member_rows=None, tensor_scale_dtype: int = BFP8_DT_NONE):
     """Builds a bfp8_weight_desc; returns (desc, keepalive)."""
     d = bfp8_weight_desc()
     d.weight_dtype = weight_dtype
@@ -181,6 +184,7 @@ def make_weight_desc(weight_dtype: int, weight_shape, scale_dtype: int = BFP8_DT
     d.has_row_scale = int(bool(has_row_scale))
     d.declared_quant_fp8 = int(bool(declared_quant_fp8))
     d.declared_block[0], d.declared_block[1] = int(declared_block[0]), int(declared_block[1])
+    d.tensor_scale_dtype = tensor_scale_dtype
     keep = None
     if member_rows is not None:
         keep = (ctypes.c_int64 * len(member_rows))(*[int(v) for v in member_rows])

@@ -188,12 +188,49 @@ int bfp8_validate_grid(const bfp8_weight_desc* d, char* msg, size_t msg_len) {
     write_msg(msg, msg_len, "checkpoint does not declare quant_method fp8");
     return BFP8_ERR_QUANT_METHOD;
   }
+  const bool has_block = d->scale_dtype != BFP8_DT_NONE;
+  if (d->tensor_scale_dtype != BFP8_DT_NONE) {
+    // per-tensor scaled: one multiplier, read as a grid with a single block
+    if (has_block || d->has_row_scale) {
+      write_msg(msg, msg_len, "a one-element weight_scale next to another scale leaf");
+      return BFP8_ERR_AMBIGUOUS_SCALE;
+    }
+    if (d->declared_block[0] != 0 || d->declared_block[1] != 0) {
+      write_msg(msg, msg_len, "per-tensor scaled weight but weight_block_size [%d,%d] declared",
+                d->declared_block[0], d->declared_block[1]);
+      return BFP8_ERR_BLOCK_SIZE;
+    }
+    if (d->tensor_scale_dtype != BFP8_DT_BF16 && d->tensor_scale_dtype != BFP8_DT_F32) {
+      write_msg(msg, msg_len, "per-tensor weight_scale must be BF16 or F32");
+      return BFP8_ERR_SCALE_DTYPE;
+    }
+    if (d->n_members > 0) {
+      if (!d->member_rows || d->n_members > BFP8_MAX_MEMBERS) {
+        write_msg(msg, msg_len, "member table missing or longer than %d", BFP8_MAX_MEMBERS);
+        return BFP8_ERR_GROUP;
+      }
+      int64_t sum = 0;
+      for (int i = 0; i < d->n_members; ++i) {
+        if (d->member_rows[i] <= 0) {
+          write_msg(msg, msg_len, "member %d has %lld rows", i, (long long)d->member_rows[i]);
+          return BFP8_ERR_GROUP;
+        }
+        sum += d->member_rows[i];
+      }
+      if (sum != N) {
+        write_msg(msg, msg_len, "member rows sum to %lld, weight has %lld", (long long)sum,
+                  (long long)N);
+        return BFP8_ERR_GROUP;
+      }
+    }
+    write_msg(msg, msg_len, "OK: per-tensor scaled, one multiplier covers the tensor");
+    return BFP8_OK;
+  }
   if (d->declared_block[0] != 128 || d->declared_block[1] != 128) {
     write_msg(msg, msg_len, "declared weight_block_size [%d,%d] is not [128,128]",
               d->declared_block[0], d->declared_block[1]);
     return BFP8_ERR_BLOCK_SIZE;
   }
-  const bool has_block = d->scale_dtype != BFP8_DT_NONE;
   if (d->has_row_scale) {
     if (has_block) {
       write_msg(msg, msg_len, "both a per-row weight_scale and a weight_scale_inv grid");
@@ -331,7 +368,7 @@ int bfp8_linear_w8a8(const void* q_a, const float* s_a, int64_t s_stride_m, int6
   if (M < 0 || N <= 0 || K <= 0) return BFP8_ERR_INVALID_ARG;
   if (M == 0) return BFP8_OK;
   if (!q_a || !s_a || !w_e4m3 || !w_scale || !y_bf16 || ldy < N) return BFP8_ERR_INVALID_ARG;
-  if (w_scale_dtype != BFP8_DT_BF16 && w_scale_dtype != BFP8_DT_F32) return BFP8_ERR_SCALE_DTYPE;
+  if (!weight_scale_dtype_ok(w_scale_dtype)) return BFP8_ERR_SCALE_DTYPE;
   MemberTable mt;
   int rc = resolve_members(N, members, &mt);
   if (rc != BFP8_OK) return rc;
@@ -346,7 +383,7 @@ int bfp8_linear_w8a16(const void* x_bf16, int64_t ldx, const void* w_e4m3, const
   if (M == 0) return BFP8_OK;
   if (!x_bf16 || !w_e4m3 || !w_scale || !y_bf16 || ldy < N || ldx < K)
     return BFP8_ERR_INVALID_ARG;
-  if (w_scale_dtype != BFP8_DT_BF16 && w_scale_dtype != BFP8_DT_F32) return BFP8_ERR_SCALE_DTYPE;
+  if (!weight_scale_dtype_ok(w_scale_dtype)) return BFP8_ERR_SCALE_DTYPE;
   MemberTable mt;
   int rc = resolve_members(N, members, &mt);
   if (rc != BFP8_OK) return rc;
@@ -367,7 +404,7 @@ int bfp8_gemv_decode(const void* x_bf16, int64_t ldx, const void* w_e4m3, const 
   if (M < 1 || M > 16 || N <= 0 || K <= 0) return BFP8_ERR_INVALID_ARG;
   if (!x_bf16 || !w_e4m3 || !w_scale || !y_bf16 || ldy < N || ldx < K)
     return BFP8_ERR_INVALID_ARG;
-  if (w_scale_dtype != BFP8_DT_BF16 && w_scale_dtype != BFP8_DT_F32) return BFP8_ERR_SCALE_DTYPE;
+  if (!weight_scale_dtype_ok(w_scale_dtype)) return BFP8_ERR_SCALE_DTYPE;
   MemberTable mt;
   int rc = resolve_members(N, members, &mt);
   if (rc != BFP8_OK) return rc;
@@ -382,7 +419,7 @@ int bfp8_gemv_decode_w8a8(const void* q_a, const float* s_a, int64_t s_stride_m,
                           size_t ws_bytes, void* stream) {
   if (M < 1 || M > 16 || N <= 0 || K <= 0) return BFP8_ERR_INVALID_ARG;
   if (!q_a || !s_a || !w_e4m3 || !w_scale || !y_bf16 || ldy < N) return BFP8_ERR_INVALID_ARG;
-  if (w_scale_dtype != BFP8_DT_BF16 && w_scale_dtype != BFP8_DT_F32) return BFP8_ERR_SCALE_DTYPE;
+  if (!weight_scale_dtype_ok(w_scale_dtype)) return BFP8_ERR_SCALE_DTYPE;
   MemberTable mt;
   int rc = resolve_members(N, members, &mt);
   if (rc != BFP8_OK) return rc;
@@ -406,7 +443,7 @@ int bfp8_grouped_linear(const void* q_a, const float* s_a, int64_t s_stride_m,
   if (total_M == 0) return BFP8_OK;
   if (!q_a || !s_a || !w_e4m3 || !w_scale || !offsets_dev || !y_bf16 || ldy < N)
     return BFP8_ERR_INVALID_ARG;
-  if (w_scale_dtype != BFP8_DT_BF16 && w_scale_dtype != BFP8_DT_F32) return BFP8_ERR_SCALE_DTYPE;
+  if (!weight_scale_dtype_ok(w_scale_dtype)) return BFP8_ERR_SCALE_DTYPE;
   return launch_grouped_w8a8(q_a, s_a, s_stride_m, s_stride_kb, w_e4m3, w_scale, w_scale_dtype,
                              offsets_dev, G, total_M, N, K, y_bf16, ldy, workspace, ws_bytes,
                              stream);
@@ -428,7 +465,7 @@ int bfp8_linear_w8a8_silu_quant(const void* q_a, const float* s_a, int64_t s_str
   if (M < 0 || I <= 0 || K <= 0) return BFP8_ERR_INVALID_ARG;
   if (M == 0) return BFP8_OK;
   if (!q_a || !s_a || !w_e4m3 || !w_scale || !q_h || !s_h || ldq < I) return BFP8_ERR_INVALID_ARG;
-  if (w_scale_dtype != BFP8_DT_BF16 && w_scale_dtype != BFP8_DT_F32) return BFP8_ERR_SCALE_DTYPE;
+  if (!weight_scale_dtype_ok(w_scale_dtype)) return BFP8_ERR_SCALE_DTYPE;
   return launch_gemm_w8a8_swiglu(q_a, s_a, s_stride_m, s_stride_kb, w_e4m3, w_scale,
                                  w_scale_dtype, M, I, K, q_h, ldq, s_h, sh_stride_m,
                                  sh_stride_kb, workspace, ws_bytes, stream);
@@ -451,7 +488,7 @@ int bfp8_grouped_linear_silu_quant(const void* q_a, const float* s_a, int64_t s_
   if (total_M == 0) return BFP8_OK;
   if (!q_a || !s_a || !w_e4m3 || !w_scale || !offsets_dev || !q_h || !s_h || ldq < I)
     return BFP8_ERR_INVALID_ARG;
-  if (w_scale_dtype != BFP8_DT_BF16 && w_scale_dtype != BFP8_DT_F32) return BFP8_ERR_SCALE_DTYPE;
+  if (!weight_scale_dtype_ok(w_scale_dtype)) return BFP8_ERR_SCALE_DTYPE;
   return launch_grouped_w8a8_swiglu(q_a, s_a, s_stride_m, s_stride_kb, w_e4m3, w_scale,
                                     w_scale_dtype, offsets_dev, G, total_M, I, K, q_h, ldq, s_h,
                                     sh_stride_m, sh_stride_kb, workspace, ws_bytes, stream);

@@ -37,6 +37,17 @@ struct MemberTable {
 };
 int resolve_members(int64_t N, const bfp8_members* members, MemberTable* out);
 
+// A projection's w_scale_dtype: BF16 or F32, optionally OR'd with
+// BFP8_SCALE_PER_TENSOR (one multiplier for the whole tensor).
+inline bool weight_scale_dtype_ok(int32_t d) {
+  const int32_t b = d & ~static_cast<int32_t>(BFP8_SCALE_PER_TENSOR);
+  return b == BFP8_DT_BF16 || b == BFP8_DT_F32;
+}
+inline bool weight_scale_f32(int32_t d) {
+  return (d & ~static_cast<int32_t>(BFP8_SCALE_PER_TENSOR)) == BFP8_DT_F32;
+}
+inline bool weight_scale_per_tensor(int32_t d) { return (d & BFP8_SCALE_PER_TENSOR) != 0; }
+
 // Launchers (argument checks beyond the common ones happen inside).
 int launch_act_quant(const void* x, int64_t M, int64_t K, int64_t ldx, void* q, int64_t ldq,
                      float* s, int64_t ssm, int64_t sskb, void* stream);

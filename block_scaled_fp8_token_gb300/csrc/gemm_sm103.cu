@@ -61,6 +61,10 @@ struct GemmParams {
   const void* s_w;
   int32_t sw_f32;
   int64_t sw_expert_stride;  // scale elements between two experts' grids
+  // scale (row block r, K-block kb) at s_w[r * sw_rs + kb * sw_ks]: (Kb, 1) for a
+  // block grid, (0, 0) for a per-tensor multiplier
+  int64_t sw_rs;
+  int32_t sw_ks;
   __nv_bfloat16* y;
   int64_t ldy;
   int32_t vec_store;
@@ -541,15 +545,15 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
       // 64 matching up columns, each half with its own member's scale row.
       const int srow = SWIGLU ? tl.srow0 : min(tl.srow0 + (h * C::kEpiCols) / 128, tl.srow_last);
       const int64_t sw_base = GROUPED ? tl.expert * p.sw_expert_stride : 0;
-      const int64_t sw_idx = sw_base + static_cast<int64_t>(srow) * p.Kb;
-      const int64_t sw_idx_up = sw_base + static_cast<int64_t>(tl.srow_up) * p.Kb;
+      const int64_t sw_idx = sw_base + static_cast<int64_t>(srow) * p.sw_rs;
+      const int64_t sw_idx_up = sw_base + static_cast<int64_t>(tl.srow_up) * p.sw_rs;
       const float* sa_row = p.s_a + (row_ok ? arow * p.sa_sm : 0);
       auto wscale = [&](int64_t idx) -> float {
         return p.sw_f32 ? __ldg(sw32 + idx) : bf16_bits_to_f32(__ldg(sw16 + idx));
       };
       // promotion factor s_a[m,kb] * s_w[row,kb] (s_w alone for W8A16)
       auto factor = [&](int64_t idx, int kb) -> float {
-        const float sw = wscale(idx + kb);
+        const float sw = wscale(idx + static_cast<int64_t>(kb) * p.sw_ks);
         if (W8A16) return sw;
         const float sa = row_ok ? __ldg(sa_row + kb * p.sa_skb) : 0.0f;
         return sa * sw;
@@ -838,6 +842,22 @@ int launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, in
 
 bool aligned16(const void* ptr) { return reinterpret_cast<uintptr_t>(ptr) % 16 == 0; }
 
+// The weight-scale fields of the parameters: a block grid ([r, kb] at
+// r * Kb + kb, expert_stride elements per expert) or, with
+// BFP8_SCALE_PER_TENSOR, one multiplier (one per expert).
+void set_weight_scale(GemmParams& p, int32_t w_scale_dtype, int64_t expert_stride) {
+  p.sw_f32 = weight_scale_f32(w_scale_dtype) ? 1 : 0;
+  if (weight_scale_per_tensor(w_scale_dtype)) {
+    p.sw_rs = 0;
+    p.sw_ks = 0;
+    p.sw_expert_stride = 1;
+  } else {
+    p.sw_rs = p.Kb;
+    p.sw_ks = 1;
+    p.sw_expert_stride = expert_stride;
+  }
+}
+
 int fill_members(GemmParams& p, const MemberTable& mt, int bn, int cluster, int64_t M,
                  const void* y, int64_t ldy) {
   p.n_members = mt.count;
@@ -938,7 +958,7 @@ int launch_gemm_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t s
   p.sa_sm = sa_sm;
   p.sa_skb = sa_skb;
   p.s_w = w_scale;
-  p.sw_f32 = w_scale_dtype == BFP8_DT_F32;
+  set_weight_scale(p, w_scale_dtype, 0);
   p.y = static_cast<__nv_bfloat16*>(y);
   p.ldy = ldy;
   rc = fill_members(p, mt, kBN8, C8::kCluster, M, y, ldy);
@@ -968,7 +988,7 @@ int launch_gemm_w8a16(const void* x, int64_t ldx, const void* w, const void* w_s
   p.Kb = static_cast<int32_t>((K + BK - 1) / BK);
   p.s_a = nullptr;
   p.s_w = w_scale;
-  p.sw_f32 = w_scale_dtype == BFP8_DT_F32;
+  set_weight_scale(p, w_scale_dtype, 0);
   p.y = static_cast<__nv_bfloat16*>(y);
   p.ldy = ldy;
   rc = fill_members(p, mt, kBN16, Cfg<kBN16, kStages16, true, false>::kCluster, M, y, ldy);
@@ -1001,8 +1021,7 @@ int launch_grouped_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_
   p.sa_sm = sa_sm;
   p.sa_skb = sa_skb;
   p.s_w = w_scale;
-  p.sw_f32 = w_scale_dtype == BFP8_DT_F32;
-  p.sw_expert_stride = ((N + 127) / 128) * static_cast<int64_t>(p.Kb);
+  set_weight_scale(p, w_scale_dtype, ((N + 127) / 128) * static_cast<int64_t>(p.Kb));
   p.y = static_cast<__nv_bfloat16*>(y);
   p.ldy = ldy;
   p.vec_store = (aligned16(y) && ldy % 8 == 0) ? 1 : 0;
@@ -1071,7 +1090,7 @@ int launch_gemm_w8a8_swiglu(const void* q_a, const float* s_a, int64_t sa_sm, in
   p.sa_sm = sa_sm;
   p.sa_skb = sa_skb;
   p.s_w = w_scale;
-  p.sw_f32 = w_scale_dtype == BFP8_DT_F32;
+  set_weight_scale(p, w_scale_dtype, 0);
   // tiles walk h's I columns 128 at a time: one member of I rows
   MemberTable mt;
   mt.count = 1;
@@ -1111,9 +1130,8 @@ int launch_grouped_w8a8_swiglu(const void* q_a, const float* s_a, int64_t sa_sm,
   p.sa_sm = sa_sm;
   p.sa_skb = sa_skb;
   p.s_w = w_scale;
-  p.sw_f32 = w_scale_dtype == BFP8_DT_F32;
   // each expert's grid stacks the gate member's rows over the up member's
-  p.sw_expert_stride = 2 * ((I + 127) / 128) * static_cast<int64_t>(p.Kb);
+  set_weight_scale(p, w_scale_dtype, 2 * ((I + 127) / 128) * static_cast<int64_t>(p.Kb));
   p.offsets = offsets;
   p.G = G;
   p.N = static_cast<int32_t>(I);

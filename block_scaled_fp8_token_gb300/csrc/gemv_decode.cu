@@ -93,6 +93,9 @@ struct GemvParams {
   int32_t grid;
   const void* s_w;
   int32_t sw_f32;
+  // scale (row block r, K-block kb) at s_w[r * sw_rs + kb * sw_ks]: (Kb, 1) for a
+  // block grid, (0, 0) for a per-tensor multiplier
+  int32_t sw_rs, sw_ks;
   int32_t n_members;
   int32_t mem_n0[BFP8_MAX_MEMBERS], mem_rows[BFP8_MAX_MEMBERS], mem_sbase[BFP8_MAX_MEMBERS];
   __nv_bfloat16* y;
@@ -397,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t tile_u0 = static_cast<int64_t>(rt) * p.Kb;
       const int64_t seg_end = min(ue, tile_u0 + p.Kb);
       const int n = rt * kRows + row;
-      const int64_t srow_idx = static_cast<int64_t>(scale_row_of(p, n)) * p.Kb;
+      const int64_t srow_idx = static_cast<int64_t>(scale_row_of(p, n)) * p.sw_rs;
       float acc[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
@@ -410,8 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int b = static_cast<int>(i % kTBufs);
           const bool pair = ((b & 1) == 0) && (uu + 1 < seg_end);
           const int kb = static_cast<int>(uu - tile_u0);
-          const float sw0 = load_scale(p, srow_idx + kb);
-          const float sw1 = pair ? load_scale(p, srow_idx + kb + 1) : 0.0f;
+          const float sw0 = load_scale(p, srow_idx + static_cast<int64_t>(kb) * p.sw_ks);
+          const float sw1 = pair ? load_scale(p, srow_idx + static_cast<int64_t>(kb + 1) * p.sw_ks)
+                                 : 0.0f;
           // per-token factors of the two K-blocks: 2^-e of the split (W8A16)
           // or the 1x128 activation scale (W8A8)
           float xi0[16], xi1[16];
@@ -651,7 +655,9 @@ int init_params(GemvParams& p, const void* w, const void* w_scale, int32_t w_sca
   p.U = static_cast<int64_t>(p.RT) * p.Kb;
   p.grid = static_cast<int32_t>(p.U < sms ? p.U : sms);
   p.s_w = w_scale;
-  p.sw_f32 = w_scale_dtype == BFP8_DT_F32;
+  p.sw_f32 = weight_scale_f32(w_scale_dtype) ? 1 : 0;
+  p.sw_rs = weight_scale_per_tensor(w_scale_dtype) ? 0 : p.Kb;
+  p.sw_ks = weight_scale_per_tensor(w_scale_dtype) ? 0 : 1;
   p.n_members = mt.count;
   for (int i = 0; i < mt.count; ++i) {
     p.mem_n0[i] = static_cast<int32_t>(mt.n0[i]);
@@ -786,7 +792,7 @@ int launch_decode_ffn(int32_t arith, const void* x, int64_t ldx, const void* w_g
   if (arith != BFP8_DECODE_W8A16 && arith != BFP8_DECODE_W8A8) return BFP8_ERR_INVALID_ARG;
   if (!x || !w_gu || !s_gu || !w_dn || !s_dn || !y || !workspace) return BFP8_ERR_INVALID_ARG;
   if (M < 1 || M > 16 || H <= 0 || I <= 0 || ldx < H || ldy < H) return BFP8_ERR_INVALID_ARG;
-  if (w_scale_dtype != BFP8_DT_BF16 && w_scale_dtype != BFP8_DT_F32) return BFP8_ERR_SCALE_DTYPE;
+  if (!weight_scale_dtype_ok(w_scale_dtype)) return BFP8_ERR_SCALE_DTYPE;
   if (H % 16 != 0 || I % 16 != 0) return BFP8_ERR_UNSUPPORTED;
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return BFP8_ERR_INVALID_ARG;
   int sms = 0;
@@ -886,7 +892,7 @@ extern "C" int bfp8_gemv_decode_noalloc(const void* x_bf16, int64_t ldx, const v
   if (M < 1 || M > 16 || N <= 0 || K <= 0) return BFP8_ERR_INVALID_ARG;
   if (!x_bf16 || !w_e4m3 || !w_scale || !y_bf16 || ldy < N || ldx < K)
     return BFP8_ERR_INVALID_ARG;
-  if (w_scale_dtype != BFP8_DT_BF16 && w_scale_dtype != BFP8_DT_F32) return BFP8_ERR_SCALE_DTYPE;
+  if (!weight_scale_dtype_ok(w_scale_dtype)) return BFP8_ERR_SCALE_DTYPE;
   MemberTable mt;
   int rc = resolve_members(N, members, &mt);
   if (rc != BFP8_OK) return rc;

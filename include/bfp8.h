@@ -71,6 +71,15 @@ enum bfp8_dtype {
   BFP8_DT_F32 = 5
 };
 
+/* OR into any w_scale_dtype argument of a projection (BFP8_DT_BF16 or
+ * BFP8_DT_F32): the weight is per-tensor scaled, and w_scale points at ONE
+ * multiplier of that dtype (one per expert for the grouped entry points),
+ * read as the degenerate block grid whose single block covers the tensor.
+ *   [FP8 Native Serving, "The two FP8 checkpoint shapes": per-tensor scaled
+ *    checkpoints read as a block case with block_size = infinity]
+ * With members, the one multiplier covers every member. */
+#define BFP8_SCALE_PER_TENSOR 0x100
+
 /* Largest number of members a grouped (fused) weight may have. */
 #define BFP8_MAX_MEMBERS 8
 
@@ -95,6 +104,8 @@ typedef struct {
   int32_t declared_block[2];   /* config's weight_block_size                  */
   int32_t n_members;           /* 0 = plain tensor; else rows per member below */
   const int64_t* member_rows;  /* host array [n_members], NULL if n_members==0 */
+  int32_t tensor_scale_dtype;  /* dtype of a one-element "weight_scale" leaf (a
+                                  per-tensor scaled weight), BFP8_DT_NONE if absent */
 } bfp8_weight_desc;
 
 /*
@@ -106,6 +117,12 @@ typedef struct {
  *    row-wise tree, a transposed or mis-blocked grid, an FP8 weight with no
  *    scale, a rank-1 scale and a config that disagrees with the bytes are each
  *    refused by name]
+ * A per-tensor scaled weight (one multiplier, tensor_scale_dtype set) is the
+ * degenerate grid [FP8 Native Serving, "The two FP8 checkpoint shapes"]:
+ * after QUANT_METHOD it is refused as AMBIGUOUS_SCALE next to another scale
+ * leaf, BLOCK_SIZE if the config declares a weight_block_size, SCALE_DTYPE
+ * unless BF16/F32, GROUP if members do not partition N; otherwise OK (pass
+ * its dtype OR'd with BFP8_SCALE_PER_TENSOR to the projections).
  * Pure host code; needs no GPU. The first failing rule decides:
  *   INVALID_ARG, E5M2, NOT_FP8, QUANT_METHOD, BLOCK_SIZE, AMBIGUOUS_SCALE
  *   (row+block), ROW_SCALE (row leaf only), NO_SCALE, ROW_SCALE (rank 1),

@@ -18,6 +18,12 @@ Test infrastructure (CPU oracle); see the package docstring for who may use it.
   load [th#1803 decoder PR, "Why the refusals matter more than the load"].
   Per 128x128 block: s32 = max(amax, 1e-10)/448, stored as BF16 (RNE) or
   F32. Then q = E4M3_RNE_sat(w / s) with s the stored scale widened to f32.
+* Per-tensor scaled weights [FP8 Native Serving, "The two FP8 checkpoint
+  shapes"]: one multiplier for the whole tensor, s = max(amax, 1e-10)/448
+  over every element (synthetic checkpoints only), read as a block case whose
+  single block covers the tensor: tensor_scale_grid writes that multiplier
+  into every 128x128 block of the member-local grid, so the block-scaled
+  projections apply it unchanged.
 * dequantize_block_scaled: w = e4m3(q) * s in float32, with s a MULTIPLIER
   despite the "_inv" suffix [Qwen checkpoints with block FP8 weights, first
   paragraph; th#1803 decoder PR, "What lands"].
@@ -98,6 +104,36 @@ def quantize_weight_blocks(w: np.ndarray, scale_dtype: str = "bf16"):
                 s = s32
             q[r0:r1, c0:c1] = e4m3_encode_rne_sat((blk / np.float32(s)).astype(np.float32))
     return q, s_out
+
+
+def quantize_weight_tensor(w: np.ndarray, scale_dtype: str = "f32"):
+    """Per-tensor quantization of a float32 weight [N, K] (one multiplier).
+
+    Returns (q uint8 [N, K], s): s a float32 scalar array (shape ()) if
+    scale_dtype == "f32", or uint16 BF16 bits if "bf16"; q = E4M3_RNE_sat(w / s)
+    with s the stored multiplier widened to float32."""
+    if scale_dtype not in ("bf16", "f32"):
+        raise ValueError("scale_dtype must be 'bf16' or 'f32'")
+    w = np.asarray(w, dtype=np.float32)
+    amax = np.float32(np.max(np.abs(w))) if w.size else np.float32(0)
+    s32 = np.float32(np.maximum(amax, SCALE_FLOOR) / E4M3_MAX_F32)
+    if scale_dtype == "bf16":
+        s_out = f32_to_bf16_bits(s32)
+        s = bf16_bits_to_f32(s_out)
+    else:
+        s_out = np.array(s32, dtype=np.float32)
+        s = s32
+    return e4m3_encode_rne_sat((w / np.float32(s)).astype(np.float32)), s_out
+
+
+def tensor_scale_grid(s, N: int, K: int, members=None) -> np.ndarray:
+    """The degenerate grid of a per-tensor multiplier s (BF16 bits or float32):
+    s in every block of the member-local grid [sum ceil(N_i/128), ceil(K/128)],
+    in s's own storage type."""
+    s = np.asarray(s)
+    rows = members or [N]
+    Nb = sum(_ceil_div(int(n), BLOCK) for n in rows)
+    return np.full((Nb, _ceil_div(K, BLOCK)), s.reshape(()), dtype=s.dtype)
 
 
 def scales_to_f32(s: np.ndarray) -> np.ndarray:

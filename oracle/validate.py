@@ -11,6 +11,9 @@ The pages list what must be refused before any weight byte is uploaded:
   that disagrees with the bytes [th#1803 decoder PR, "Why the refusals matter
   more than the load"];
 * dense trees [th#1803 decoder PR, "Proof", item 4].
+A per-tensor scaled weight (one f32 multiplier in a "weight_scale" leaf) is
+the other FP8 checkpoint shape, read as a block case whose single block
+covers the tensor [FP8 Native Serving, "The two FP8 checkpoint shapes"].
 The checkpoint must declare quant_method fp8 and weight_block_size [128,128],
 and the grid is ceil-divided with member-local origins [Qwen checkpoints with
 block FP8 weights, first and third paragraphs]. Verification uses headers
@@ -27,6 +30,10 @@ Readings where the pages are silent:
   row count equals N (a per-row grid) when N != ceil(N/128).
 * a grouped tensor whose grid was built on the stacked rows (ceil(sum N_i /
   128) rows) instead of member-local origins is refused as GROUP.
+* per-tensor: its one-element scale next to a block grid or a per-row scale is
+  ambiguous; a declared weight_block_size disagrees with it (BLOCK_SIZE); its
+  dtype must be BF16 or F32 like a grid's; members must still partition N,
+  and the one multiplier covers every member.
 """
 
 from __future__ import annotations
@@ -45,7 +52,8 @@ def validate_grid(desc: dict) -> str:
     desc keys: weight_dtype ("E4M3", "E5M2", "BF16", "F16", "F32"),
     weight_shape (tuple), scale_dtype (None or a dtype name),
     scale_shape (tuple or None), has_row_scale (bool),
-    declared_quant_fp8 (bool), declared_block (pair), member_rows (list or None).
+    declared_quant_fp8 (bool), declared_block (pair), member_rows (list or None),
+    tensor_scale_dtype (None or a dtype name: a one-element weight_scale).
     """
     shape = tuple(desc.get("weight_shape") or ())
     if len(shape) != 2 or shape[0] <= 0 or shape[1] <= 0:
@@ -58,10 +66,24 @@ def validate_grid(desc: dict) -> str:
         return "NOT_FP8"
     if not desc.get("declared_quant_fp8", False):
         return "QUANT_METHOD"
-    if tuple(desc.get("declared_block") or ()) != (128, 128):
-        return "BLOCK_SIZE"
     sdt = desc.get("scale_dtype")
     has_block = sdt is not None
+    tdt = desc.get("tensor_scale_dtype")
+    if tdt is not None:
+        if has_block or desc.get("has_row_scale", False):
+            return "AMBIGUOUS_SCALE"
+        if tuple(desc.get("declared_block") or (0, 0)) != (0, 0):
+            return "BLOCK_SIZE"
+        if tdt not in SCALE_DTYPES_OK:
+            return "SCALE_DTYPE"
+        members = desc.get("member_rows")
+        if members is not None:
+            members = [int(v) for v in members]
+            if len(members) == 0 or any(v <= 0 for v in members) or sum(members) != N:
+                return "GROUP"
+        return "OK"
+    if tuple(desc.get("declared_block") or ()) != (128, 128):
+        return "BLOCK_SIZE"
     if desc.get("has_row_scale", False):
         return "AMBIGUOUS_SCALE" if has_block else "ROW_SCALE"
     if not has_block:

@@ -15,6 +15,7 @@ import torch
 from block_scaled_fp8_token_gb300 import synth
 from conftest import GOLDEN
 from oracle import formats as F
+from oracle import linear as L
 from oracle import quant as Q
 from oracle.linear import scale_grid_shape
 
@@ -188,3 +189,48 @@ def test_silu_mul_quant_is_quant_of_silu():
     q, s = Q.silu_mul_act_quant(gu)
     q2, s2 = Q.act_quant_group(Q.silu_mul_bf16(gu))
     assert q.shape == (6, 256) and np.array_equal(q, q2) and np.array_equal(s, s2)
+
+
+# ---- per-tensor scaled weights (the degenerate grid) -------------------------
+
+def test_per_tensor_quant_max_element_and_bound():
+    rng = np.random.default_rng(21)
+    w = (rng.normal(size=(200, 300)) * 0.02).astype(np.float32)
+    w[17, 250] = 0.5                                   # the tensor maximum
+    for sd in ("f32", "bf16"):
+        q, s = Q.quantize_weight_tensor(w, sd)
+        s32 = float(F.bf16_bits_to_f32(s)) if sd == "bf16" else float(s)
+        lut = F.e4m3_decode_lut().astype(np.float64)
+        if sd == "f32":
+            assert s32 == float(np.float32(0.5) / np.float32(448.0))
+            assert lut[q[17, 250]] == 448.0            # the maximum maps to the top code
+        deq = lut[q] * s32
+        # every element within half an E4M3 step of w (relative 2^-4 for
+        # normals, 2^-10 * s absolute in the subnormal range)
+        err = np.abs(deq - w)
+        assert np.all(err <= np.maximum(np.abs(w) * 2.0 ** -4, s32 * 2.0 ** -10) * (1 + 2 ** -8))
+
+
+def test_tensor_scale_grid_is_the_degenerate_block_case():
+    rng = np.random.default_rng(22)
+    w = (rng.normal(size=(300, 260)) * 0.02).astype(np.float32)
+    q, s = Q.quantize_weight_tensor(w, "f32")
+    grid = Q.tensor_scale_grid(s, 300, 260)
+    assert grid.shape == (3, 3) and grid.dtype == np.float32 and np.all(grid == s)
+    # dequantizing through the grid is e4m3(q) * s, element by element
+    assert np.array_equal(Q.dequantize_block_scaled(q, grid),
+                          (F.e4m3_decode_lut()[q].astype(np.float32) * np.float32(s)))
+    # members: one multiplier covers both members' member-local grids
+    gm = Q.tensor_scale_grid(F.f32_to_bf16_bits(np.float32(0.125)), 300, 260, [200, 100])
+    assert gm.shape == (2 + 1, 3) and gm.dtype == np.uint16
+    assert np.all(F.bf16_bits_to_f32(gm) == np.float32(0.125))
+
+
+def test_per_tensor_projection_is_plain_matmul_of_dequantized_operands():
+    rng = np.random.default_rng(23)
+    xb = F.f64_to_bf16_bits(rng.normal(size=(5, 200)))
+    q, s = Q.quantize_weight_tensor((rng.normal(size=(140, 200)) * 0.05).astype(np.float32), "f32")
+    grid = Q.tensor_scale_grid(s, 140, 200)
+    x = F.bf16_bits_to_f32(xb).astype(np.float64)
+    wdeq = F.e4m3_decode_lut()[q].astype(np.float64) * float(s)
+    assert np.allclose(L.linear_w8a16(xb, q, grid), x @ wdeq.T, rtol=1e-12, atol=1e-12)

@@ -23,6 +23,7 @@ def _oracle_desc(d):
         "declared_quant_fp8": d.get("declared_quant_fp8", True),
         "declared_block": tuple(d.get("declared_block", (128, 128))),
         "member_rows": d.get("member_rows"),
+        "tensor_scale_dtype": d.get("tensor_scale_dtype"),
     }
 
 
@@ -39,7 +40,8 @@ def test_library_refusals(case, bfp8):
         scale_dtype=DT.get(d.get("scale_dtype"), 0) if d.get("scale_dtype") else 0,
         scale_shape=d.get("scale_shape"), has_row_scale=d.get("has_row_scale", False),
         declared_quant_fp8=d.get("declared_quant_fp8", True),
-        declared_block=d.get("declared_block", (128, 128)), member_rows=d.get("member_rows"))
+        declared_block=d.get("declared_block", (128, 128)), member_rows=d.get("member_rows"),
+        tensor_scale_dtype=DT.get(d.get("tensor_scale_dtype"), 0))
     rc, msg = bfp8.bfp8_validate_grid(desc)
     assert bfp8.bfp8_status_string(rc) == case["expect"], msg
     assert msg
