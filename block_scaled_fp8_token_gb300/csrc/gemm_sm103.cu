@@ -180,8 +180,8 @@ struct Cfg {
   static constexpr int kLaunchRegs = 168;      // 65536 / 384 rounded down to a multiple of 8
   // The fused SiLU*up epilogue keeps a second scale factor live in the
   // promotion loop, so it takes 8 more registers per epilogue thread.
-  static constexpr int kCtrlRegs = SWIGLU ? 48 : 64;
-  static constexpr int kEpiRegs = SWIGLU ? 224 : 216;
+  static constexpr int kCtrlRegs = SWIGLU ? 40 : 64;
+  static constexpr int kEpiRegs = SWIGLU ? 232 : 216;
   static_assert(!kSplitRegs || kCtrlRegs * 128 + kEpiRegs * 256 <= kLaunchRegs * kThreads,
                 "register split must add up to the launch allocation");
   static constexpr int kEpiCols = BN / 2;
@@ -548,33 +548,52 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
       const int64_t sw_idx = sw_base + static_cast<int64_t>(srow) * p.sw_rs;
       const int64_t sw_idx_up = sw_base + static_cast<int64_t>(tl.srow_up) * p.sw_rs;
       const float* sa_row = p.s_a + (row_ok ? arow * p.sa_sm : 0);
-      auto wscale = [&](int64_t idx) -> float {
-        return p.sw_f32 ? __ldg(sw32 + idx) : bf16_bits_to_f32(__ldg(sw16 + idx));
+      // The promotion factor is s_a[m,kb] * s_w[row,kb] (s_w alone for W8A16).
+      // No value loaded in this loop is used before the loop's barrier wait:
+      // a warp that stalled on a load there would hold up the TMEM buffer for
+      // every other warp. s_w is fetched 32 K-blocks at a time, one K-block
+      // per lane, as raw bits (a window ahead), and each K-block takes its
+      // value with a shuffle; s_a is loaded at the top of its K-block and
+      // multiplied in after the wait.
+      auto sw_raw = [&](int64_t idx, int k) -> uint32_t {
+        uint32_t r = 0u;
+        if (k < kb1) {
+          const int64_t i = idx + static_cast<int64_t>(k) * p.sw_ks;
+          if (p.sw_f32)
+            r = __ldg(reinterpret_cast<const uint32_t*>(sw32) + i);
+          else
+            r = __ldg(sw16 + i);
+        }
+        return r;
       };
-      // promotion factor s_a[m,kb] * s_w[row,kb] (s_w alone for W8A16)
-      auto factor = [&](int64_t idx, int kb) -> float {
-        const float sw = wscale(idx + static_cast<int64_t>(kb) * p.sw_ks);
-        if (W8A16) return sw;
-        const float sa = row_ok ? __ldg(sa_row + kb * p.sa_skb) : 0.0f;
-        return sa * sw;
+      auto sw_value = [&](uint32_t raw) -> float {
+        return __uint_as_float(p.sw_f32 ? raw : raw << 16);
       };
       // FP32 accumulator pairs: the promotion runs as packed FP32x2 FMAs
       float2 acc[C::kEpiCols / 2];
 #pragma unroll
       for (int i = 0; i < C::kEpiCols / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
-      // factors of the next K-block are loaded one K-block ahead; the up
-      // half's factor exists only with the fused SiLU*up epilogue
-      float f_next = factor(sw_idx, kb0);
-      float fu_next = SWIGLU ? factor(sw_idx_up, kb0) : 0.0f;
+      // the up half's factor exists only with the fused SiLU*up epilogue
+      uint32_t sw_cur = sw_raw(sw_idx, kb0 + lane);
+      uint32_t su_cur = SWIGLU ? sw_raw(sw_idx_up, kb0 + lane) : 0u;
+      uint32_t sw_nxt = sw_raw(sw_idx, kb0 + 32 + lane);
+      uint32_t su_nxt = SWIGLU ? sw_raw(sw_idx_up, kb0 + 32 + lane) : 0u;
       for (int kb = kb0; kb < kb1 && ok; ++kb) {
-        const float f = f_next, fu = fu_next;
-        const float2 f2 = make_float2(f, f);
-        if (kb + 1 < kb1) {
-          f_next = factor(sw_idx, kb + 1);
-          if (SWIGLU) fu_next = factor(sw_idx_up, kb + 1);
+        const int wl = (kb - kb0) & 31;
+        if (wl == 0 && kb != kb0) {
+          sw_cur = sw_nxt;
+          su_cur = su_nxt;
+          sw_nxt = sw_raw(sw_idx, kb + 32 + lane);
+          if (SWIGLU) su_nxt = sw_raw(sw_idx_up, kb + 32 + lane);
         }
+        const uint32_t sw_bits = __shfl_sync(0xffffffffu, sw_cur, wl);
+        const uint32_t su_bits = SWIGLU ? __shfl_sync(0xffffffffu, su_cur, wl) : 0u;
+        const float sa = (W8A16 || !row_ok) ? (W8A16 ? 1.0f : 0.0f) : __ldg(sa_row + kb * p.sa_skb);
         const bool w_ok = mbar_wait(tfull_bar(buf), bphase, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
+        const float f = W8A16 ? sw_value(sw_bits) : sa * sw_value(sw_bits);
+        const float fu = SWIGLU ? sa * sw_value(su_bits) : 0.0f;
+        const float2 f2 = make_float2(f, f);
         tc_fence_after();
         const uint32_t tcol0 = static_cast<uint32_t>(buf * BN + h * (SWIGLU ? 64 : C::kEpiCols));
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + tcol0;
