@@ -86,45 +86,65 @@ struct GemmParams {
   // stream-K: split tiles exchange FP32 partials through a caller workspace
   int32_t stream_k;
   int32_t* ws_counters;   // one arrival counter per tile, zero on entry
-  float* ws_partials;     // [CTAs][2][BM][BN] FP32 partial tiles
+  float* ws_partials;     // [CTAs][2] FP32 partial tiles, each [BN/4][BM] float4s
 };
 
 // Work partition over G CTAs. Whole tiles: CTA c takes tiles c, c + G, ...,
 // so the CTAs running at the same time work on neighbouring tiles and share
 // weight tiles through L2. With stream-K, all but the last one-to-two waves are
 // still whole tiles in that order. The K-block units of the remaining tiles are
-// cut into G equal contiguous ranges, one per CTA, so the last wave leaves no
-// SM idle, and each of those tiles has only two or three contributors.
+// cut into G equal contiguous ranges, one per contributor, so the last wave
+// leaves no SM idle, and each of those tiles has only two or three
+// contributors (see the lockstep grouping below when every tile is split).
 // Work is walked as segments: runs of K-blocks inside one tile.
 struct SegIter {
   int64_t u, ue;   // stream-K part: next unit, end of this CTA's range (absolute units)
   int t, t_end, step;  // whole-tile part: next tile, end, stride
+  int mu, r;       // stream-K tile of unit u: (u / Kb) * mu + r
 };
-struct SkSplit {
+// Stream-K geometry. Plain: G = CTAs contributors, one per CTA (mu = 1).
+// Lockstep (dense, every tile split): the CTAs form G = CTAs / mu groups of
+// mu = m_tiles; a group's contributor range runs over (N tile, K-block) units
+// and member r of the group computes M tile r of each, so the mu CTAs that
+// share a weight tile read each of its K-blocks at the same time (through L2,
+// once from DRAM) instead of at staggered offsets. CTAs past the last group
+// get no stream-K work.
+struct SkGeo {
   int dp_tiles;    // tiles handed out whole
   int64_t U0;      // first stream-K unit (dp_tiles * Kb)
-  int64_t U;       // stream-K units
+  int64_t U;       // stream-K units per member (contributor unit space)
+  int G, mu;
 };
-BFP8_DEV SkSplit sk_split(bool sk, int total, int Kb, int G) {
-  SkSplit s;
-  const int waves = total / G;
-  s.dp_tiles = sk ? (waves > 1 ? (waves - 1) * G : 0) : total;
-  s.U0 = static_cast<int64_t>(s.dp_tiles) * Kb;
-  s.U = static_cast<int64_t>(total - s.dp_tiles) * Kb;
-  return s;
+BFP8_DEV SkGeo sk_geo(bool sk, int total, int Kb, int ncl, int mu_lock) {
+  SkGeo g;
+  const int waves = total / ncl;
+  g.dp_tiles = sk ? (waves > 1 ? (waves - 1) * ncl : 0) : total;
+  g.mu = 1;
+  g.G = ncl;
+  if (sk && g.dp_tiles == 0 && mu_lock > 1 && mu_lock <= ncl && total % mu_lock == 0) {
+    g.mu = mu_lock;
+    g.G = ncl / mu_lock;
+  }
+  g.U0 = static_cast<int64_t>(g.dp_tiles) * Kb;
+  g.U = static_cast<int64_t>((total - g.dp_tiles) / g.mu) * Kb;
+  return g;
 }
 BFP8_DEV int64_t sk_unit_begin(int64_t U, int G, int64_t c) { return (c * U) / G; }
-// The CTA whose range holds unit u.
+// The contributor whose range holds unit u.
 BFP8_DEV int64_t sk_cta_of_unit(int64_t U, int G, int64_t u) { return ((u + 1) * G + U - 1) / U - 1; }
 
-BFP8_DEV SegIter seg_begin(bool sk, int total, int Kb, int cid, int ncl) {
-  const SkSplit sp = sk_split(sk, total, Kb, ncl);
+BFP8_DEV SegIter seg_begin(bool sk, int total, int Kb, int cid, int ncl, int mu_lock) {
+  const SkGeo g = sk_geo(sk, total, Kb, ncl, mu_lock);
   SegIter it;
   it.t = cid;
-  it.t_end = sp.dp_tiles;
+  it.t_end = g.dp_tiles;
   it.step = ncl;
-  it.u = sk ? sp.U0 + sk_unit_begin(sp.U, ncl, cid) : 0;
-  it.ue = sk ? sp.U0 + sk_unit_begin(sp.U, ncl, cid + 1) : 0;
+  it.mu = g.mu;
+  it.r = cid % g.mu;
+  const int v = cid / g.mu;
+  const bool has = sk && v < g.G;
+  it.u = has ? g.U0 + sk_unit_begin(g.U, g.G, v) : 0;
+  it.ue = has ? g.U0 + sk_unit_begin(g.U, g.G, v + 1) : 0;
   return it;
 }
 BFP8_DEV bool next_seg(bool sk, SegIter& it, int total, int Kb, int& t, int& kb0, int& kb1) {
@@ -138,8 +158,9 @@ BFP8_DEV bool next_seg(bool sk, SegIter& it, int total, int Kb, int& t, int& kb0
     return true;
   }
   if (it.u >= it.ue) return false;
-  t = static_cast<int>(it.u / Kb);
-  kb0 = static_cast<int>(it.u - static_cast<int64_t>(t) * Kb);
+  const int nt = static_cast<int>(it.u / Kb);
+  t = nt * it.mu + it.r;
+  kb0 = static_cast<int>(it.u - static_cast<int64_t>(nt) * Kb);
   const int64_t left = it.ue - it.u;
   kb1 = left < Kb - kb0 ? kb0 + static_cast<int>(left) : Kb;
   it.u += kb1 - kb0;
@@ -416,9 +437,14 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
   // empty (partial tiles cost an FP32 round trip through L2 and a fixup); it
   // also needs every CTA to own at least one K-block unit of the split part.
   const int waves = (total + ncl - 1) / ncl;
-  const bool sparse_tail = waves > 0 && 5 * total < 4 * waves * ncl;   // fill < 80%
+  // Dense: last-wave fill < 85% (O at M=4096, 84%, gains 4%; QKV at 93% loses
+  // 2%). Grouped tiles are short and their split tiles cost more: < 80%.
+  const bool sparse_tail = waves > 0 && (GROUPED ? 5 * total < 4 * waves * ncl
+                                                 : 20 * total < 17 * waves * ncl);
   const bool sk = CL == 1 && p.stream_k && sparse_tail &&
-                  sk_split(true, total, p.Kb, ncl).U >= static_cast<int64_t>(ncl);
+                  sk_geo(true, total, p.Kb, ncl, 0).U >= static_cast<int64_t>(ncl);
+  // lockstep stream-K groups (dense tiles are numbered M-fastest)
+  const int mu_lock = (GROUPED || CL > 1) ? 0 : p.m_tiles;
 
   if (warp < C::kEpiWarp0) {
     // warpgroup 0: producer (warp 0) and MMA issuer (warp 1)
@@ -429,7 +455,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
         int stage = 0;
         uint32_t phase = 0, armed = 0, armed_phase = 0;
         bool ok = true;
-        SegIter it = seg_begin(sk, total, p.Kb, cid, ncl);
+        SegIter it = seg_begin(sk, total, p.Kb, cid, ncl, mu_lock);
         int t, kb0, kb1;
         while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
           Tile tl;
@@ -486,7 +512,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
       int stage = 0, buf = 0;
       uint32_t phase = 0, bphase = 0;
       bool ok = true;
-      SegIter it = seg_begin(sk, total, p.Kb, cid, ncl);
+      SegIter it = seg_begin(sk, total, p.Kb, cid, ncl, mu_lock);
       int t, kb0, kb1;
       while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -551,7 +577,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
       int slot = 0;
       uint32_t fphase = 0;
       bool ok = true;
-      SegIter it = seg_begin(sk, total, p.Kb, cid, ncl);
+      SegIter it = seg_begin(sk, total, p.Kb, cid, ncl, mu_lock);
       int t, kb0, kb1;
       while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
         Tile tl;
@@ -599,7 +625,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
     bool ok = true;
     // Every epilogue warp walks every segment, even after a failed wait, so
     // that all of them reach the same named barriers (those cannot time out).
-    SegIter it = seg_begin(sk, total, p.Kb, cid, ncl);
+    SegIter it = seg_begin(sk, total, p.Kb, cid, ncl, mu_lock);
     int t, kb0, kb1;
     while (next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
       Tile tl;
@@ -716,22 +742,29 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
         // Split tile: publish this CTA's FP32 partial. The last contributor to
         // arrive sums every contributor's partial in CTA order (deterministic)
         // and stores the tile; nobody waits for anybody.
-        const SkSplit sp = sk_split(true, total, p.Kb, ncl);
-        const int64_t U = sp.U;
-        const int64_t tile_u0 = static_cast<int64_t>(t) * p.Kb - sp.U0;  // within the split part
-        const int slot = (tile_u0 + kb0 == sk_unit_begin(U, ncl, cid)) ? 0 : 1;
+        // contributors are indexed v = cid / mu (member r = cid % mu of each)
+        const SkGeo sg = sk_geo(true, total, p.Kb, ncl, mu_lock);
+        const int64_t U = sg.U;
+        const int G = sg.G;
+        const int mu = sg.mu, r = cid % sg.mu;
+        const int64_t tile_u0 = static_cast<int64_t>((t - r) / mu) * p.Kb - sg.U0;
+        const int slot = (tile_u0 + kb0 == sk_unit_begin(U, G, cid / mu)) ? 0 : 1;
+        // A partial tile is stored column-chunk-major ([BN/4][BM] float4s),
+        // so each warp store (and each fixup load) covers 32 consecutive rows
+        // of one 4-column chunk: 512 contiguous bytes.
         float4* mine = reinterpret_cast<float4*>(
-            p.ws_partials + ((static_cast<int64_t>(cid) * 2 + slot) * BM + row_in_tile) * BN +
-            h * C::kEpiCols);
+                           p.ws_partials + (static_cast<int64_t>(cid) * 2 + slot) * BM * BN) +
+                       (h * (C::kEpiCols / 4)) * BM + row_in_tile;
         if (ok) {
 #pragma unroll
           for (int i = 0; i < C::kEpiCols / 4; ++i)
-            __stcg(mine + i, make_float4(acc[2 * i].x, acc[2 * i].y, acc[2 * i + 1].x, acc[2 * i + 1].y));
+            __stcg(mine + i * BM,
+                   make_float4(acc[2 * i].x, acc[2 * i].y, acc[2 * i + 1].x, acc[2 * i + 1].y));
         }
         __threadfence();
         named_bar_sync(1, 32 * C::kEpiWarps);
-        const int64_t c_first = sk_cta_of_unit(U, ncl, tile_u0);
-        const int64_t c_last = sk_cta_of_unit(U, ncl, tile_u0 + p.Kb - 1);
+        const int64_t c_first = sk_cta_of_unit(U, G, tile_u0);
+        const int64_t c_last = sk_cta_of_unit(U, G, tile_u0 + p.Kb - 1);
         if (ew == 0 && lane == 0) {
           int last_arrival = 0;
           if (ok && !*abort_flag) {
@@ -748,12 +781,14 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
 #pragma unroll
         for (int i = 0; i < C::kEpiCols / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
         for (int64_t c = c_first; c <= c_last; ++c) {
-          const int sl = (sk_unit_begin(U, ncl, c) >= tile_u0) ? 0 : 1;
-          const float4* src = reinterpret_cast<const float4*>(
-              p.ws_partials + ((c * 2 + sl) * BM + row_in_tile) * BN + h * C::kEpiCols);
+          const int sl = (sk_unit_begin(U, G, c) >= tile_u0) ? 0 : 1;
+          const int64_t cta = c * mu + r;
+          const float4* src =
+              reinterpret_cast<const float4*>(p.ws_partials + (cta * 2 + sl) * BM * BN) +
+              (h * (C::kEpiCols / 4)) * BM + row_in_tile;
 #pragma unroll
           for (int i = 0; i < C::kEpiCols / 4; ++i) {
-            const float4 v = __ldcg(src + i);
+            const float4 v = __ldcg(src + i * BM);
             acc[2 * i].x += v.x;
             acc[2 * i].y += v.y;
             acc[2 * i + 1].x += v.z;
@@ -860,7 +895,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    SegIter it = seg_begin(sk, total, p.Kb, cid, ncl);
+    SegIter it = seg_begin(sk, total, p.Kb, cid, ncl, mu_lock);
     int t, kb0, kb1;
     while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
       for (int kb = kb0; kb < kb1; ++kb) {
