@@ -98,20 +98,20 @@ struct GemmParams {
 // contributors (see the lockstep grouping below when every tile is split).
 // Work is walked as segments: runs of K-blocks inside one tile.
 struct SegIter {
-  int64_t u, ue;   // stream-K part: next unit, end of this CTA's range (absolute units)
+  int64_t u, ue;   // stream-K part: next unit, end of this CTA's range (units of the split part)
   int t, t_end, step;  // whole-tile part: next tile, end, stride
-  int mu, r;       // stream-K tile of unit u: (u / Kb) * mu + r
+  int mu, r;       // stream-K tile of unit u: t_end + (u / Kb) * mu + r
 };
 // Stream-K geometry. Plain: G = CTAs contributors, one per CTA (mu = 1).
-// Lockstep (dense, every tile split): the CTAs form G = CTAs / mu groups of
-// mu = m_tiles; a group's contributor range runs over (N tile, K-block) units
-// and member r of the group computes M tile r of each, so the mu CTAs that
-// share a weight tile read each of its K-blocks at the same time (through L2,
-// once from DRAM) instead of at staggered offsets. CTAs past the last group
-// get no stream-K work.
+// Lockstep (dense tiles, numbered M-fastest): when the whole-tile prefix and
+// the split part are both whole multiples of mu = m_tiles, the CTAs form
+// G = CTAs / mu groups; a group's contributor range runs over the split
+// part's (N tile, K-block) units and member r of the group computes M tile r
+// of each, so the mu CTAs that share a weight tile read each of its K-blocks
+// at the same time (through L2, once from DRAM) instead of at staggered
+// offsets. CTAs past the last group get no stream-K work.
 struct SkGeo {
-  int dp_tiles;    // tiles handed out whole
-  int64_t U0;      // first stream-K unit (dp_tiles * Kb)
+  int dp_tiles;    // tiles handed out whole (the split part starts there)
   int64_t U;       // stream-K units per member (contributor unit space)
   int G, mu;
 };
@@ -121,11 +121,11 @@ BFP8_DEV SkGeo sk_geo(bool sk, int total, int Kb, int ncl, int mu_lock) {
   g.dp_tiles = sk ? (waves > 1 ? (waves - 1) * ncl : 0) : total;
   g.mu = 1;
   g.G = ncl;
-  if (sk && g.dp_tiles == 0 && mu_lock > 1 && mu_lock <= ncl && total % mu_lock == 0) {
+  if (sk && mu_lock > 1 && mu_lock <= ncl && g.dp_tiles % mu_lock == 0 &&
+      (total - g.dp_tiles) % mu_lock == 0) {
     g.mu = mu_lock;
     g.G = ncl / mu_lock;
   }
-  g.U0 = static_cast<int64_t>(g.dp_tiles) * Kb;
   g.U = static_cast<int64_t>((total - g.dp_tiles) / g.mu) * Kb;
   return g;
 }
@@ -143,8 +143,8 @@ BFP8_DEV SegIter seg_begin(bool sk, int total, int Kb, int cid, int ncl, int mu_
   it.r = cid % g.mu;
   const int v = cid / g.mu;
   const bool has = sk && v < g.G;
-  it.u = has ? g.U0 + sk_unit_begin(g.U, g.G, v) : 0;
-  it.ue = has ? g.U0 + sk_unit_begin(g.U, g.G, v + 1) : 0;
+  it.u = has ? sk_unit_begin(g.U, g.G, v) : 0;
+  it.ue = has ? sk_unit_begin(g.U, g.G, v + 1) : 0;
   return it;
 }
 BFP8_DEV bool next_seg(bool sk, SegIter& it, int total, int Kb, int& t, int& kb0, int& kb1) {
@@ -159,7 +159,7 @@ BFP8_DEV bool next_seg(bool sk, SegIter& it, int total, int Kb, int& t, int& kb0
   }
   if (it.u >= it.ue) return false;
   const int nt = static_cast<int>(it.u / Kb);
-  t = nt * it.mu + it.r;
+  t = it.t_end + nt * it.mu + it.r;
   kb0 = static_cast<int>(it.u - static_cast<int64_t>(nt) * Kb);
   const int64_t left = it.ue - it.u;
   kb1 = left < Kb - kb0 ? kb0 + static_cast<int>(left) : Kb;
@@ -438,9 +438,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
   // also needs every CTA to own at least one K-block unit of the split part.
   const int waves = (total + ncl - 1) / ncl;
   // Dense: last-wave fill < 85% (O at M=4096, 84%, gains 4%; QKV at 93% loses
-  // 2%). Grouped tiles are short and their split tiles cost more: < 80%.
-  const bool sparse_tail = waves > 0 && (GROUPED ? 5 * total < 4 * waves * ncl
-                                                 : 20 * total < 17 * waves * ncl);
+  // 2%; gate/up at 89%, plain or fused, gains nothing in the chain). Grouped
+  // tiles are short and their split tiles cost more: < 80%.
+  const int fill_pct = GROUPED ? 80 : 85;
+  const bool sparse_tail = waves > 0 && 100 * total < fill_pct * waves * ncl;
   const bool sk = CL == 1 && p.stream_k && sparse_tail &&
                   sk_geo(true, total, p.Kb, ncl, 0).U >= static_cast<int64_t>(ncl);
   // lockstep stream-K groups (dense tiles are numbered M-fastest)
@@ -747,7 +748,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
         const int64_t U = sg.U;
         const int G = sg.G;
         const int mu = sg.mu, r = cid % sg.mu;
-        const int64_t tile_u0 = static_cast<int64_t>((t - r) / mu) * p.Kb - sg.U0;
+        const int64_t tile_u0 = static_cast<int64_t>((t - sg.dp_tiles - r) / mu) * p.Kb;
         const int slot = (tile_u0 + kb0 == sk_unit_begin(U, G, cid / mu)) ? 0 : 1;
         // A partial tile is stored column-chunk-major ([BN/4][BM] float4s),
         // so each warp store (and each fixup load) covers 32 consecutive rows
