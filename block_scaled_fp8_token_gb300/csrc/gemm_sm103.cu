@@ -210,15 +210,24 @@ struct Cfg {
   static constexpr uint32_t kABytes = W8A16 ? BM * BK * 2 : BM * BK;
   static constexpr uint32_t kBRawBytes = BN * BK;
   static constexpr uint32_t kBConvBytes = W8A16 ? BN * BK * 2 : 0;
-  static constexpr uint32_t kStage = kABytes + kBRawBytes + kBConvBytes;
-  static constexpr uint32_t kTmaBytes = kABytes + kBRawBytes;
+  // W8A16 keeps three rings with their own barriers: A (BF16) in STAGES
+  // stages, the raw E4M3 B tile in kRawStages stages (freed as soon as the
+  // decode warps have read it) and the decoded BF16 B tile in kConvBufs
+  // buffers (freed by the MMA), so TMA, decode and MMA overlap. W8A8 stages
+  // hold A and B together.
+  static constexpr int kRawStages = W8A16 ? 2 : 0;
+  static constexpr int kConvBufs = W8A16 ? 2 : 0;
+  static constexpr uint32_t kStage = W8A16 ? kABytes : kABytes + kBRawBytes;
+  static constexpr uint32_t kTmaBytes = kStage;   // bytes one stage's TMA loads bring
+  static constexpr uint32_t kOffRaw = STAGES * kStage;
+  static constexpr uint32_t kOffConv = kOffRaw + kRawStages * kBRawBytes;
   static constexpr uint32_t kStgPitch = 80;  // 32 BF16 (64 B) + 16 B pad per row
   static constexpr uint32_t kStgWarp = 32 * kStgPitch;
   // TMEM (512 columns) holds 512/BN partial buffers, so the tensor cores run
   // up to that many K-blocks minus one ahead of the promotion.
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kNumBufs = 512 / BN;
-  static constexpr uint32_t kOffStg = STAGES * kStage;
+  static constexpr uint32_t kOffStg = kOffConv + kConvBufs * kBConvBytes;
   // Grouped and fused W8A8 instances: warp 2 (otherwise idle, on its own
   // sub-partition) computes each K-block's promotion factors s_a[m,kb] *
   // s_w[r,kb] for the tile's 128 rows into a ring of kFacSlots slots, two
@@ -232,7 +241,8 @@ struct Cfg {
   static constexpr uint32_t kFacBytes = 2 * BM * 4;
   static constexpr uint32_t kOffFac = kOffStg + kEpiWarps * kStgWarp;
   static constexpr uint32_t kOffBar = kOffFac + (kFacWarp ? kFacSlots * kFacBytes : 0);
-  static constexpr uint32_t kNumBars = 3 * STAGES + 2 * kNumBufs + 1 + 2 * kFacSlots;
+  static constexpr uint32_t kNumBars =
+      3 * STAGES + 2 * kNumBufs + 1 + 2 * kFacSlots + 2 * kRawStages + 2 * kConvBufs;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffOff = kOffMisc + 16;  // misc: TMEM slot, abort flag, last-arriver flag
   static constexpr uint32_t kOffPre = kOffOff + (kMaxExperts + 1) * 4;
@@ -383,7 +393,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
   const uint32_t bar0 = base + C::kOffBar;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto conv_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+  // (barriers 2*STAGES .. 3*STAGES-1 are unused)
   auto tfull_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + C::kNumBufs + b); };
   const uint32_t drain_bar = bar0 + 8u * (3 * STAGES + 2 * C::kNumBufs);
@@ -392,6 +402,14 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
     return bar0 + 8u * (3 * STAGES + 2 * C::kNumBufs + 1 + C::kFacSlots + f);
   };
   float* fac = reinterpret_cast<float*>(base_ptr + C::kOffFac);   // [slot][2][BM]
+  // W8A16 rings: raw E4M3 B stages and decoded BF16 B buffers
+  constexpr int kW16Bar0 = 3 * STAGES + 2 * C::kNumBufs + 1 + 2 * C::kFacSlots;
+  auto raw_full = [&](int r) { return bar0 + 8u * (kW16Bar0 + r); };
+  auto raw_empty = [&](int r) { return bar0 + 8u * (kW16Bar0 + C::kRawStages + r); };
+  auto cv_full = [&](int c) { return bar0 + 8u * (kW16Bar0 + 2 * C::kRawStages + c); };
+  auto cv_empty = [&](int c) {
+    return bar0 + 8u * (kW16Bar0 + 2 * C::kRawStages + C::kConvBufs + c);
+  };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::kOffMisc + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(base_ptr + C::kOffMisc + 8);
@@ -402,7 +420,6 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), CL);  // released by the MMA of every CTA that reads the stage
-      mbar_init(conv_bar(s), W8A16 ? C::kConvWarps : 1);
     }
     for (int b = 0; b < C::kNumBufs; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -412,6 +429,14 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
     for (int f = 0; f < C::kFacSlots; ++f) {
       mbar_init(ffull_bar(f), 32);              // every lane of the factor warp
       mbar_init(fempty_bar(f), C::kEpiWarps);
+    }
+    for (int r = 0; r < C::kRawStages; ++r) {
+      mbar_init(raw_full(r), 1);
+      mbar_init(raw_empty(r), C::kConvWarps);
+    }
+    for (int c = 0; c < C::kConvBufs; ++c) {
+      mbar_init(cv_full(c), C::kConvWarps);
+      mbar_init(cv_empty(c), 1);
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -492,7 +517,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
               }
             } else if (GROUPED) {
               tma_load_3d(sB, &tmB, kb * BK, tl.b_row0, tl.expert, full_bar(stage));
-            } else {
+            } else if (!W8A16) {
               tma_load_2d(sB, &tmB, kb * BK, tl.b_row0, full_bar(stage));
             }
             armed |= 1u << stage;
@@ -504,14 +529,37 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
         // No copy may still be landing in shared memory when the CTA exits.
         for (int s = 0; s < STAGES; ++s)
           if ((armed >> s) & 1u) wait_bounded(full_bar(s), (armed_phase >> s) & 1u, kDrainLimitNs);
+      } else if (W8A16 && lane == 1) {
+        // W8A16: the raw E4M3 B tiles, in their own ring
+        int rs = 0;
+        uint32_t rphase = 0, armed = 0, armed_phase = 0;
+        bool ok = true;
+        SegIter it = seg_begin(sk, total, p.Kb, cid, ncl, mu_lock);
+        int t, kb0, kb1;
+        while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
+          Tile tl;
+          decode_tile<C::kOutCols, CL, GROUPED>(p, s_off, s_pre, t, rank, tl);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait_sleep(raw_empty(rs), rphase ^ 1u, abort_flag)) { ok = false; break; }
+            const uint32_t sR = base + C::kOffRaw + rs * C::kBRawBytes;
+            mbar_arrive_expect_tx(raw_full(rs), C::kBRawBytes);
+            tma_load_2d(sR, &tmB, kb * BK, tl.b_row0, raw_full(rs));
+            armed |= 1u << rs;
+            armed_phase = (armed_phase & ~(1u << rs)) | (rphase << rs);
+            if (++rs == C::kRawStages) { rs = 0; rphase ^= 1u; }
+          }
+        }
+        if (!ok) raise_abort(abort_flag);
+        for (int r = 0; r < C::kRawStages; ++r)
+          if ((armed >> r) & 1u) wait_bounded(raw_full(r), (armed_phase >> r) & 1u, kDrainLimitNs);
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
       // The whole warp runs the loop (barrier waits, addresses) converged and
       // one elected lane issues the tcgen05 instructions and their commits; a
       // lone-lane loop issues them several times slower.
-      int stage = 0, buf = 0;
-      uint32_t phase = 0, bphase = 0;
+      int stage = 0, buf = 0, cs = 0;
+      uint32_t phase = 0, bphase = 0, cphase = 0;
       bool ok = true;
       SegIter it = seg_begin(sk, total, p.Kb, cid, ncl, mu_lock);
       int t, kb0, kb1;
@@ -525,7 +573,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
             ok = false;
             break;
           }
-          if (W8A16 && !__all_sync(0xffffffffu, mbar_wait_sleep(conv_bar(stage), phase, abort_flag))) {
+          if (W8A16 && !__all_sync(0xffffffffu, mbar_wait_sleep(cv_full(cs), cphase, abort_flag))) {
             ok = false;
             break;
           }
@@ -540,7 +588,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
               for (int k = 0; k < BK / 32; ++k)  // K = 32 bytes per MMA: +2 in 16-byte units
                 umma_e4m3(d, da + 2u * k, db + 2u * k, C::kIdesc, k > 0 ? 1u : 0u);
             } else {
-              const uint32_t sConv = sA + C::kABytes + C::kBRawBytes;
+              const uint32_t sConv = base + C::kOffConv + cs * C::kBConvBytes;
 #pragma unroll
               for (int k = 0; k < BK / 16; ++k) {  // K = 16 BF16 = 32 bytes per MMA
                 const int j = k >> 2, kk = k & 3;
@@ -553,11 +601,13 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
               umma_commit_mc(empty_bar(stage), 0x3);  // frees the stage in both CTAs
             else
               umma_commit(empty_bar(stage));
+            if (W8A16) umma_commit(cv_empty(cs));   // the decoded B buffer is free again
             umma_commit(tfull_bar(buf));
           }
           __syncwarp();
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           if (++buf == C::kNumBufs) { buf = 0; bphase ^= 1u; }
+          if (W8A16 && ++cs == C::kConvBufs) { cs = 0; cphase ^= 1u; }
         }
       }
       if (!ok) raise_abort(abort_flag);
@@ -893,17 +943,18 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
   } else {
     // ------------------------------------------------------------ E4M3 -> BF16 decode (W8A16)
     const int cw = warp - C::kEpiWarp0 - C::kEpiWarps;
-    int stage = 0;
-    uint32_t phase = 0;
+    int stage = 0, cs = 0;          // raw B stage, decoded B buffer
+    uint32_t phase = 0, cphase = 0;
     bool ok = true;
     SegIter it = seg_begin(sk, total, p.Kb, cid, ncl, mu_lock);
     int t, kb0, kb1;
     while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
       for (int kb = kb0; kb < kb1; ++kb) {
-        const bool w_ok = mbar_wait(full_bar(stage), phase, abort_flag);
+        const bool w_ok = mbar_wait(raw_full(stage), phase, abort_flag) &&
+                          mbar_wait(cv_empty(cs), cphase ^ 1u, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
-        const uint32_t sRaw = base + stage * C::kStage + C::kABytes;
-        const uint32_t sConv = sRaw + C::kBRawBytes;
+        const uint32_t sRaw = base + C::kOffRaw + stage * C::kBRawBytes;
+        const uint32_t sConv = base + C::kOffConv + cs * C::kBConvBytes;
         for (int idx = cw * 32 + lane; idx < BN * 8; idx += C::kConvWarps * 32) {
           const int r = idx >> 3, c = idx & 7;  // row, 16-byte chunk (16 K values)
           const uint4 raw = lds128(sRaw + r * 128 + c * 16);
@@ -919,8 +970,12 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(conv_bar(stage));
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        if (lane == 0) {
+          mbar_arrive(cv_full(cs));
+          mbar_arrive(raw_empty(stage));
+        }
+        if (++stage == C::kRawStages) { stage = 0; phase ^= 1u; }
+        if (++cs == C::kConvBufs) { cs = 0; cphase ^= 1u; }
       }
     }
     if (!ok) raise_abort(abort_flag);
@@ -1059,7 +1114,7 @@ int64_t member_tiles(const MemberTable& mt, int bn) {
 }  // namespace
 
 constexpr int kBN8 = 256, kStages8 = 4;
-constexpr int kBN16 = 128, kStages16 = 2;
+constexpr int kBN16 = 128, kStages16 = 3;   // A stages; raw and decoded B have their own rings
 
 size_t gemm_w8a8_workspace_bytes(int64_t M, int64_t N, const MemberTable& mt, int sms) {
   (void)N;
