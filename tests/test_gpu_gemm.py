@@ -134,8 +134,9 @@ def test_w8a8_vs_w8a16_accuracy_gate(bfp8, cuda_device):
     assert cos >= 0.999 and rrms <= 0.02
 
 
+@pytest.mark.parametrize("stream_k", [True, False], ids=["stream_k", "whole_tiles"])
 @pytest.mark.parametrize("which", ["gate_up", "down"])
-def test_w8a8_dense_ffn_full_size(bfp8, cuda_device, which):
+def test_w8a8_dense_ffn_full_size(bfp8, cuda_device, which, stream_k):
     qgu, sgu, qd, sd, xb = dense_ffn_weights(0)
     if which == "gate_up":
         q, s, members = qgu, sgu, [17408, 17408]
@@ -144,7 +145,7 @@ def test_w8a8_dense_ffn_full_size(bfp8, cuda_device, which):
         q, s, members = qd, sd, None
         h = bits16(synth.activations_bf16(synth.generator(77), 949, 17408))
         qa, sa = Q.act_quant_group(h)
-    y = gpu_bf16_to_f64(_w8a8(bfp8, cuda_device, qa, sa, q, s, members))
+    y = gpu_bf16_to_f64(_w8a8(bfp8, cuda_device, qa, sa, q, s, members, stream_k=stream_k))
     rows = sample_indices(qa.shape[0], 48, seed=1)
     cols = sample_indices(q.shape[0], 700, seed=2)
     ref = L.linear_w8a8(qa, sa, q, s, members, rows=rows, cols=cols)
@@ -180,3 +181,30 @@ def test_w8a16_dense_ffn_gate_up_full_size(bfp8, cuda_device):
     cols = sample_indices(34816, 400, seed=9)
     assert_close(y[np.ix_(rows, cols)],
                  L.linear_w8a16(xb, qgu, sgu, [17408, 17408], rows=rows, cols=cols), "w8a16 gu")
+
+
+@pytest.mark.parametrize("M,N,K,members", [
+    (949, 10240, 5120, [8192, 1024, 1024]),   # 320 tiles: 152 whole, then 168 split in 19 groups of 8
+    (1064, 5120, 2048, None),                 # 180 tiles, all split: 16 groups of 9, 8 CTAs idle
+])
+def test_w8a8_stream_k_lockstep_geometries(bfp8, cuda_device, M, N, K, members):
+    """Split tiles in lockstep groups (one CTA per M tile of an (N tile,
+    K-block) range): against the oracle on sampled rows and columns, within
+    two BF16 roundings of the whole-tile result everywhere, and
+    byte-identical from call to call."""
+    dev = cuda_device
+    xb, q, s = _problem(91 + M, M, N, K, members)
+    qa, sa = Q.act_quant_group(xb)
+    y1 = _w8a8(bfp8, dev, qa, sa, q, s, members)
+    y2 = _w8a8(bfp8, dev, qa, sa, q, s, members)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    yw = gpu_bf16_to_f64(_w8a8(bfp8, dev, qa, sa, q, s, members, stream_k=False))
+    y = gpu_bf16_to_f64(y1)
+    rows = sample_indices(M, 40, seed=M)
+    cols = sample_indices(N, 500, seed=N)
+    assert_close(y[np.ix_(rows, cols)], L.linear_w8a8(qa, sa, q, s, members, rows=rows, cols=cols),
+                 f"lockstep stream-K {M}x{N}x{K}")
+    # both results are BF16 roundings (unit roundoff 2^-8 each) of FP32 sums
+    # that differ only in summation order: at most 2^-7 apart, relatively
+    rms = float(np.sqrt(np.mean(yw ** 2)))
+    assert np.all(np.abs(y - yw) <= 2.0 ** -7 * np.abs(yw) + 1e-4 * rms), "stream-K vs whole tiles"
