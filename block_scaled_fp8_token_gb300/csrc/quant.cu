@@ -32,10 +32,12 @@ constexpr int kThreads = 256;
 constexpr int kQuad = 4;
 constexpr int kChunks = 4;
 
-// row[c .. c+8) as four bf16x2 words, zero past K.
+// row[c .. c+8) as four bf16x2 words, zero past K. FULL: the caller knows the
+// chunk is in range and 16-byte aligned.
+template <bool FULL>
 __device__ __forceinline__ void load_chunk(const __nv_bfloat16* row, int64_t c, int64_t K,
                                            bool vec, uint32_t (&w)[4]) {
-  if (vec && c + 8 <= K) {
+  if (FULL || (vec && c + 8 <= K)) {
     const uint4 raw = __ldg(reinterpret_cast<const uint4*>(row + c));
     w[0] = raw.x;
     w[1] = raw.y;
@@ -70,7 +72,9 @@ __device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w 
 // For finite inputs the codes and scales equal the CPU definition bit for bit:
 // the group maximum is exact (taken on the BF16 bit patterns of |x|, or on the
 // BF16-rounded h), and every quotient is the correctly rounded x / s.
-template <bool SILU>
+// FULL: K is a multiple of 128 and every row and pitch is aligned for 16-byte
+// loads and 8-byte stores, so no chunk needs a bounds or alignment test.
+template <bool SILU, bool FULL>
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K, int64_t ld,
     uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s, int64_t ssm, int64_t sskb,
@@ -98,8 +102,8 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(
         uint32_t u[4] = {0u, 0u, 0u, 0u};
         a[i][0] = a[i][1] = a[i][2] = a[i][3] = 0u;
         if (ok) {
-          load_chunk(row, c0 + 32 * i, K, vec_in, a[i]);
-          load_chunk(row + K, c0 + 32 * i, K, vec_in, u);
+          load_chunk<FULL>(row, c0 + 32 * i, K, vec_in, a[i]);
+          load_chunk<FULL>(row + K, c0 + 32 * i, K, vec_in, u);
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -115,7 +119,7 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(
 #pragma unroll
       for (int i = 0; i < kChunks; ++i) {
         a[i][0] = a[i][1] = a[i][2] = a[i][3] = 0u;
-        if (ok) load_chunk(row, c0 + 32 * i, K, vec_in, a[i]);
+        if (ok) load_chunk<FULL>(row, c0 + 32 * i, K, vec_in, a[i]);
 #pragma unroll
         for (int j = 0; j < 4; ++j) mx = max_u16x2(mx, a[i][j] & 0x7FFF7FFFu);
       }
@@ -143,7 +147,7 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(
       const uint32_t w1 = static_cast<uint32_t>(p[2]) | (static_cast<uint32_t>(p[3]) << 16);
       const int64_t c = c0 + 32 * i;
       if (!live) continue;
-      if (vec_out && c + 8 <= K) {
+      if (FULL || (vec_out && c + 8 <= K)) {
         *reinterpret_cast<uint2*>(qrow + c) = make_uint2(w0, w1);
       } else {
 #pragma unroll
@@ -337,22 +341,25 @@ int act_quant_common(bool silu, const void* x, int64_t M, int64_t K, int64_t ld,
   if (rc != BFP8_OK) return rc;
   const int vec_in = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (ld % 8 == 0) && (K % 8 == 0);
   const int vec_out = (reinterpret_cast<uintptr_t>(q) % 8 == 0) && (ldq % 8 == 0);
-  static const int per_sm[2] = {resident_blocks(act_quant_kernel<false>),
-                                resident_blocks(act_quant_kernel<true>)};
+  const bool full = vec_in && vec_out && K % 128 == 0;
+  static const int per_sm[4] = {
+      resident_blocks(act_quant_kernel<false, false>), resident_blocks(act_quant_kernel<true, false>),
+      resident_blocks(act_quant_kernel<false, true>), resident_blocks(act_quant_kernel<true, true>)};
   const int64_t items = M * Kb;
   const int64_t per_block = kThreads / kQuad;   // groups one block covers per pass
   const int64_t want = (items + per_block - 1) / per_block;
-  const int64_t cap = static_cast<int64_t>(sms) * per_sm[silu ? 1 : 0];
+  const int64_t cap = static_cast<int64_t>(sms) * per_sm[(silu ? 1 : 0) + (full ? 2 : 0)];
   const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto go = [&](auto kernel) {
+    kernel<<<blocks, kThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(x), M, K, ld,
+                                         static_cast<uint8_t*>(q), ldq, s, ssm, sskb, vec_in,
+                                         vec_out, rows, rows ? n_src : M);
+  };
   if (silu)
-    act_quant_kernel<true><<<blocks, kThreads, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(x), M, K, ld, static_cast<uint8_t*>(q), ldq, s, ssm,
-        sskb, vec_in, vec_out, rows, rows ? n_src : M);
+    full ? go(act_quant_kernel<true, true>) : go(act_quant_kernel<true, false>);
   else
-    act_quant_kernel<false><<<blocks, kThreads, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(x), M, K, ld, static_cast<uint8_t*>(q), ldq, s, ssm,
-        sskb, vec_in, vec_out, rows, rows ? n_src : M);
+    full ? go(act_quant_kernel<false, true>) : go(act_quant_kernel<false, false>);
   return check_launch();
 }
 
