@@ -147,6 +147,25 @@ BFP8_DEV float2 f16x2_bits_to_f32x2(uint32_t h) {
 BFP8_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 BFP8_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Launches `kernel` as a programmatic dependent of the previous work on the
+// stream: it may start before that work ends, so it must griddepcontrol.wait
+// before touching anything the previous work reads or writes.
+template <typename Kernel, typename... Args>
+int launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+               Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? BFP8_OK : BFP8_ERR_CUDA;
+}
+
 // One CTA per K-block, 64 threads: thread t handles token t / 4 and the 32
 // values [32*(t%4), +32) of the block. Writes the hi/lo E4M3 rows of the
 // block's 32 x 128 token tile (row-major; TMA applies the swizzle on load)
@@ -182,6 +201,9 @@ __global__ void __launch_bounds__(64) gemv_split_tokens_kernel(
     uint8_t* __restrict__ xtile, float* __restrict__ xinv, int32_t* __restrict__ counters,
     int32_t n_counters) {
   pdl_launch_dependents();  // let the GEMV start streaming weights now
+  // This kernel may start while the previous GEMV (which reads the same
+  // workspace, or wrote x) is still running: wait for it before any access.
+  pdl_wait();
   const int kb = blockIdx.x;
   for (int i = kb * 64 + threadIdx.x; i < n_counters; i += gridDim.x * 64) counters[i] = 0;
   const int tok = threadIdx.x >> 2, q4 = threadIdx.x & 3;
@@ -239,6 +261,7 @@ __global__ void __launch_bounds__(64) gemv_split_tokens_kernel(
 __global__ void __launch_bounds__(256) gemv_clear_counters_kernel(int32_t* __restrict__ counters,
                                                                  int32_t n) {
   pdl_launch_dependents();
+  pdl_wait();   // the previous GEMV may still be using the counters
   for (int i = threadIdx.x; i < n; i += 256) counters[i] = 0;
 }
 
@@ -253,6 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - raw_u32);
+  // The next call's first kernel (token split or counter clear) may launch
+  // now; it waits for this grid before touching the workspace, and the next
+  // GEMV's CTAs take SMs as this grid's CTAs leave and stream their weights.
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t bar0 = base + kOffBar;
@@ -329,9 +356,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(base + (g * kGroup + j) * kStage, &tmW, kb * 128, rt * kRows, full_bar(g));
           }
         }
-        // the W8A16 arm's token tiles come from the split kernel this grid
-        // depends on; the W8A8 arm's tokens come from the caller
-        if (!W8A8 && !tokens_ready) {
+        // the token tiles (W8A16: from the split kernel this grid depends on;
+        // W8A8: from the caller, ordered before the counter clear this grid
+        // depends on) are read only after the dependency wait
+        if (!tokens_ready) {
           pdl_wait();
           tokens_ready = true;
         }
@@ -538,6 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) raise_abort(abort_flag);
   } else if (warp == kPublisherWarp) {
     // ------------------------------------------------------------ arrivals
+    pdl_wait();  // the counters belong to the previous call until its grid ends
     // For each split tile of this CTA (at most two: the first and the last
     // segment), once the epilogue has written its partial: one acquire-release
     // atomic on the tile's counter publishes the partial (cumulative release
@@ -583,13 +612,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 int launch_kernels(const void* x, int64_t ldx, uint8_t* xtile, float* xinv, const CUtensorMap& tw,
                    const CUtensorMap& tx, const GemvParams& p, void* stream, bool silu = false) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (silu)
-    gemv_split_tokens_kernel<true><<<p.Kb, 64, 0, st>>>(static_cast<const __nv_bfloat16*>(x), ldx,
-                                                        p.M, p.K, xtile, xinv, p.counters, p.RT);
-  else
-    gemv_split_tokens_kernel<false><<<p.Kb, 64, 0, st>>>(static_cast<const __nv_bfloat16*>(x), ldx,
-                                                         p.M, p.K, xtile, xinv, p.counters, p.RT);
-  int rc = check_launch();
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  int rc = silu ? launch_pdl(gemv_split_tokens_kernel<true>, dim3(p.Kb), dim3(64), 0, st, xb, ldx,
+                             p.M, p.K, xtile, xinv, p.counters, p.RT)
+                : launch_pdl(gemv_split_tokens_kernel<false>, dim3(p.Kb), dim3(64), 0, st, xb, ldx,
+                             p.M, p.K, xtile, xinv, p.counters, p.RT);
+  if (rc != BFP8_OK) return rc;
+  rc = check_launch();
   if (rc != BFP8_OK) return rc;
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel<false>), kSmemBytes);
   if (rc != BFP8_OK) return rc;
@@ -720,7 +749,8 @@ int launch_gemv_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t s
                     CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != BFP8_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  gemv_clear_counters_kernel<<<1, 256, 0, st>>>(p.counters, p.RT);
+  rc = launch_pdl(gemv_clear_counters_kernel, dim3(1), dim3(256), 0, st, p.counters, p.RT);
+  if (rc != BFP8_OK) return rc;
   rc = check_launch();
   if (rc != BFP8_OK) return rc;
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel<true>), kSmemBytes);
