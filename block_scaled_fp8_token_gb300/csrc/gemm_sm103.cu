@@ -449,7 +449,16 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
-  if (GROUPED && warp == C::kEpiWarp0) build_schedule<CL>(p, s_off, s_pre, lane);
+  // This grid runs as a programmatic dependent of the previous kernel on the
+  // stream: let the next one launch (it waits for this grid before touching
+  // what this grid reads or writes), and read nothing the previous kernels
+  // wrote (activations, their scales, the expert offsets) and write no output
+  // before griddepcontrol.wait. Weights and on-chip setup come first.
+  pdl_launch_dependents();
+  if (GROUPED && warp == C::kEpiWarp0) {
+    pdl_wait();
+    build_schedule<CL>(p, s_off, s_pre, lane);
+  }
   tc_fence_before();
   __syncthreads();
   // The peer CTA multicasts into this CTA's shared memory and arrives on its
@@ -481,6 +490,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
         int stage = 0;
         uint32_t phase = 0, armed = 0, armed_phase = 0;
         bool ok = true;
+        bool a_ready = false;    // activations are read only after the dependency wait
         SegIter it = seg_begin(sk, total, p.Kb, cid, ncl, mu_lock);
         int t, kb0, kb1;
         while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
@@ -491,6 +501,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
             const uint32_t sA = base + stage * C::kStage;
             const uint32_t sB = sA + C::kABytes;
             mbar_arrive_expect_tx(full_bar(stage), C::kTmaBytes);
+            if (!a_ready) {
+              pdl_wait();
+              a_ready = true;
+            }
             if (W8A16) {
               tma_load_2d(sA, &tmA, kb * BK, tl.a_row0, full_bar(stage));
               tma_load_2d(sA + BM * 128, &tmA, kb * BK + 64, tl.a_row0, full_bar(stage));
@@ -618,6 +632,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
       wait_bounded(drain_bar, 0, kDrainLimitNs);
     } else if (C::kFacWarp && warp == 2) {
       // ------------------------------------------------------------ factors
+      pdl_wait();
       // Walks the epilogue's segments in the same order. Lane l fills rows
       // l, l+32, l+64, l+96 of each slot; rows past the tile get 0.
       const uint16_t* fsw16 = static_cast<const uint16_t*>(p.s_w);
@@ -662,6 +677,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
   } else if (warp < C::kEpiWarp0 + C::kEpiWarps) {
     if constexpr (C::kSplitRegs) warpgroup_reg_alloc<C::kEpiRegs>();
     // ------------------------------------------------------------ promotion + epilogue
+    pdl_wait();
     const int ew = warp - C::kEpiWarp0;
     const int q = warp & 3;
     const int h = ew >> 2;
@@ -1011,16 +1027,18 @@ int launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, in
   int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel), C::kSmemBytes);
   if (rc != BFP8_OK) return rc;
   cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C::kCluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see the kernel's first wait
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = static_cast<cudaStream_t>(stream);
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;   // occupancy query: cluster shape only
   // persistent: at most as many clusters as can be resident at once
   int max_clusters = 0;
   cfg.gridDim = dim3(C::kCluster);
@@ -1030,6 +1048,7 @@ int launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, in
   if (p.stream_k) items = static_cast<int64_t>(work_items) * p.Kb;  // stream-K splits by K-block units
   const int clusters = items < max_clusters ? static_cast<int>(items) : max_clusters;
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * C::kCluster));
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, p) != cudaSuccess) return BFP8_ERR_CUDA;
   return check_launch();
 }

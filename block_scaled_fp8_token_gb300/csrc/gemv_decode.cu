@@ -144,8 +144,6 @@ BFP8_DEV float2 f16x2_bits_to_f32x2(uint32_t h) {
   return __half22float2(*reinterpret_cast<const __half2*>(&h));
 }
 
-BFP8_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-BFP8_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Launches `kernel` as a programmatic dependent of the previous work on the
 // stream: it may start before that work ends, so it must griddepcontrol.wait

@@ -22,6 +22,12 @@ BFP8_DEV uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch: let the next kernel on the stream launch
+// now (it waits for this grid before touching shared data), and wait for the
+// grids this one depends on (their memory operations become visible).
+BFP8_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+BFP8_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 BFP8_DEV uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

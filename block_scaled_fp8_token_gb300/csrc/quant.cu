@@ -79,6 +79,9 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K, int64_t ld,
     uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s, int64_t ssm, int64_t sskb,
     int vec_in, int vec_out, const int32_t* __restrict__ rows, int64_t n_src) {
+  // a programmatic dependent of the previous kernel: wait before any access
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t Kb = (K + 127) / 128;
   const int ql = threadIdx.x & (kQuad - 1);
   const int64_t quad = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / kQuad;
@@ -239,6 +242,9 @@ __global__ void __launch_bounds__(kThreads) moe_combine_kernel(
     const __nv_bfloat16* __restrict__ y, int64_t R, int64_t H, int64_t ldy,
     const int32_t* __restrict__ rows, const float* __restrict__ w, int64_t T, int topk,
     __nv_bfloat16* __restrict__ out, int64_t ldo, int vec) {
+  // a programmatic dependent of the previous kernel: wait before any access
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t hc = (H + 7) / 8;
   const int64_t it0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -312,6 +318,22 @@ __global__ void __launch_bounds__(kThreads) moe_combine_kernel(
   }
 }
 
+// Launch as a programmatic dependent of the previous work on the stream (the
+// kernels wait for it before any memory access).
+template <typename Kernel, typename... Args>
+int launch_dependent(Kernel kernel, unsigned blocks, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? BFP8_OK : BFP8_ERR_CUDA;
+}
+
 // Blocks of kThreads that one SM keeps resident for `kernel` (at least 1):
 // the grid-stride kernels launch exactly one wave of them.
 template <typename Kernel>
@@ -352,14 +374,13 @@ int act_quant_common(bool silu, const void* x, int64_t M, int64_t K, int64_t ld,
   const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   auto go = [&](auto kernel) {
-    kernel<<<blocks, kThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(x), M, K, ld,
-                                         static_cast<uint8_t*>(q), ldq, s, ssm, sskb, vec_in,
-                                         vec_out, rows, rows ? n_src : M);
+    return launch_dependent(kernel, blocks, st, static_cast<const __nv_bfloat16*>(x), M, K, ld,
+                            static_cast<uint8_t*>(q), ldq, s, ssm, sskb, vec_in, vec_out, rows,
+                            rows ? n_src : M);
   };
-  if (silu)
-    full ? go(act_quant_kernel<true, true>) : go(act_quant_kernel<true, false>);
-  else
-    full ? go(act_quant_kernel<false, true>) : go(act_quant_kernel<false, false>);
+  const int lrc = silu ? (full ? go(act_quant_kernel<true, true>) : go(act_quant_kernel<true, false>))
+                       : (full ? go(act_quant_kernel<false, true>) : go(act_quant_kernel<false, false>));
+  if (lrc != BFP8_OK) return lrc;
   return check_launch();
 }
 
@@ -400,9 +421,11 @@ int launch_moe_combine(const void* y, int64_t R, int64_t H, int64_t ldy, const i
   const int64_t want = (items + kThreads - 1) / kThreads;
   const int64_t cap = static_cast<int64_t>(sms) * per_sm;
   const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
-  moe_combine_kernel<<<blocks, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const __nv_bfloat16*>(y), R, H, ldy, token_rows, token_weights, T, topk,
-      static_cast<__nv_bfloat16*>(out), ldo, vec);
+  rc = launch_dependent(moe_combine_kernel, blocks, static_cast<cudaStream_t>(stream),
+                        static_cast<const __nv_bfloat16*>(y), R, H, ldy, token_rows,
+                        token_weights, T, static_cast<int>(topk),
+                        static_cast<__nv_bfloat16*>(out), ldo, vec);
+  if (rc != BFP8_OK) return rc;
   return check_launch();
 }
 
