@@ -388,6 +388,21 @@ BFP8_DEV void sts128(uint32_t addr, uint4 v) {
                : "memory");
 }
 
+// TMA tensor store of one box from shared memory (bulk-group completion):
+// the coordinates are the box's first element; elements outside the tensor
+// are not written. The issuing thread tracks its stores as bulk groups:
+// commit closes a group; wait_group.read 0 returns once every committed group
+// has finished reading shared memory (the source may be rewritten),
+// wait_group 0 once their global writes are complete.
+BFP8_DEV void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+BFP8_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+BFP8_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+BFP8_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Named barrier over a subset of warps (id 0 is __syncthreads).
 BFP8_DEV void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
