@@ -82,3 +82,30 @@ def test_grouped_moe_workload(bfp8, cuda_device):
     cols = np.unique(np.concatenate([rng.choice(2048, 64, replace=False), [0, 2047]]))
     assert_close(yd[np.ix_(rows, cols)],
                  L.grouped_linear_w8a8(qh, sh, qd, sd, offsets, rows=rows, cols=cols), "moe down")
+
+
+@pytest.mark.parametrize("pad", [8, 3], ids=["ldy_aligned", "ldy_unaligned"])
+def test_grouped_strided_output_keeps_padding(bfp8, cuda_device, pad):
+    """y as a row-strided view: with a 16-byte aligned row pitch, whole
+    32-row warp tiles go out by TMA tensor stores (clipped at column N), the
+    rows of an expert's last partial group by the masked warp stores; with an
+    unaligned pitch every store is a masked warp store. Either way the
+    padding columns and nothing else stay untouched. Expert sizes put tile
+    and 32-row boundaries on both sides of the split."""
+    dev = cuda_device
+    offsets = [0, 32, 96, 96, 224, 385, 386, 514]
+    G, N, K = 7, 320, 384
+    g = synth.generator(43)
+    qw, sw = _stack_quant(synth.weight_stack_f32(g, G, N, K).numpy())
+    xb = bits16(synth.activations_bf16(g, offsets[-1], K))
+    qa, sa = Q.act_quant_group(xb)
+    T = offsets[-1]
+    yb = torch.full((T, N + pad), float("nan"), dtype=torch.bfloat16, device=dev)
+    y = yb[:, :N]
+    off = torch.from_numpy(np.asarray(offsets, dtype=np.int32)).to(dev)
+    bfp8.bfp8_grouped_linear(to_dev_u8(qa, dev), torch.from_numpy(sa).to(dev), to_dev_u8(qw, dev),
+                             scale_to_dev(sw, dev), off, y)
+    torch.cuda.synchronize()
+    assert bfp8.bfp8_device_status() == 0
+    assert torch.isnan(yb[:, N:].float()).all()
+    assert_close(gpu_bf16_to_f64(y), L.grouped_linear_w8a8(qa, sa, qw, sw, offsets), f"grouped pad {pad}")
