@@ -27,6 +27,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 from pathlib import Path
 
@@ -158,12 +159,15 @@ def parse_clock_samples(lines, t_begin=None, t_end=None) -> dict:
 
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples, kept only while the timed
-    region runs (begin() / end() mark it)."""
+    region runs (begin() / end() mark it). The raw samples go to
+    $BFP8_CLOCK_LOG if set, else to a file in the system temporary folder."""
 
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
-        self.path = ROOT / "gpurun_out" / f"clocks_bench_{os.getpid()}.csv"
+        env = os.environ.get("BFP8_CLOCK_LOG")
+        self.path = (Path(env) if env else
+                     Path(tempfile.gettempdir()) / f"bfp8_clocks_{os.getpid()}.csv")
         self.t_begin = self.t_end = None
 
     def start(self):
