@@ -124,10 +124,14 @@ def _check(status: int, where: str) -> None:
 
 
 def _ptr(t) -> int | None:
+    """A tensor's device address. Every pointer the library takes is device
+    memory; a host tensor is refused here, before any kernel could read it."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_cuda:
+        raise ValueError(f"bfp8: expected a CUDA tensor, got one on {t.device}")
     return t.data_ptr()
 
 

@@ -64,3 +64,20 @@ def test_argument_errors_without_gpu(bfp8):
     rows = (ctypes.c_int64 * 2)(3, 3)
     mem = bfp8.bfp8_members(2, rows)
     assert lib.bfp8_linear_w8a8(p, p, 1, 1, p, p, 3, 4, 8, 16, p, 8, ctypes.byref(mem), None, 0, None) == 11
+
+
+def test_binding_refuses_host_tensors(bfp8):
+    """A host tensor never reaches the library: the kernels would read its
+    address as device memory."""
+    import torch
+
+    x = torch.zeros(4, 128, dtype=torch.bfloat16)
+    q = torch.empty(4, 128, dtype=torch.uint8)
+    s = torch.empty(4, 1, dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        bfp8.bfp8_act_quant_group(x, q, s)
+    w = torch.zeros(128, 128, dtype=torch.uint8)
+    sw = torch.ones(1, 1, dtype=torch.bfloat16)
+    y = torch.empty(4, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        bfp8.bfp8_linear_w8a8(q, s, w, sw, y)
