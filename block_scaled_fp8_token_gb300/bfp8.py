@@ -124,14 +124,18 @@ def _check(status: int, where: str) -> None:
 
 
 def _ptr(t) -> int | None:
-    """A tensor's device address. Every pointer the library takes is device
-    memory; a host tensor is refused here, before any kernel could read it."""
+    """A tensor's device address. Every pointer the library takes is memory of
+    the current device; a host tensor, or one on another GPU, is refused here,
+    before any kernel could read it."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
     if not t.is_cuda:
         raise ValueError(f"bfp8: expected a CUDA tensor, got one on {t.device}")
+    if t.get_device() != torch.cuda.current_device():
+        raise ValueError(f"bfp8: tensor on {t.device}, but the current device is "
+                         f"cuda:{torch.cuda.current_device()}")
     return t.data_ptr()
 
 
