@@ -205,6 +205,10 @@ def bfp8_act_quant_group(x, q, scales, s_stride_m=None, s_stride_kb=None, stream
     M, K = x.shape
     ssm = scales.stride(0) if s_stride_m is None else s_stride_m
     sskb = scales.stride(1) if s_stride_kb is None else s_stride_kb
+    _span(x, "x", M, K, x.stride(0), 1, 2)
+    _out(q, "q", M, K, 1)
+    _scales_out(scales, "scales", M, -(-K // 128), ssm, sskb,
+                s_stride_m is not None or s_stride_kb is not None)
     _check(_lib.bfp8_act_quant_group(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0),
                                      _ptr(scales), ssm, sskb, _stream(stream)),
            "bfp8_act_quant_group")
@@ -214,6 +218,10 @@ def bfp8_silu_mul_act_quant(gu, q, scales, s_stride_m=None, s_stride_kb=None, st
     M, two_i = gu.shape
     ssm = scales.stride(0) if s_stride_m is None else s_stride_m
     sskb = scales.stride(1) if s_stride_kb is None else s_stride_kb
+    _span(gu, "gu", M, two_i, gu.stride(0), 1, 2)
+    _out(q, "q", M, two_i // 2, 1)
+    _scales_out(scales, "scales", M, -(-(two_i // 2) // 128), ssm, sskb,
+                s_stride_m is not None or s_stride_kb is not None)
     _check(_lib.bfp8_silu_mul_act_quant(_ptr(gu), M, two_i // 2, gu.stride(0), _ptr(q),
                                         q.stride(0), _ptr(scales), ssm, sskb, _stream(stream)),
            "bfp8_silu_mul_act_quant")
@@ -221,9 +229,70 @@ def bfp8_silu_mul_act_quant(gu, q, scales, s_stride_m=None, s_stride_kb=None, st
 
 def bfp8_quantize_weight_block(w, q, scale, stream=None) -> None:
     N, K = w.shape
+    _span(w, "w", N, K, w.stride(0), 1, 4)  # float32, as the library reads it
+    _out(q, "q", N, K, 1)
+    _grid_span(scale, "scale", -(-N // 128), -(-K // 128))
     _check(_lib.bfp8_quantize_weight_block(_ptr(w), N, K, w.stride(0), _ptr(q), q.stride(0),
                                            _ptr(scale), _scale_dtype(scale), _stream(stream)),
            "bfp8_quantize_weight_block")
+
+
+def _span(t, name: str, rows: int, cols: int, rs: int, cs: int, elem_bytes: int) -> None:
+    """Refuse a call that would make the library touch memory past the end of
+    t's storage: rows x cols elements of elem_bytes bytes at element strides
+    (rs, cs) from t's first element, as the library addresses them."""
+    if t is None or isinstance(t, int) or rows <= 0 or cols <= 0:
+        return
+    if rs < 0 or cs < 0:
+        raise ValueError(f"bfp8: {name}: negative stride ({rs}, {cs})")
+    need = ((rows - 1) * rs + (cols - 1) * cs + 1) * elem_bytes
+    if need <= t.numel() * t.element_size() and t.is_contiguous():
+        return  # within the tensor's own elements
+    st = t.untyped_storage()
+    if t.data_ptr() + need > st.data_ptr() + st.nbytes():
+        raise ValueError(f"bfp8: {name} is too small for the call: {rows} x {cols} elements "
+                         f"at strides ({rs}, {cs}) reach past its storage")
+
+
+def _out(t, name: str, rows: int, cols: int, elem_bytes: int) -> None:
+    """An output the library writes as rows x cols row-major elements at
+    t.stride(0): the view must cover them, not only its storage."""
+    if rows <= 0 or cols <= 0:
+        return
+    if t.dim() != 2 or t.shape[0] < rows or t.shape[1] < cols:
+        raise ValueError(f"bfp8: {name} is too small for the call: needs [{rows}, {cols}], "
+                         f"got {list(t.shape)}")
+    _span(t, name, rows, cols, t.stride(0), 1, elem_bytes)
+
+
+def _scales_out(t, name: str, rows: int, cols: int, s_m: int, s_kb: int, explicit: bool) -> None:
+    """A float32 scale output [rows, cols]: with the view's own strides the
+    view must cover it; with caller strides (for example token-contiguous
+    scales) only the storage can be checked."""
+    if not explicit and rows > 0 and cols > 0 and (
+            t.dim() != 2 or t.shape[0] < rows or t.shape[1] < cols):
+        raise ValueError(f"bfp8: {name} is too small for the call: needs [{rows}, {cols}], "
+                         f"got {list(t.shape)}")
+    _span(t, name, rows, cols, s_m, s_kb, 4)
+
+
+_SCALE_BYTES = {BFP8_DT_BF16: 2, BFP8_DT_F16: 2, BFP8_DT_F32: 4}
+
+
+def _grid_span(t, name: str, rows: int, kb: int, experts: int = 1) -> None:
+    """A weight-scale argument: `experts` contiguous [rows, kb] block grids, or
+    one multiplier per expert (a tensor of rank 0 or 1)."""
+    eb = _SCALE_BYTES.get(_scale_dtype(t) & 0xFF)
+    if eb is None:
+        return  # refused by the library (SCALE_DTYPE) before anything is read
+    if t.dim() <= 1:
+        _span(t, name, experts, 1, 1, 1, eb)
+    else:
+        _span(t, name, experts * rows, kb, kb, 1, eb)
+
+
+def _scale_rows(N: int, member_rows) -> int:
+    return sum(-(-int(m) // 128) for m in member_rows) if member_rows else -(-N // 128)
 
 
 def _ws(workspace):
@@ -243,6 +312,12 @@ def bfp8_linear_w8a8(q_a, s_a, w, w_scale, y, member_rows=None, s_stride_m=None,
     N = w.shape[0]
     ssm = s_a.stride(0) if s_stride_m is None else s_stride_m
     sskb = s_a.stride(1) if s_stride_kb is None else s_stride_kb
+    Kb = -(-K // 128)
+    _span(q_a, "q_a", M, K, K, 1, 1)
+    _span(s_a, "s_a", M, Kb, ssm, sskb, 4)
+    _span(w, "w", N, K, K, 1, 1)
+    _grid_span(w_scale, "w_scale", _scale_rows(N, member_rows), Kb)
+    _out(y, "y", M, N, 2)
     mref, _keep = _members(member_rows)
     wsp, wsb = _ws(workspace)
     _check(_lib.bfp8_linear_w8a8(_ptr(q_a), _ptr(s_a), ssm, sskb, _ptr(w), _ptr(w_scale),
@@ -254,6 +329,10 @@ def bfp8_linear_w8a8(q_a, s_a, w, w_scale, y, member_rows=None, s_stride_m=None,
 def bfp8_linear_w8a16(x, w, w_scale, y, member_rows=None, stream=None) -> None:
     M, K = x.shape
     N = w.shape[0]
+    _span(x, "x", M, K, x.stride(0), 1, 2)
+    _span(w, "w", N, K, K, 1, 1)
+    _grid_span(w_scale, "w_scale", _scale_rows(N, member_rows), -(-K // 128))
+    _out(y, "y", M, N, 2)
     mref, _keep = _members(member_rows)
     _check(_lib.bfp8_linear_w8a16(_ptr(x), x.stride(0), _ptr(w), _ptr(w_scale),
                                   _scale_dtype(w_scale), M, N, K, _ptr(y), y.stride(0), mref,
@@ -268,6 +347,10 @@ def bfp8_gemv_decode_workspace(M: int, N: int, K: int) -> int:
 def bfp8_gemv_decode(x, w, w_scale, y, workspace, member_rows=None, stream=None) -> None:
     M, K = x.shape
     N = w.shape[0]
+    _span(x, "x", M, K, x.stride(0), 1, 2)
+    _span(w, "w", N, K, K, 1, 1)
+    _grid_span(w_scale, "w_scale", _scale_rows(N, member_rows), -(-K // 128))
+    _out(y, "y", M, N, 2)
     mref, _keep = _members(member_rows)
     _check(_lib.bfp8_gemv_decode(_ptr(x), x.stride(0), _ptr(w), _ptr(w_scale),
                                  _scale_dtype(w_scale), M, N, K, _ptr(y), y.stride(0), mref,
@@ -283,6 +366,12 @@ def bfp8_gemv_decode_w8a8(q_a, s_a, w, w_scale, y, workspace, member_rows=None, 
     N = w.shape[0]
     ssm = s_a.stride(0) if s_stride_m is None else s_stride_m
     sskb = s_a.stride(1) if s_stride_kb is None else s_stride_kb
+    Kb = -(-K // 128)
+    _span(q_a, "q_a", M, K, K, 1, 1)
+    _span(s_a, "s_a", M, Kb, ssm, sskb, 4)
+    _span(w, "w", N, K, K, 1, 1)
+    _grid_span(w_scale, "w_scale", _scale_rows(N, member_rows), Kb)
+    _out(y, "y", M, N, 2)
     mref, _keep = _members(member_rows)
     _check(_lib.bfp8_gemv_decode_w8a8(_ptr(q_a), _ptr(s_a), ssm, sskb, _ptr(w), _ptr(w_scale),
                                       _scale_dtype(w_scale), M, N, K, _ptr(y), y.stride(0), mref,
@@ -297,6 +386,10 @@ def bfp8_gemv_decode_noalloc(x, w, w_scale, y, member_rows=None, stream=None) ->
     allocate device memory; its scratch is a fixed array inside the library."""
     M, K = x.shape
     N = w.shape[0]
+    _span(x, "x", M, K, x.stride(0), 1, 2)
+    _span(w, "w", N, K, K, 1, 1)
+    _grid_span(w_scale, "w_scale", _scale_rows(N, member_rows), -(-K // 128))
+    _out(y, "y", M, N, 2)
     mref, _keep = _members(member_rows)
     _check(_lib.bfp8_gemv_decode_noalloc(_ptr(x), x.stride(0), _ptr(w), _ptr(w_scale),
                                          _scale_dtype(w_scale), M, N, K, _ptr(y), y.stride(0),
@@ -314,6 +407,13 @@ def bfp8_grouped_linear(q_a, s_a, w, w_scale, offsets, y, s_stride_m=None, s_str
     G, N = w.shape[0], w.shape[1]
     ssm = s_a.stride(0) if s_stride_m is None else s_stride_m
     sskb = s_a.stride(1) if s_stride_kb is None else s_stride_kb
+    Kb = -(-K // 128)
+    _span(q_a, "q_a", T, K, K, 1, 1)
+    _span(s_a, "s_a", T, Kb, ssm, sskb, 4)
+    _span(w, "w", G * N, K, K, 1, 1)
+    _grid_span(w_scale, "w_scale", -(-N // 128), Kb, G)
+    _span(offsets, "offsets", 1, G + 1, 1, 1, 4)
+    _out(y, "y", T, N, 2)
     wsp, wsb = _ws(workspace)
     _check(_lib.bfp8_grouped_linear(_ptr(q_a), _ptr(s_a), ssm, sskb, _ptr(w), _ptr(w_scale),
                                     _scale_dtype(w_scale), _ptr(offsets), G, T, N, K, _ptr(y),
@@ -336,6 +436,14 @@ def bfp8_linear_w8a8_silu_quant(q_a, s_a, w, w_scale, q_h, s_h, s_stride_m=None,
     sskb = s_a.stride(1) if s_stride_kb is None else s_stride_kb
     hsm = s_h.stride(0) if sh_stride_m is None else sh_stride_m
     hskb = s_h.stride(1) if sh_stride_kb is None else sh_stride_kb
+    Kb = -(-K // 128)
+    _span(q_a, "q_a", M, K, K, 1, 1)
+    _span(s_a, "s_a", M, Kb, ssm, sskb, 4)
+    _span(w, "w", 2 * I, K, K, 1, 1)
+    _grid_span(w_scale, "w_scale", _scale_rows(2 * I, [I, I]), Kb)
+    _out(q_h, "q_h", M, I, 1)
+    _scales_out(s_h, "s_h", M, -(-I // 128), hsm, hskb,
+                sh_stride_m is not None or sh_stride_kb is not None)
     wsp, wsb = _ws(workspace)
     _check(_lib.bfp8_linear_w8a8_silu_quant(_ptr(q_a), _ptr(s_a), ssm, sskb, _ptr(w),
                                             _ptr(w_scale), _scale_dtype(w_scale), M, I, K,
@@ -359,6 +467,15 @@ def bfp8_grouped_linear_silu_quant(q_a, s_a, w, w_scale, offsets, q_h, s_h, s_st
     sskb = s_a.stride(1) if s_stride_kb is None else s_stride_kb
     hsm = s_h.stride(0) if sh_stride_m is None else sh_stride_m
     hskb = s_h.stride(1) if sh_stride_kb is None else sh_stride_kb
+    Kb = -(-K // 128)
+    _span(q_a, "q_a", T, K, K, 1, 1)
+    _span(s_a, "s_a", T, Kb, ssm, sskb, 4)
+    _span(w, "w", G * 2 * I, K, K, 1, 1)
+    _grid_span(w_scale, "w_scale", _scale_rows(2 * I, [I, I]), Kb, G)
+    _span(offsets, "offsets", 1, G + 1, 1, 1, 4)
+    _out(q_h, "q_h", T, I, 1)
+    _scales_out(s_h, "s_h", T, -(-I // 128), hsm, hskb,
+                sh_stride_m is not None or sh_stride_kb is not None)
     wsp, wsb = _ws(workspace)
     _check(_lib.bfp8_grouped_linear_silu_quant(_ptr(q_a), _ptr(s_a), ssm, sskb, _ptr(w),
                                                _ptr(w_scale), _scale_dtype(w_scale),
@@ -380,6 +497,13 @@ def bfp8_decode_ffn(x, w_gate_up, s_gate_up, w_down, s_down, y, workspace,
     """One dense-FFN decode step: gate/up GEMV -> SiLU*up -> down GEMV."""
     M, H = x.shape
     I = w_down.shape[1]
+    Hb, Ib = -(-H // 128), -(-I // 128)
+    _span(x, "x", M, H, x.stride(0), 1, 2)
+    _span(w_gate_up, "w_gate_up", 2 * I, H, H, 1, 1)
+    _grid_span(s_gate_up, "s_gate_up", 2 * Ib, Hb)
+    _span(w_down, "w_down", H, I, I, 1, 1)
+    _grid_span(s_down, "s_down", Hb, Ib)
+    _out(y, "y", M, H, 2)
     _check(_lib.bfp8_decode_ffn(arith, _ptr(x), x.stride(0), _ptr(w_gate_up), _ptr(s_gate_up),
                                 _ptr(w_down), _ptr(s_down), _scale_dtype(s_gate_up), M, H, I,
                                 _ptr(y), y.stride(0), *_ws(workspace),
@@ -394,6 +518,11 @@ def bfp8_moe_gather_act_quant(x, row_token, q, scales, s_stride_m=None, s_stride
     R = row_token.shape[0]
     ssm = scales.stride(0) if s_stride_m is None else s_stride_m
     sskb = scales.stride(1) if s_stride_kb is None else s_stride_kb
+    _span(x, "x", T, H, x.stride(0), 1, 2)
+    _span(row_token, "row_token", 1, R, 1, 1, 4)
+    _out(q, "q", R, H, 1)
+    _scales_out(scales, "scales", R, -(-H // 128), ssm, sskb,
+                s_stride_m is not None or s_stride_kb is not None)
     _check(_lib.bfp8_moe_gather_act_quant(_ptr(x), T, H, x.stride(0), _ptr(row_token), R, _ptr(q),
                                           q.stride(0), _ptr(scales), ssm, sskb, _stream(stream)),
            "bfp8_moe_gather_act_quant")
@@ -403,6 +532,10 @@ def bfp8_moe_combine(y, token_rows, token_weights, out, stream=None) -> None:
     """out[t] = bf16(sum_j token_weights[t, j] * y[token_rows[t, j]]), slot order j."""
     R, H = y.shape
     T, topk = token_rows.shape
+    _span(y, "y", R, H, y.stride(0), 1, 2)
+    _span(token_rows, "token_rows", T, topk, topk, 1, 4)
+    _span(token_weights, "token_weights", T, topk, topk, 1, 4)
+    _out(out, "out", T, H, 2)
     _check(_lib.bfp8_moe_combine(_ptr(y), R, H, y.stride(0), _ptr(token_rows),
                                  _ptr(token_weights), T, topk, _ptr(out), out.stride(0),
                                  _stream(stream)),

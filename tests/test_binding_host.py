@@ -1,0 +1,112 @@
+"""The Python binding's argument checks, on the CPU.
+
+Every pointer the library takes must be device memory of the current GPU,
+and every tensor must hold all the elements the call will address (rows x
+columns at the strides passed, in the library's element size). Both are
+refused in the binding, before the library sees the call: a kernel reading
+a host address, or past a too-small tensor, would fault the GPU.
+
+A valid call made with host tensors must fail on the device check alone,
+which shows that the extent checks accept every argument layout the library
+supports (strided outputs, token-contiguous scales, member grids, expert
+stacks, per-tensor multipliers)."""
+
+import pytest
+import torch
+
+M, K, N = 20, 320, 384
+Kb, Nb = 3, 3
+bf16, u8, f32, i32 = torch.bfloat16, torch.uint8, torch.float32, torch.int32
+
+
+def _device_error(fn, *args, **kw):
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fn(*args, **kw)
+
+
+def _too_small(fn, *args, **kw):
+    with pytest.raises(ValueError, match="too small"):
+        fn(*args, **kw)
+
+
+def test_valid_dense_calls_pass_the_extent_checks(bfp8):
+    x = torch.zeros(M, K, dtype=bf16)
+    q = torch.zeros(M, K, dtype=u8)
+    s = torch.zeros(M, Kb, dtype=f32)
+    _device_error(bfp8.bfp8_act_quant_group, x, q, s)
+    st = torch.zeros(Kb, M, dtype=f32)          # token-contiguous scales
+    _device_error(bfp8.bfp8_act_quant_group, x, q, st, s_stride_m=1, s_stride_kb=M)
+    gu = torch.zeros(M, 2 * K, dtype=bf16)
+    _device_error(bfp8.bfp8_silu_mul_act_quant, gu, q, s)
+    _device_error(bfp8.bfp8_quantize_weight_block, torch.zeros(N, K, dtype=f32),
+                  torch.zeros(N, K, dtype=u8), torch.zeros(Nb, Kb, dtype=bf16))
+    w = torch.zeros(N, K, dtype=u8)
+    yb = torch.zeros(M, N + 8, dtype=bf16)
+    y = yb[:, :N]                                # strided output
+    for sw in (torch.zeros(Nb, Kb, dtype=bf16), torch.zeros(Nb, Kb, dtype=f32),
+               torch.ones((), dtype=f32)):
+        _device_error(bfp8.bfp8_linear_w8a8, q, s, w, sw, y)
+        _device_error(bfp8.bfp8_linear_w8a16, x, w, sw, y)
+        _device_error(bfp8.bfp8_gemv_decode_noalloc, x[:4], w, sw, y[:4])
+    members = [200, 184]                         # grid rows 2 + 2
+    swm = torch.zeros(4, Kb, dtype=bf16)
+    _device_error(bfp8.bfp8_linear_w8a8, q, s, w, swm, y, member_rows=members)
+    ws = torch.zeros(1 << 16, dtype=u8)
+    _device_error(bfp8.bfp8_gemv_decode, x[:4], w, swm, y[:4], ws, member_rows=members)
+    _device_error(bfp8.bfp8_gemv_decode_w8a8, q[:4], s[:4], w, swm, y[:4], ws,
+                  member_rows=members)
+    I = N // 2                                   # fused gate/up: grid rows 2 * ceil(I / 128)
+    _device_error(bfp8.bfp8_linear_w8a8_silu_quant, q, s, w, torch.zeros(4, Kb, dtype=bf16),
+                  torch.zeros(M, I, dtype=u8), torch.zeros(M, 2, dtype=f32))
+
+
+def test_valid_grouped_moe_and_decode_calls_pass_the_extent_checks(bfp8):
+    G, T = 4, 50
+    q = torch.zeros(T, K, dtype=u8)
+    s = torch.zeros(T, Kb, dtype=f32)
+    off = torch.tensor([0, 10, 10, 30, 50], dtype=i32)
+    w = torch.zeros(G, N, K, dtype=u8)
+    y = torch.zeros(T, N, dtype=bf16)
+    for sw in (torch.zeros(G, Nb, Kb, dtype=bf16), torch.ones(G, dtype=f32)):
+        _device_error(bfp8.bfp8_grouped_linear, q, s, w, sw, off, y)
+    I = N // 2
+    _device_error(bfp8.bfp8_grouped_linear_silu_quant, q, s, w, torch.zeros(G, 4, Kb, dtype=bf16),
+                  off, torch.zeros(T, I, dtype=u8), torch.zeros(T, 2, dtype=f32))
+    H, R, k = 256, 12, 3
+    x = torch.zeros(6, H, dtype=bf16)
+    _device_error(bfp8.bfp8_moe_gather_act_quant, x, torch.zeros(R, dtype=i32),
+                  torch.zeros(R, H, dtype=u8), torch.zeros(R, 2, dtype=f32))
+    _device_error(bfp8.bfp8_moe_combine, torch.zeros(R, H, dtype=bf16),
+                  torch.zeros(4, k, dtype=i32), torch.zeros(4, k, dtype=f32),
+                  torch.zeros(4, H, dtype=bf16))
+    Hh, Ii = 256, 384
+    _device_error(bfp8.bfp8_decode_ffn, torch.zeros(2, Hh, dtype=bf16),
+                  torch.zeros(2 * Ii, Hh, dtype=u8), torch.zeros(6, 2, dtype=bf16),
+                  torch.zeros(Hh, Ii, dtype=u8), torch.zeros(2, 3, dtype=bf16),
+                  torch.zeros(2, Hh, dtype=bf16), torch.zeros(1 << 16, dtype=u8))
+
+
+def test_tensors_too_small_for_the_call_are_refused(bfp8):
+    x = torch.zeros(M, K, dtype=bf16)
+    q = torch.zeros(M, K, dtype=u8)
+    s = torch.zeros(M, Kb, dtype=f32)
+    _too_small(bfp8.bfp8_act_quant_group, x, q[: M - 1], s)           # shape [M-1, K]
+    _too_small(bfp8.bfp8_act_quant_group, x, q, s[:, :2])             # strides reach past
+    _too_small(bfp8.bfp8_act_quant_group, x, q, torch.zeros(Kb, M - 1, dtype=f32),
+               s_stride_m=1, s_stride_kb=M)
+    w = torch.zeros(N, K, dtype=u8)
+    y = torch.zeros(M, N, dtype=bf16)
+    _too_small(bfp8.bfp8_linear_w8a8, q, s, w, torch.zeros(Nb - 1, Kb, dtype=bf16), y)
+    _too_small(bfp8.bfp8_linear_w8a8, q, s, w, torch.zeros(Nb, Kb, dtype=bf16), y[: M - 1])
+    _too_small(bfp8.bfp8_linear_w8a8, q, s, w, torch.zeros(3, Kb, dtype=bf16), y,
+               member_rows=[200, 184])                                # needs 4 grid rows
+    _too_small(bfp8.bfp8_quantize_weight_block, torch.zeros(N, K, dtype=bf16),  # read as f32
+               torch.zeros(N, K, dtype=u8), torch.zeros(Nb, Kb, dtype=bf16))
+    G, T = 4, 50
+    off = torch.tensor([0, 10, 10, 30], dtype=i32)                     # needs G + 1 entries
+    _too_small(bfp8.bfp8_grouped_linear, torch.zeros(T, K, dtype=u8), torch.zeros(T, Kb, dtype=f32),
+               torch.zeros(G, N, K, dtype=u8), torch.zeros(G, Nb, Kb, dtype=bf16), off,
+               torch.zeros(T, N, dtype=bf16))
+    _too_small(bfp8.bfp8_moe_combine, torch.zeros(12, 256, dtype=bf16),
+               torch.zeros(4, 3, dtype=i32), torch.zeros(4, 2, dtype=f32),
+               torch.zeros(4, 256, dtype=bf16))
