@@ -81,3 +81,48 @@ def test_binding_refuses_host_tensors(bfp8):
     y = torch.empty(4, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA tensor"):
         bfp8.bfp8_linear_w8a8(q, s, w, sw, y)
+
+
+def test_every_entry_point_refuses_bad_arguments_without_gpu(bfp8):
+    """Each refusal below is decided from the arguments alone, before any CUDA
+    call (placeholder pointers are never dereferenced)."""
+    lib, p = bfp8._lib, ctypes.c_void_p(256)
+    INVAL, SCALE_DTYPE, UNSUPPORTED = 1, 8, 13
+    cases = [
+        # act quant: negative size, row pitch below K, zero scale stride over several rows
+        (lib.bfp8_act_quant_group(p, 4, -1, 4, p, 4, p, 1, 1, None), INVAL),
+        (lib.bfp8_act_quant_group(p, 4, 256, 255, p, 256, p, 2, 1, None), INVAL),
+        (lib.bfp8_act_quant_group(p, 4, 256, 256, p, 255, p, 2, 1, None), INVAL),
+        (lib.bfp8_act_quant_group(p, 4, 256, 256, p, 256, p, 0, 1, None), INVAL),
+        # SiLU*up quant: the gate/up pitch must hold 2I values
+        (lib.bfp8_silu_mul_act_quant(p, 4, 128, 255, p, 128, p, 1, 4, None), INVAL),
+        # weight quantization
+        (lib.bfp8_quantize_weight_block(p, -1, 128, 128, p, 128, p, 3, None), INVAL),
+        (lib.bfp8_quantize_weight_block(p, 128, 128, 127, p, 128, p, 3, None), INVAL),
+        (lib.bfp8_quantize_weight_block(p, 128, 128, 128, p, 128, p, 4, None), SCALE_DTYPE),
+        # W8A16: activation pitch below K
+        (lib.bfp8_linear_w8a16(p, 127, p, p, 3, 4, 128, 128, p, 128, None, None), INVAL),
+        # decode GEMV, W8A8 arm: more than 16 tokens
+        (lib.bfp8_gemv_decode_w8a8(p, p, 1, 1, p, p, 3, 17, 128, 128, p, 128, None, p, 1 << 20,
+                                   None), INVAL),
+        # grouped: more experts than the schedule holds; fused: h pitch below I
+        (lib.bfp8_grouped_linear(p, p, 1, 1, p, p, 3, p, 1025, 8, 128, 128, p, 128, None, 0, None),
+         INVAL),
+        (lib.bfp8_linear_w8a8_silu_quant(p, p, 1, 1, p, p, 3, 4, 128, 128, p, 127, p, 1, 1, None,
+                                         0, None), INVAL),
+        (lib.bfp8_grouped_linear_silu_quant(p, p, 1, 1, p, p, 3, p, 0, 8, 128, 128, p, 128, p, 1,
+                                            1, None, 0, None), INVAL),
+        # decode step: unknown arithmetic, 17 tokens, sizes not multiples of 16
+        (lib.bfp8_decode_ffn(7, p, 256, p, p, p, p, 3, 4, 256, 256, p, 256, p, 1 << 24, None),
+         INVAL),
+        (lib.bfp8_decode_ffn(0, p, 256, p, p, p, p, 3, 17, 256, 256, p, 256, p, 1 << 24, None),
+         INVAL),
+        (lib.bfp8_decode_ffn(0, p, 264, p, p, p, p, 3, 4, 264, 256, p, 264, p, 1 << 24, None),
+         UNSUPPORTED),
+        # MoE glue: a negative routed-row count; top-k of zero; output pitch below H
+        (lib.bfp8_moe_gather_act_quant(p, 8, 256, 256, p, -1, p, 256, p, 2, 1, None), INVAL),
+        (lib.bfp8_moe_combine(p, 16, 256, 256, p, p, 8, 0, p, 256, None), INVAL),
+        (lib.bfp8_moe_combine(p, 16, 256, 256, p, p, 8, 2, p, 255, None), INVAL),
+    ]
+    for i, (got, want) in enumerate(cases):
+        assert got == want, (i, got, want)
