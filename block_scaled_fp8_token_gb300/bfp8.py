@@ -70,6 +70,7 @@ _SIGS = {
     "bfp8_validate_grid": (ctypes.c_int, [ctypes.POINTER(bfp8_weight_desc), ctypes.c_char_p, _sz]),
     "bfp8_act_quant_group": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _vp]),
     "bfp8_silu_mul_act_quant": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _vp]),
+    "bfp8_silu_mul": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp]),
     "bfp8_quantize_weight_block": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i32, _vp]),
     "bfp8_linear_w8a8": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i32, _i64, _i64, _i64,
                                         _vp, _i64, ctypes.POINTER(bfp8_members), _vp, _sz, _vp]),
@@ -205,6 +206,7 @@ def bfp8_act_quant_group(x, q, scales, s_stride_m=None, s_stride_kb=None, stream
     M, K = x.shape
     ssm = scales.stride(0) if s_stride_m is None else s_stride_m
     sskb = scales.stride(1) if s_stride_kb is None else s_stride_kb
+    _rows(x, "x")
     _span(x, "x", M, K, x.stride(0), 1, 2)
     _out(q, "q", M, K, 1)
     _scales_out(scales, "scales", M, -(-K // 128), ssm, sskb,
@@ -218,6 +220,7 @@ def bfp8_silu_mul_act_quant(gu, q, scales, s_stride_m=None, s_stride_kb=None, st
     M, two_i = gu.shape
     ssm = scales.stride(0) if s_stride_m is None else s_stride_m
     sskb = scales.stride(1) if s_stride_kb is None else s_stride_kb
+    _rows(gu, "gu")
     _span(gu, "gu", M, two_i, gu.stride(0), 1, 2)
     _out(q, "q", M, two_i // 2, 1)
     _scales_out(scales, "scales", M, -(-(two_i // 2) // 128), ssm, sskb,
@@ -227,8 +230,20 @@ def bfp8_silu_mul_act_quant(gu, q, scales, s_stride_m=None, s_stride_kb=None, st
            "bfp8_silu_mul_act_quant")
 
 
+def bfp8_silu_mul(gu, h, stream=None) -> None:
+    """h = bf16(silu(gate) * up) for gu = [gate | up] ([M, 2I] BF16); h [M, I] BF16."""
+    M, two_i = gu.shape
+    _rows(gu, "gu")
+    _span(gu, "gu", M, two_i, gu.stride(0), 1, 2)
+    _out(h, "h", M, two_i // 2, 2)
+    _check(_lib.bfp8_silu_mul(_ptr(gu), M, two_i // 2, gu.stride(0), _ptr(h), h.stride(0),
+                              _stream(stream)),
+           "bfp8_silu_mul")
+
+
 def bfp8_quantize_weight_block(w, q, scale, stream=None) -> None:
     N, K = w.shape
+    _rows(w, "w")
     _span(w, "w", N, K, w.stride(0), 1, 4)  # float32, as the library reads it
     _out(q, "q", N, K, 1)
     _grid_span(scale, "scale", -(-N // 128), -(-K // 128))
@@ -254,6 +269,38 @@ def _span(t, name: str, rows: int, cols: int, rs: int, cs: int, elem_bytes: int)
                          f"at strides ({rs}, {cs}) reach past its storage")
 
 
+def _layout(t, name: str, shape, pitch: int | None = None) -> None:
+    """t must have exactly `shape` and unit stride along its last dimension
+    (row pitch `pitch` when given, dense strides for higher ranks): the
+    library reads it as dense row-major data, so a transposed view, a column
+    slice or a permuted grid would be misread silently. Strides of size-1
+    dimensions do not matter and are not checked."""
+    if t is None or isinstance(t, int):
+        return
+    shape = tuple(int(v) for v in shape)
+    if tuple(t.shape) != shape:
+        raise ValueError(f"bfp8: {name} has shape {list(t.shape)}, expected {list(shape)}")
+    want = [1] * len(shape)
+    for d in range(len(shape) - 2, -1, -1):
+        want[d] = want[d + 1] * shape[d + 1]
+    if pitch is not None and len(shape) >= 2:
+        want[-2] = int(pitch)
+    for d, (st, w) in enumerate(zip(t.stride(), want)):
+        if shape[d] > 1 and st != w:
+            raise ValueError(f"bfp8: {name} has strides {list(t.stride())}; the library reads it "
+                             f"as row-major with strides {want}")
+
+
+def _rows(t, name: str) -> None:
+    """An activation or output matrix passed with its own row pitch: the
+    columns must be contiguous (unit stride along the last dimension)."""
+    if t is None or isinstance(t, int) or t.dim() != 2:
+        return
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError(f"bfp8: {name} must have contiguous columns, got strides "
+                         f"{list(t.stride())}")
+
+
 def _out(t, name: str, rows: int, cols: int, elem_bytes: int) -> None:
     """An output the library writes as rows x cols row-major elements at
     t.stride(0): the view must cover them, not only its storage."""
@@ -262,6 +309,7 @@ def _out(t, name: str, rows: int, cols: int, elem_bytes: int) -> None:
     if t.dim() != 2 or t.shape[0] < rows or t.shape[1] < cols:
         raise ValueError(f"bfp8: {name} is too small for the call: needs [{rows}, {cols}], "
                          f"got {list(t.shape)}")
+    _rows(t, name)
     _span(t, name, rows, cols, t.stride(0), 1, elem_bytes)
 
 
@@ -279,16 +327,24 @@ def _scales_out(t, name: str, rows: int, cols: int, s_m: int, s_kb: int, explici
 _SCALE_BYTES = {BFP8_DT_BF16: 2, BFP8_DT_F16: 2, BFP8_DT_F32: 4}
 
 
-def _grid_span(t, name: str, rows: int, kb: int, experts: int = 1) -> None:
-    """A weight-scale argument: `experts` contiguous [rows, kb] block grids, or
-    one multiplier per expert (a tensor of rank 0 or 1)."""
+def _grid_span(t, name: str, rows: int, kb: int, experts: int | None = None) -> None:
+    """A weight-scale argument: the block grid [rows, kb] (rows = the sum of
+    ceil(N_i / 128) over members, kb = ceil(K / 128)), or [experts, rows, kb]
+    for expert stacks, dense row-major; or one multiplier (one per expert) as
+    a tensor of rank 0 or 1. A transposed or mis-shaped grid is refused here
+    (the library would read it as this layout)."""
     eb = _SCALE_BYTES.get(_scale_dtype(t) & 0xFF)
     if eb is None:
         return  # refused by the library (SCALE_DTYPE) before anything is read
+    n = 1 if experts is None else experts
     if t.dim() <= 1:
-        _span(t, name, experts, 1, 1, 1, eb)
-    else:
-        _span(t, name, experts * rows, kb, kb, 1, eb)
+        if t.numel() != n:
+            raise ValueError(f"bfp8: {name}: a per-tensor scale needs {n} element(s), "
+                             f"got {t.numel()}")
+        _span(t, name, n, 1, 1, 1, eb)
+        return
+    _layout(t, name, (rows, kb) if experts is None else (experts, rows, kb))
+    _span(t, name, n * rows, kb, kb, 1, eb)
 
 
 def _scale_rows(N: int, member_rows) -> int:
@@ -313,9 +369,9 @@ def bfp8_linear_w8a8(q_a, s_a, w, w_scale, y, member_rows=None, s_stride_m=None,
     ssm = s_a.stride(0) if s_stride_m is None else s_stride_m
     sskb = s_a.stride(1) if s_stride_kb is None else s_stride_kb
     Kb = -(-K // 128)
-    _span(q_a, "q_a", M, K, K, 1, 1)
+    _layout(q_a, "q_a", (M, K))
     _span(s_a, "s_a", M, Kb, ssm, sskb, 4)
-    _span(w, "w", N, K, K, 1, 1)
+    _layout(w, "w", (N, K))
     _grid_span(w_scale, "w_scale", _scale_rows(N, member_rows), Kb)
     _out(y, "y", M, N, 2)
     mref, _keep = _members(member_rows)
@@ -329,8 +385,9 @@ def bfp8_linear_w8a8(q_a, s_a, w, w_scale, y, member_rows=None, s_stride_m=None,
 def bfp8_linear_w8a16(x, w, w_scale, y, member_rows=None, stream=None) -> None:
     M, K = x.shape
     N = w.shape[0]
+    _rows(x, "x")
     _span(x, "x", M, K, x.stride(0), 1, 2)
-    _span(w, "w", N, K, K, 1, 1)
+    _layout(w, "w", (N, K))
     _grid_span(w_scale, "w_scale", _scale_rows(N, member_rows), -(-K // 128))
     _out(y, "y", M, N, 2)
     mref, _keep = _members(member_rows)
@@ -347,8 +404,9 @@ def bfp8_gemv_decode_workspace(M: int, N: int, K: int) -> int:
 def bfp8_gemv_decode(x, w, w_scale, y, workspace, member_rows=None, stream=None) -> None:
     M, K = x.shape
     N = w.shape[0]
+    _rows(x, "x")
     _span(x, "x", M, K, x.stride(0), 1, 2)
-    _span(w, "w", N, K, K, 1, 1)
+    _layout(w, "w", (N, K))
     _grid_span(w_scale, "w_scale", _scale_rows(N, member_rows), -(-K // 128))
     _out(y, "y", M, N, 2)
     mref, _keep = _members(member_rows)
@@ -367,9 +425,9 @@ def bfp8_gemv_decode_w8a8(q_a, s_a, w, w_scale, y, workspace, member_rows=None, 
     ssm = s_a.stride(0) if s_stride_m is None else s_stride_m
     sskb = s_a.stride(1) if s_stride_kb is None else s_stride_kb
     Kb = -(-K // 128)
-    _span(q_a, "q_a", M, K, K, 1, 1)
+    _layout(q_a, "q_a", (M, K))
     _span(s_a, "s_a", M, Kb, ssm, sskb, 4)
-    _span(w, "w", N, K, K, 1, 1)
+    _layout(w, "w", (N, K))
     _grid_span(w_scale, "w_scale", _scale_rows(N, member_rows), Kb)
     _out(y, "y", M, N, 2)
     mref, _keep = _members(member_rows)
@@ -386,8 +444,9 @@ def bfp8_gemv_decode_noalloc(x, w, w_scale, y, member_rows=None, stream=None) ->
     allocate device memory; its scratch is a fixed array inside the library."""
     M, K = x.shape
     N = w.shape[0]
+    _rows(x, "x")
     _span(x, "x", M, K, x.stride(0), 1, 2)
-    _span(w, "w", N, K, K, 1, 1)
+    _layout(w, "w", (N, K))
     _grid_span(w_scale, "w_scale", _scale_rows(N, member_rows), -(-K // 128))
     _out(y, "y", M, N, 2)
     mref, _keep = _members(member_rows)
@@ -408,11 +467,11 @@ def bfp8_grouped_linear(q_a, s_a, w, w_scale, offsets, y, s_stride_m=None, s_str
     ssm = s_a.stride(0) if s_stride_m is None else s_stride_m
     sskb = s_a.stride(1) if s_stride_kb is None else s_stride_kb
     Kb = -(-K // 128)
-    _span(q_a, "q_a", T, K, K, 1, 1)
+    _layout(q_a, "q_a", (T, K))
     _span(s_a, "s_a", T, Kb, ssm, sskb, 4)
-    _span(w, "w", G * N, K, K, 1, 1)
+    _layout(w, "w", (G, N, K))
     _grid_span(w_scale, "w_scale", -(-N // 128), Kb, G)
-    _span(offsets, "offsets", 1, G + 1, 1, 1, 4)
+    _layout(offsets, "offsets", (G + 1,))
     _out(y, "y", T, N, 2)
     wsp, wsb = _ws(workspace)
     _check(_lib.bfp8_grouped_linear(_ptr(q_a), _ptr(s_a), ssm, sskb, _ptr(w), _ptr(w_scale),
@@ -437,9 +496,9 @@ def bfp8_linear_w8a8_silu_quant(q_a, s_a, w, w_scale, q_h, s_h, s_stride_m=None,
     hsm = s_h.stride(0) if sh_stride_m is None else sh_stride_m
     hskb = s_h.stride(1) if sh_stride_kb is None else sh_stride_kb
     Kb = -(-K // 128)
-    _span(q_a, "q_a", M, K, K, 1, 1)
+    _layout(q_a, "q_a", (M, K))
     _span(s_a, "s_a", M, Kb, ssm, sskb, 4)
-    _span(w, "w", 2 * I, K, K, 1, 1)
+    _layout(w, "w", (2 * I, K))
     _grid_span(w_scale, "w_scale", _scale_rows(2 * I, [I, I]), Kb)
     _out(q_h, "q_h", M, I, 1)
     _scales_out(s_h, "s_h", M, -(-I // 128), hsm, hskb,
@@ -468,11 +527,11 @@ def bfp8_grouped_linear_silu_quant(q_a, s_a, w, w_scale, offsets, q_h, s_h, s_st
     hsm = s_h.stride(0) if sh_stride_m is None else sh_stride_m
     hskb = s_h.stride(1) if sh_stride_kb is None else sh_stride_kb
     Kb = -(-K // 128)
-    _span(q_a, "q_a", T, K, K, 1, 1)
+    _layout(q_a, "q_a", (T, K))
     _span(s_a, "s_a", T, Kb, ssm, sskb, 4)
-    _span(w, "w", G * 2 * I, K, K, 1, 1)
+    _layout(w, "w", (G, 2 * I, K))
     _grid_span(w_scale, "w_scale", _scale_rows(2 * I, [I, I]), Kb, G)
-    _span(offsets, "offsets", 1, G + 1, 1, 1, 4)
+    _layout(offsets, "offsets", (G + 1,))
     _out(q_h, "q_h", T, I, 1)
     _scales_out(s_h, "s_h", T, -(-I // 128), hsm, hskb,
                 sh_stride_m is not None or sh_stride_kb is not None)
@@ -498,10 +557,11 @@ def bfp8_decode_ffn(x, w_gate_up, s_gate_up, w_down, s_down, y, workspace,
     M, H = x.shape
     I = w_down.shape[1]
     Hb, Ib = -(-H // 128), -(-I // 128)
+    _rows(x, "x")
     _span(x, "x", M, H, x.stride(0), 1, 2)
-    _span(w_gate_up, "w_gate_up", 2 * I, H, H, 1, 1)
+    _layout(w_gate_up, "w_gate_up", (2 * I, H))
     _grid_span(s_gate_up, "s_gate_up", 2 * Ib, Hb)
-    _span(w_down, "w_down", H, I, I, 1, 1)
+    _layout(w_down, "w_down", (H, I))
     _grid_span(s_down, "s_down", Hb, Ib)
     _out(y, "y", M, H, 2)
     _check(_lib.bfp8_decode_ffn(arith, _ptr(x), x.stride(0), _ptr(w_gate_up), _ptr(s_gate_up),
@@ -518,8 +578,9 @@ def bfp8_moe_gather_act_quant(x, row_token, q, scales, s_stride_m=None, s_stride
     R = row_token.shape[0]
     ssm = scales.stride(0) if s_stride_m is None else s_stride_m
     sskb = scales.stride(1) if s_stride_kb is None else s_stride_kb
+    _rows(x, "x")
     _span(x, "x", T, H, x.stride(0), 1, 2)
-    _span(row_token, "row_token", 1, R, 1, 1, 4)
+    _layout(row_token, "row_token", (R,))
     _out(q, "q", R, H, 1)
     _scales_out(scales, "scales", R, -(-H // 128), ssm, sskb,
                 s_stride_m is not None or s_stride_kb is not None)
@@ -532,9 +593,10 @@ def bfp8_moe_combine(y, token_rows, token_weights, out, stream=None) -> None:
     """out[t] = bf16(sum_j token_weights[t, j] * y[token_rows[t, j]]), slot order j."""
     R, H = y.shape
     T, topk = token_rows.shape
+    _rows(y, "y")
     _span(y, "y", R, H, y.stride(0), 1, 2)
-    _span(token_rows, "token_rows", T, topk, topk, 1, 4)
-    _span(token_weights, "token_weights", T, topk, topk, 1, 4)
+    _layout(token_rows, "token_rows", (T, topk))
+    _layout(token_weights, "token_weights", (T, topk))
     _out(out, "out", T, H, 2)
     _check(_lib.bfp8_moe_combine(_ptr(y), R, H, y.stride(0), _ptr(token_rows),
                                  _ptr(token_weights), T, topk, _ptr(out), out.stride(0),

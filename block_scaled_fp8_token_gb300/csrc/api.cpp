@@ -87,6 +87,22 @@ int check_launch() {
   return cudaPeekAtLastError() == cudaSuccess ? BFP8_OK : BFP8_ERR_CUDA;
 }
 
+int check_device_ptrs(std::initializer_list<const void*> ptrs) {
+  int dev = 0;
+  int rc = current_device(&dev);
+  if (rc != BFP8_OK) return rc;
+  for (const void* p : ptrs) {
+    if (!p) continue;
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+      cudaGetLastError();  // not sticky; keep it out of the next launch check
+      return BFP8_ERR_INVALID_ARG;
+    }
+    if (a.type != cudaMemoryTypeDevice || a.device != dev) return BFP8_ERR_INVALID_ARG;
+  }
+  return BFP8_OK;
+}
+
 int set_max_dynamic_smem(const void* kernel, int bytes) {
   // Cheap and idempotent; done on every launch so that every device is covered.
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
@@ -315,6 +331,11 @@ int bfp8_silu_mul_act_quant(const void* gu_bf16, int64_t M, int64_t I, int64_t l
                             int64_t s_stride_kb, void* stream) {
   return launch_silu_mul_act_quant(gu_bf16, M, I, ld, q_e4m3, ldq, scales, s_stride_m,
                                    s_stride_kb, stream);
+}
+
+int bfp8_silu_mul(const void* gu_bf16, int64_t M, int64_t I, int64_t ld, void* h_bf16,
+                  int64_t ldh, void* stream) {
+  return launch_silu_mul(gu_bf16, M, I, ld, h_bf16, ldh, stream);
 }
 
 size_t bfp8_decode_ffn_workspace(int64_t M, int64_t H, int64_t I, int32_t arith) {

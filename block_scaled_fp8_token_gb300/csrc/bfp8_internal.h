@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <initializer_list>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -14,6 +15,12 @@ namespace bfp8 {
 int sm_count(int* out);
 // Map the last launch error (if any) to a status.
 int check_launch();
+// Every pointer a kernel or a tensor map will dereference must be device
+// memory of the current device (cudaMalloc, a stream-ordered pool, or the
+// library's own __device__ arrays). Host memory, pinned or not, managed
+// memory and another GPU's memory are refused with BFP8_ERR_INVALID_ARG,
+// before anything is launched. Null entries are skipped.
+int check_device_ptrs(std::initializer_list<const void*> ptrs);
 // Make `kernel` accept `bytes` of dynamic shared memory on the current device.
 int set_max_dynamic_smem(const void* kernel, int bytes);
 
@@ -53,6 +60,8 @@ int launch_act_quant(const void* x, int64_t M, int64_t K, int64_t ldx, void* q, 
                      float* s, int64_t ssm, int64_t sskb, void* stream);
 int launch_silu_mul_act_quant(const void* gu, int64_t M, int64_t I, int64_t ld, void* q,
                               int64_t ldq, float* s, int64_t ssm, int64_t sskb, void* stream);
+int launch_silu_mul(const void* gu, int64_t M, int64_t I, int64_t ld, void* h, int64_t ldh,
+                    void* stream);
 int launch_moe_gather_act_quant(const void* x, int64_t T, int64_t H, int64_t ldx,
                                 const int32_t* row_token, int64_t R, void* q, int64_t ldq,
                                 float* s, int64_t ssm, int64_t sskb, void* stream);

@@ -176,11 +176,6 @@ struct Tile {
   int32_t b_row0_up, srow_up;  // fused SiLU*up: first up row and its scale row
 };
 
-#ifndef BFP8_W8A8_CLUSTER
-#define BFP8_W8A8_CLUSTER 1
-#endif
-constexpr int kW8A8Cluster = BFP8_W8A8_CLUSTER;
-
 template <int BN, int STAGES, bool W8A16, bool GROUPED, bool SWIGLU = false>
 struct Cfg {
   static_assert(!SWIGLU || (!W8A16 && BN == 256),
@@ -193,9 +188,6 @@ struct Cfg {
   // promotion/epilogue. setmaxnreg moves registers from warpgroup 0 to the
   // epilogue, whose FP32 tile accumulator takes 128 registers per thread.
   static constexpr bool kSplitRegs = !W8A16;
-  // W8A8 runs in 2-CTA clusters on adjacent M tiles: each CTA loads its own A
-  // tile and half of the shared B tile, multicast to both CTAs.
-  static constexpr int kCluster = (W8A16 || SWIGLU) ? 1 : kW8A8Cluster;
   static constexpr int kEpiWarp0 = kSplitRegs ? 4 : 2;
   static constexpr int kWarps = kEpiWarp0 + kEpiWarps + kConvWarps;
   static constexpr int kThreads = kWarps * 32;
@@ -262,19 +254,15 @@ struct Cfg {
   static_assert(kEpiCols % 32 == 0, "epilogue columns come in 32-column TMEM loads");
 };
 
-// Work item t covers CL adjacent M tiles (one per CTA of the cluster) of one
-// N tile of TW output columns; `rank` picks this CTA's M tile. A rank past the
-// last M tile gets m_valid <= 0: it still loads and multicasts its share of B,
-// but stores nothing. The up-half fields serve the fused SiLU*up epilogue,
-// whose tile of TW output columns reads TW gate rows and the TW matching up
-// rows of W.
-template <int TW, int CL, bool GROUPED>
+// Work item t is one M tile of one N tile of TW output columns (M tiles
+// fastest). The up-half fields serve the fused SiLU*up epilogue, whose tile of
+// TW output columns reads TW gate rows and the TW matching up rows of W.
+template <int TW, bool GROUPED>
 __device__ __forceinline__ void decode_tile(const GemmParams& p, const int* s_off,
-                                            const int* s_pre, int t, int rank, Tile& tl) {
+                                            const int* s_pre, int t, Tile& tl) {
   if (!GROUPED) {
-    const int m_units = (p.m_tiles + CL - 1) / CL;
-    const int nt = t / m_units;
-    const int mt = (t - nt * m_units) * CL + rank;
+    const int nt = t / p.m_tiles;
+    const int mt = t - nt * p.m_tiles;
     int i = 0;
 #pragma unroll 1
     while (i + 1 < p.n_members && nt >= p.mem_tile0[i + 1]) ++i;
@@ -299,10 +287,10 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, const int* s_of
     const int e = lo;
     const int row0 = s_off[e];
     const int rows = s_off[e + 1] - row0;
-    const int units = ((rows + BM - 1) / BM + CL - 1) / CL;
+    const int units = (rows + BM - 1) / BM;
     const int local = t - s_pre[e];
     const int nt = local / units;
-    const int mt = (local - nt * units) * CL + rank;
+    const int mt = local - nt * units;
     tl.a_row0 = row0 + mt * BM;
     tl.m_valid = min(BM, rows - mt * BM);
     tl.b_row0 = nt * TW;
@@ -317,9 +305,8 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, const int* s_of
 }
 
 // Grouped schedule, built by one warp: clamp the offsets into [0, M], make
-// them non-decreasing, then prefix-sum the work items (CL M tiles x one N tile)
-// of every expert.
-template <int CL>
+// them non-decreasing, then prefix-sum the work items (one M tile x one N
+// tile) of every expert.
 __device__ void build_schedule(const GemmParams& p, int* s_off, int* s_pre, int lane) {
   const int n = p.G + 1;
   const int per = (n + 31) / 32;
@@ -345,7 +332,7 @@ __device__ void build_schedule(const GemmParams& p, int* s_off, int* s_pre, int 
   const int b2 = min(p.G, lane * per2), e2 = min(p.G, b2 + per2);
   int sum = 0;
   for (int i = b2; i < e2; ++i)
-    sum += (((s_off[i + 1] - s_off[i] + BM - 1) / BM + CL - 1) / CL) * p.n_tiles;
+    sum += ((s_off[i + 1] - s_off[i] + BM - 1) / BM) * p.n_tiles;
   int incl2 = sum;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -355,7 +342,7 @@ __device__ void build_schedule(const GemmParams& p, int* s_off, int* s_pre, int 
   int run2 = incl2 - sum;
   for (int i = b2; i < e2; ++i) {
     s_pre[i] = run2;
-    run2 += (((s_off[i + 1] - s_off[i] + BM - 1) / BM + CL - 1) / CL) * p.n_tiles;
+    run2 += ((s_off[i + 1] - s_off[i] + BM - 1) / BM) * p.n_tiles;
   }
   if (lane == 31) s_pre[p.G] = incl2;
   __syncwarp();
@@ -393,10 +380,8 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
   uint8_t* const base_ptr = smem_raw + (base - raw_u32);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  constexpr int CL = C::kCluster;
-  const int rank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int cid = blockIdx.x / CL;     // cluster index (CTAs of a cluster are consecutive)
-  const int ncl = gridDim.x / CL;
+  const int cid = blockIdx.x;
+  const int ncl = gridDim.x;
 
   const uint32_t bar0 = base + C::kOffBar;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -427,7 +412,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), CL);  // released by the MMA of every CTA that reads the stage
+      mbar_init(empty_bar(s), 1);   // released by the MMA's commit
     }
     for (int b = 0; b < C::kNumBufs; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -465,13 +450,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
   pdl_launch_dependents();
   if (GROUPED && warp == C::kEpiWarp0) {
     pdl_wait();
-    build_schedule<CL>(p, s_off, s_pre, lane);
+    build_schedule(p, s_off, s_pre, lane);
   }
   tc_fence_before();
   __syncthreads();
-  // The peer CTA multicasts into this CTA's shared memory and arrives on its
-  // barriers: both must be initialised before either CTA issues anything.
-  if constexpr (CL > 1) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = GROUPED ? s_pre[p.G] : p.total_tiles;
@@ -484,10 +466,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
   // tiles are short and their split tiles cost more: < 80%.
   const int fill_pct = GROUPED ? 80 : 85;
   const bool sparse_tail = waves > 0 && 100 * total < fill_pct * waves * ncl;
-  const bool sk = CL == 1 && p.stream_k && sparse_tail &&
+  const bool sk = p.stream_k && sparse_tail &&
                   sk_geo(true, total, p.Kb, ncl, 0).U >= static_cast<int64_t>(ncl);
   // lockstep stream-K groups (dense tiles are numbered M-fastest)
-  const int mu_lock = (GROUPED || CL > 1) ? 0 : p.m_tiles;
+  const int mu_lock = GROUPED ? 0 : p.m_tiles;
 
   if (warp < C::kEpiWarp0) {
     // warpgroup 0: producer (warp 0) and MMA issuer (warp 1)
@@ -503,7 +485,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
         int t, kb0, kb1;
         while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
           Tile tl;
-          decode_tile<C::kOutCols, CL, GROUPED>(p, s_off, s_pre, t, rank, tl);
+          decode_tile<C::kOutCols, GROUPED>(p, s_off, s_pre, t, tl);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait_sleep(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
             const uint32_t sA = base + stage * C::kStage;
@@ -519,15 +501,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
             } else {
               tma_load_2d(sA, &tmA, kb * BK, tl.a_row0, full_bar(stage));
             }
-            if constexpr (CL > 1) {
-              // this CTA's half of the B tile, into the same offset of both CTAs
-              const uint32_t half = static_cast<uint32_t>(rank) * (BN / CL) * 128u;
-              const int brow = tl.b_row0 + rank * (BN / CL);
-              if (GROUPED)
-                tma_load_3d_mc(sB + half, &tmB, kb * BK, brow, tl.expert, full_bar(stage), 0x3);
-              else
-                tma_load_2d_mc(sB + half, &tmB, kb * BK, brow, full_bar(stage), 0x3);
-            } else if constexpr (SWIGLU) {
+            if constexpr (SWIGLU) {
               // gate rows into B rows [0, BN/2), the matching up rows into [BN/2, BN)
               const uint32_t sBu = sB + (BN / 2) * 128u;
               if (GROUPED) {
@@ -560,7 +534,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
         int t, kb0, kb1;
         while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
           Tile tl;
-          decode_tile<C::kOutCols, CL, GROUPED>(p, s_off, s_pre, t, rank, tl);
+          decode_tile<C::kOutCols, GROUPED>(p, s_off, s_pre, t, tl);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait_sleep(raw_empty(rs), rphase ^ 1u, abort_flag)) { ok = false; break; }
             const uint32_t sR = base + C::kOffRaw + rs * C::kBRawBytes;
@@ -619,10 +593,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
                 umma_bf16(d, da, db, C::kIdesc, k > 0 ? 1u : 0u);
               }
             }
-            if constexpr (CL > 1)
-              umma_commit_mc(empty_bar(stage), 0x3);  // frees the stage in both CTAs
-            else
-              umma_commit(empty_bar(stage));
+            umma_commit(empty_bar(stage));
             if (W8A16) umma_commit(cv_empty(cs));   // the decoded B buffer is free again
             umma_commit(tfull_bar(buf));
           }
@@ -655,7 +626,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
       int t, kb0, kb1;
       while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
         Tile tl;
-        decode_tile<C::kOutCols, CL, GROUPED>(p, s_off, s_pre, t, rank, tl);
+        decode_tile<C::kOutCols, GROUPED>(p, s_off, s_pre, t, tl);
         const int64_t sw_base = GROUPED ? tl.expert * p.sw_expert_stride : 0;
         const int srow0 = SWIGLU ? tl.srow0 : tl.srow0;
         const int srow1 = SWIGLU ? tl.srow_up : min(tl.srow0 + C::kEpiCols / 128, tl.srow_last);
@@ -704,7 +675,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
     int t, kb0, kb1;
     while (next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
       Tile tl;
-      decode_tile<C::kOutCols, CL, GROUPED>(p, s_off, s_pre, t, rank, tl);
+      decode_tile<C::kOutCols, GROUPED>(p, s_off, s_pre, t, tl);
       const bool row_ok = row_in_tile < tl.m_valid;
       const int64_t arow = static_cast<int64_t>(tl.a_row0) + row_in_tile;
       // This warp's columns of the tile: 128 consecutive ones (one weight-scale
@@ -1046,8 +1017,6 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
   }
 
   __syncthreads();
-  // No CTA may exit while its peer can still arrive on its barriers.
-  if constexpr (CL > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
@@ -1074,29 +1043,28 @@ int launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, 
   }
   int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel), C::kSmemBytes);
   if (rc != BFP8_OK) return rc;
+  // persistent: at most as many CTAs as can be resident at once (one per SM)
+  int per_sm = 0, sms = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, C::kThreads, C::kSmemBytes) !=
+          cudaSuccess ||
+      per_sm < 1)
+    return BFP8_ERR_CUDA;
+  rc = sm_count(&sms);
+  if (rc != BFP8_OK) return rc;
+  const int64_t max_ctas = static_cast<int64_t>(per_sm) * sms;
+  int64_t items = work_items;
+  if (p.stream_k) items = static_cast<int64_t>(work_items) * p.Kb;  // stream-K splits by K-block units
+  const int ctas = static_cast<int>(items < max_ctas ? items : max_ctas);
   cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C::kCluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see the kernel's first wait
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see the kernel's first wait
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = static_cast<cudaStream_t>(stream);
   cfg.attrs = attr;
-  cfg.numAttrs = 1;   // occupancy query: cluster shape only
-  // persistent: at most as many clusters as can be resident at once
-  int max_clusters = 0;
-  cfg.gridDim = dim3(C::kCluster);
-  if (cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg) != cudaSuccess || max_clusters < 1)
-    return BFP8_ERR_CUDA;
-  int64_t items = work_items;
-  if (p.stream_k) items = static_cast<int64_t>(work_items) * p.Kb;  // stream-K splits by K-block units
-  const int clusters = items < max_clusters ? static_cast<int>(items) : max_clusters;
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters * C::kCluster));
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, ty, p) != cudaSuccess) return BFP8_ERR_CUDA;
   return check_launch();
 }
@@ -1119,8 +1087,8 @@ void set_weight_scale(GemmParams& p, int32_t w_scale_dtype, int64_t expert_strid
   }
 }
 
-int fill_members(GemmParams& p, const MemberTable& mt, int bn, int cluster, int64_t M,
-                 const void* y, int64_t ldy) {
+int fill_members(GemmParams& p, const MemberTable& mt, int bn, int64_t M, const void* y,
+                 int64_t ldy) {
   p.n_members = mt.count;
   int tiles = 0;
   bool vec = aligned16(y) && (ldy % 8 == 0);
@@ -1134,8 +1102,7 @@ int fill_members(GemmParams& p, const MemberTable& mt, int bn, int cluster, int6
   }
   p.mem_tile0[mt.count] = tiles;
   p.m_tiles = static_cast<int32_t>((M + BM - 1) / BM);
-  const int64_t m_units = (p.m_tiles + cluster - 1) / cluster;
-  const int64_t total = m_units * tiles;
+  const int64_t total = static_cast<int64_t>(p.m_tiles) * tiles;
   if (total > 0x7FFFFFFF) return BFP8_ERR_UNSUPPORTED;
   p.total_tiles = static_cast<int32_t>(total);
   p.vec_store = vec ? 1 : 0;
@@ -1206,13 +1173,13 @@ int launch_gemm_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t s
   if (K % 16 != 0 || !aligned16(q_a) || !aligned16(w)) return BFP8_ERR_UNSUPPORTED;
   if (!fits_i32(M) || !fits_i32(N) || !fits_i32(K)) return BFP8_ERR_UNSUPPORTED;
   if (sa_sm < 0 || sa_skb < 0) return BFP8_ERR_INVALID_ARG;
-  using C8 = Cfg<kBN8, kStages8, false, false>;
-  CUtensorMap ta, tb;
-  int rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_a, K, M, K, BK, BM,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
+  int rc = check_device_ptrs({q_a, s_a, w, w_scale, y, workspace});
   if (rc != BFP8_OK) return rc;
-  // each CTA of a cluster loads (and multicasts) its share of the B tile rows
-  rc = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, K, BK, kBN8 / C8::kCluster,
+  CUtensorMap ta, tb;
+  rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_a, K, M, K, BK, BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != BFP8_OK) return rc;
+  rc = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, K, BK, kBN8,
                     CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != BFP8_OK) return rc;
   GemmParams p{};
@@ -1226,12 +1193,10 @@ int launch_gemm_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t s
   set_weight_scale(p, w_scale_dtype, 0);
   p.y = static_cast<__nv_bfloat16*>(y);
   p.ldy = ldy;
-  rc = fill_members(p, mt, kBN8, C8::kCluster, M, y, ldy);
+  rc = fill_members(p, mt, kBN8, M, y, ldy);
   if (rc != BFP8_OK) return rc;
-  if (C8::kCluster == 1) {
-    rc = sk_setup(p, p.total_tiles, kBN8, workspace, ws_bytes, stream);
-    if (rc != BFP8_OK) return rc;
-  }
+  rc = sk_setup(p, p.total_tiles, kBN8, workspace, ws_bytes, stream);
+  if (rc != BFP8_OK) return rc;
   const CUtensorMap ty{};  // unused: dense BF16 tiles are stored by the warps
   return launch<kBN8, kStages8, false, false>(ta, tb, ty, p, p.total_tiles, stream);
 }
@@ -1241,8 +1206,10 @@ int launch_gemm_w8a16(const void* x, int64_t ldx, const void* w, const void* w_s
                       int64_t ldy, const MemberTable& mt, void* stream) {
   if (K % 16 != 0 || ldx % 8 != 0 || !aligned16(x) || !aligned16(w)) return BFP8_ERR_UNSUPPORTED;
   if (!fits_i32(M) || !fits_i32(N) || !fits_i32(K)) return BFP8_ERR_UNSUPPORTED;
+  int rc = check_device_ptrs({x, w, w_scale, y});
+  if (rc != BFP8_OK) return rc;
   CUtensorMap ta, tb;
-  int rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, ldx * 2, 64, BM,
+  rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, ldx * 2, 64, BM,
                     CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != BFP8_OK) return rc;
   rc = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, K, BK, kBN16,
@@ -1257,7 +1224,7 @@ int launch_gemm_w8a16(const void* x, int64_t ldx, const void* w, const void* w_s
   set_weight_scale(p, w_scale_dtype, 0);
   p.y = static_cast<__nv_bfloat16*>(y);
   p.ldy = ldy;
-  rc = fill_members(p, mt, kBN16, Cfg<kBN16, kStages16, true, false>::kCluster, M, y, ldy);
+  rc = fill_members(p, mt, kBN16, M, y, ldy);
   if (rc != BFP8_OK) return rc;
   const CUtensorMap ty{};
   return launch<kBN16, kStages16, true, false>(ta, tb, ty, p, p.total_tiles, stream);
@@ -1272,13 +1239,14 @@ int launch_grouped_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_
   if (!fits_i32(total_M) || !fits_i32(N) || !fits_i32(K)) return BFP8_ERR_UNSUPPORTED;
   if (G < 1 || G > kMaxExperts) return BFP8_ERR_INVALID_ARG;
   if (sa_sm < 0 || sa_skb < 0) return BFP8_ERR_INVALID_ARG;
-  using CG = Cfg<kBN8, kStagesGrouped, false, true>;
-  CUtensorMap ta, tb;
-  int rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_a, K, total_M, K, BK, BM,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
+  int rc = check_device_ptrs({q_a, s_a, w, w_scale, offsets, y, workspace});
   if (rc != BFP8_OK) return rc;
-  rc = make_tmap_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, G, K, N * K, BK,
-                    kBN8 / CG::kCluster, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+  CUtensorMap ta, tb;
+  rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_a, K, total_M, K, BK, BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != BFP8_OK) return rc;
+  rc = make_tmap_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, N, G, K, N * K, BK, kBN8, 1,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != BFP8_OK) return rc;
   GemmParams p{};
   p.M = static_cast<int32_t>(total_M);
@@ -1297,12 +1265,10 @@ int launch_grouped_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_
   p.N = static_cast<int32_t>(N);
   p.n_tiles = static_cast<int32_t>((N + kBN8 - 1) / kBN8);
   p.n_members = 1;
-  if (CG::kCluster == 1) {
-    const int64_t tile_bound = ((total_M + BM - 1) / BM + G) * p.n_tiles;
-    rc = sk_setup(p, tile_bound, kBN8, workspace, ws_bytes, stream);
-    if (rc != BFP8_OK) return rc;
-  }
-  // the work-item count is only known on the device: launch every resident cluster
+  const int64_t tile_bound = ((total_M + BM - 1) / BM + G) * p.n_tiles;
+  rc = sk_setup(p, tile_bound, kBN8, workspace, ws_bytes, stream);
+  if (rc != BFP8_OK) return rc;
+  // the work-item count is only known on the device: launch every resident CTA
   CUtensorMap ty{};
   if (p.vec_store && total_M > 0 && N > 0) {
     // 32-row x 64-column boxes (128 bytes, the swizzle span) of y [total_M, N]
@@ -1349,9 +1315,11 @@ int launch_gemm_w8a8_swiglu(const void* q_a, const float* s_a, int64_t sa_sm, in
   if (K % 16 != 0 || !aligned16(q_a) || !aligned16(w)) return BFP8_ERR_UNSUPPORTED;
   if (!fits_i32(M) || !fits_i32(2 * I) || !fits_i32(K)) return BFP8_ERR_UNSUPPORTED;
   if (sa_sm < 0 || sa_skb < 0 || sh_sm < 0 || sh_skb < 0) return BFP8_ERR_INVALID_ARG;
+  int rc = check_device_ptrs({q_a, s_a, w, w_scale, q_h, s_h, workspace});
+  if (rc != BFP8_OK) return rc;
   CUtensorMap ta, tb;
-  int rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_a, K, M, K, BK, BM,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
+  rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_a, K, M, K, BK, BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != BFP8_OK) return rc;
   // gate and up halves of a B tile are separate 128-row boxes
   rc = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, 2 * I, K, BK, kBN8 / 2,
@@ -1373,7 +1341,7 @@ int launch_gemm_w8a8_swiglu(const void* q_a, const float* s_a, int64_t sa_sm, in
   mt.rows[0] = I;
   mt.sbase[0] = 0;
   mt.scale_rows = (I + 127) / 128;
-  rc = fill_members(p, mt, kBN8 / 2, 1, M, nullptr, 0);
+  rc = fill_members(p, mt, kBN8 / 2, M, nullptr, 0);
   if (rc != BFP8_OK) return rc;
   fill_swiglu(p, I, q_h, ldq, s_h, sh_sm, sh_skb);
   rc = sk_setup(p, p.total_tiles, kBN8, workspace, ws_bytes, stream);
@@ -1391,9 +1359,11 @@ int launch_grouped_w8a8_swiglu(const void* q_a, const float* s_a, int64_t sa_sm,
   if (!fits_i32(total_M) || !fits_i32(2 * I) || !fits_i32(K)) return BFP8_ERR_UNSUPPORTED;
   if (G < 1 || G > kMaxExperts) return BFP8_ERR_INVALID_ARG;
   if (sa_sm < 0 || sa_skb < 0 || sh_sm < 0 || sh_skb < 0) return BFP8_ERR_INVALID_ARG;
+  int rc = check_device_ptrs({q_a, s_a, w, w_scale, offsets, q_h, s_h, workspace});
+  if (rc != BFP8_OK) return rc;
   CUtensorMap ta, tb;
-  int rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_a, K, total_M, K, BK, BM,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
+  rc = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_a, K, total_M, K, BK, BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != BFP8_OK) return rc;
   rc = make_tmap_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K, 2 * I, G, K, 2 * I * K, BK,
                     kBN8 / 2, 1, CU_TENSOR_MAP_SWIZZLE_128B);

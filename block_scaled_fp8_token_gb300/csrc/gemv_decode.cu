@@ -709,9 +709,11 @@ int launch_gemv(const void* x, int64_t ldx, const void* w, const void* w_scale,
                 const MemberTable& mt, void* workspace, size_t ws_bytes, void* stream, bool silu) {
   if (ldx % 8 != 0 || reinterpret_cast<uintptr_t>(x) % 16 != 0) return BFP8_ERR_UNSUPPORTED;
   if (silu && K % 8 != 0) return BFP8_ERR_UNSUPPORTED;
+  int rc = check_device_ptrs({x, w, w_scale, y, workspace});
+  if (rc != BFP8_OK) return rc;
   GemvParams p{};
   int sms = 0;
-  int rc = init_params(p, w, w_scale, w_scale_dtype, M, N, K, y, ldy, mt, workspace, ws_bytes, &sms);
+  rc = init_params(p, w, w_scale, w_scale_dtype, M, N, K, y, ldy, mt, workspace, ws_bytes, &sms);
   if (rc != BFP8_OK) return rc;
   uint8_t* xtile = static_cast<uint8_t*>(workspace) + ws_layout(N, K, sms).xtile;
   CUtensorMap tw, tx;
@@ -731,9 +733,11 @@ int launch_gemv_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t s
                      void* workspace, size_t ws_bytes, void* stream) {
   if (reinterpret_cast<uintptr_t>(q_a) % 16 != 0) return BFP8_ERR_UNSUPPORTED;
   if (sa_sm < 0 || sa_skb < 0) return BFP8_ERR_INVALID_ARG;
+  int rc = check_device_ptrs({q_a, s_a, w, w_scale, y, workspace});
+  if (rc != BFP8_OK) return rc;
   GemvParams p{};
   int sms = 0;
-  int rc = init_params(p, w, w_scale, w_scale_dtype, M, N, K, y, ldy, mt, workspace, ws_bytes, &sms);
+  rc = init_params(p, w, w_scale, w_scale_dtype, M, N, K, y, ldy, mt, workspace, ws_bytes, &sms);
   if (rc != BFP8_OK) return rc;
   p.s_a = s_a;
   p.sa_sm = sa_sm;
@@ -823,8 +827,10 @@ int launch_decode_ffn(int32_t arith, const void* x, int64_t ldx, const void* w_g
   if (!weight_scale_dtype_ok(w_scale_dtype)) return BFP8_ERR_SCALE_DTYPE;
   if (H % 16 != 0 || I % 16 != 0) return BFP8_ERR_UNSUPPORTED;
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return BFP8_ERR_INVALID_ARG;
+  int rc = check_device_ptrs({x, w_gu, s_gu, w_dn, s_dn, y, workspace});
+  if (rc != BFP8_OK) return rc;
   int sms = 0;
-  int rc = sm_count(&sms);
+  rc = sm_count(&sms);
   if (rc != BFP8_OK) return rc;
   const DecodeFfnLayout l = decode_ffn_layout(M, H, I, arith, sms);
   if (ws_bytes < l.total) return BFP8_ERR_INVALID_ARG;
@@ -876,26 +882,29 @@ namespace {
 
 constexpr int kNoAllocMaxDevices = 64;
 
-struct NoAllocSlot {
-  std::once_flag once;
-  void* ptr = nullptr;
-  cudaError_t err = cudaSuccess;
-};
-NoAllocSlot g_noalloc_slots[kNoAllocMaxDevices];
+// The device address of the array on each device, once a lookup succeeded.
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+std::mutex g_noalloc_mutex;
 
 // The host-side name of a __device__ array is only a stand-in, not a device
-// address, so look the real address up once per device, with that device
-// current (the first call on each device does this).
+// address, so look the real address up per device, with that device current.
+// Only a successful lookup is kept: a failed one (for instance a first call
+// made under stream capture) returns BFP8_ERR_CUDA, clears its error and is
+// tried again by the next call.
 int noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return BFP8_ERR_CUDA;
   if (dev < 0 || dev >= kNoAllocMaxDevices) return BFP8_ERR_UNSUPPORTED;
-  NoAllocSlot& slot = g_noalloc_slots[dev];
-  std::call_once(slot.once, [&slot] {
-    slot.err = cudaGetSymbolAddress(&slot.ptr, g_gemv_noalloc_scratch);
-  });
-  if (slot.err != cudaSuccess || slot.ptr == nullptr) return BFP8_ERR_CUDA;
-  *out = slot.ptr;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_gemv_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return BFP8_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
   return BFP8_OK;
 }
 

@@ -1,6 +1,7 @@
 // ptx.cuh -- inline-PTX building blocks for sm_103a kernels: mbarriers with
-// bounded waits, TMA tensor loads, tcgen05 (TMEM alloc, MMA, commit, loads),
-// legacy mma.sync for the small-M GEMV, and the exact E4M3 -> BF16 decode.
+// bounded waits, TMA tensor loads and stores, tcgen05 (TMEM alloc, MMA,
+// commit, loads) and the exact E4M3 -> BF16 decode. Every copy is CTA-local:
+// one CTA per SM, no thread-block clusters.
 #pragma once
 
 #include <cuda.h>
@@ -154,37 +155,6 @@ BFP8_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t c0, int3
 }
 
 
-// TMA load multicast to every CTA in `mask` (same shared-memory offset and
-// same mbarrier offset in each destination CTA of the cluster).
-BFP8_DEV void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
-                             uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
-      : "memory");
-}
-BFP8_DEV void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
-                             int32_t c2, uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "h"(mask)
-      : "memory");
-}
-
-// ---------------------------------------------------------------- clusters
-BFP8_DEV uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Cluster-wide barrier: every thread of every CTA in the cluster.
-BFP8_DEV void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-
 // ---------------------------------------------------------------- tcgen05
 // TMEM allocation is warp-collective; the allocated base address is written
 // to shared memory at `slot`.
@@ -257,14 +227,6 @@ BFP8_DEV void umma_commit(uint32_t bar) {
       : "memory");
 }
 
-// Same, arriving on the mbarrier at this offset in every CTA of `mask`.
-BFP8_DEV void umma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(mask)
-      : "memory");
-}
-
 // 32 consecutive FP32 columns of this thread's TMEM lane, waited on before the
 // values are returned (the wait sits in the same asm statement, so no use of
 // the registers can be scheduled before it).
@@ -322,56 +284,29 @@ BFP8_DEV uint32_t e4m3x2_to_f16x2(uint16_t pair) {
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(pair));
   return h;
 }
-// Two F16 values that came from E4M3 codes -> two BF16, exactly. Keeping the
-// sign and moving the 5-bit exponent and top mantissa bits into BF16 position
-// gives a normal BF16 equal to the value times 2^-112 (zero stays zero); one
-// exact multiply by 2^112 (BF16 0x7780) restores it. E4M3 NaN codes come out
-// finite; the decode is exact for every finite code.
-BFP8_DEV uint32_t f16x2_to_bf16x2_e4m3range(uint32_t h) {
-  const uint32_t b = (h & 0x80008000u) | ((h >> 3) & 0x0FFF0FFFu);
+// Two F16 values that came from E4M3 codes -> two BF16, exactly: widened to
+// FP32 (exact) and packed with one round-to-nearest conversion, which is exact
+// too because an E4M3 value has at most 4 significant bits and lies well inside
+// the BF16 range. The E4M3 NaN codes (0x7F, 0xFF) are F16 NaNs after the first
+// conversion and come out as BF16 NaN, so a NaN weight propagates through the
+// BF16 MMA exactly as it does through the FP8 one.
+BFP8_DEV uint32_t f16x2_to_bf16x2_exact(uint32_t h) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
   uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(b), "r"(0x77807780u));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(f.y), "f"(f.x));
   return r;
 }
 // Four E4M3 codes packed little-endian -> BF16 pairs: lo = (byte0, byte1),
 // hi = (byte2, byte3), lower-addressed element in the low half.
 BFP8_DEV void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  lo = f16x2_to_bf16x2_e4m3range(e4m3x2_to_f16x2(static_cast<uint16_t>(w & 0xFFFFu)));
-  hi = f16x2_to_bf16x2_e4m3range(e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16)));
+  lo = f16x2_to_bf16x2_exact(e4m3x2_to_f16x2(static_cast<uint16_t>(w & 0xFFFFu)));
+  hi = f16x2_to_bf16x2_exact(e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16)));
 }
 // Two float32 -> two E4M3 codes, round to nearest even, saturating to +-448.
 // `a` goes to byte 0 (lower address), `b` to byte 1.
 BFP8_DEV uint16_t f32x2_to_e4m3x2(float a, float b) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
-  return r;
-}
-
-// Legacy warp-level BF16 MMA (m16n8k16, FP32 accumulate), used only by the
-// memory-bound small-M GEMV.
-BFP8_DEV void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                             uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// The same MMA on F16 operands.
-BFP8_DEV void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                            uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// Two float32 -> packed F16 (round to nearest even); `a` in the low half.
-BFP8_DEV uint32_t f32x2_to_f16x2(float a, float b) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
   return r;
 }
 

@@ -168,6 +168,43 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(
   }
 }
 
+// h[m, c] = bf16(silu(gu[m, c]) * gu[m, I + c]) for the W8A16 arm (no
+// quantization). Each thread owns 8 consecutive columns of one row; with
+// `vec`, 16-byte loads and stores.
+__global__ void __launch_bounds__(kThreads) silu_mul_kernel(
+    const __nv_bfloat16* __restrict__ gu, int64_t M, int64_t I, int64_t ld,
+    __nv_bfloat16* __restrict__ h, int64_t ldh, int vec) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t cpr = (I + 7) / 8;  // 8-column chunks per row
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t it = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; it < M * cpr;
+       it += step) {
+    const int64_t m = it / cpr;
+    const int64_t c = (it - m * cpr) * 8;
+    const __nv_bfloat16* row = gu + m * ld;
+    uint32_t g[4], u[4];
+    load_chunk<false>(row, c, I, vec, g);
+    load_chunk<false>(row + I, c, I, vec, u);
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float h0 = silu_mul_bf16_round(lo_bf16(g[j]), lo_bf16(u[j]));
+      const float h1 = silu_mul_bf16_round(hi_bf16(g[j]), hi_bf16(u[j]));
+      o[j] = (__float_as_uint(h0) >> 16) | (__float_as_uint(h1) & 0xFFFF0000u);
+    }
+    __nv_bfloat16* dst = h + m * ldh + c;
+    if (vec && c + 8 <= I) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+      uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (c + e < I) d16[e] = static_cast<uint16_t>(o[e >> 1] >> (16 * (e & 1)));
+    }
+  }
+}
+
 // One CTA per 128x128 weight block. Pass 1 finds the block maximum; pass 2
 // writes the codes against the stored (BF16-rounded or F32) scale.
 __global__ void __launch_bounds__(kThreads) weight_quant_kernel(
@@ -358,8 +395,10 @@ int act_quant_common(bool silu, const void* x, int64_t M, int64_t K, int64_t ld,
   const int64_t Kb = (K + 127) / 128;
   if (ssm < 0 || sskb < 0 || (M > 1 && ssm == 0) || (Kb > 1 && sskb == 0))
     return BFP8_ERR_INVALID_ARG;
+  int rc = check_device_ptrs({x, q, s, rows});
+  if (rc != BFP8_OK) return rc;
   int sms = 0;
-  int rc = sm_count(&sms);
+  rc = sm_count(&sms);
   if (rc != BFP8_OK) return rc;
   const int vec_in = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (ld % 8 == 0) && (K % 8 == 0);
   const int vec_out = (reinterpret_cast<uintptr_t>(q) % 8 == 0) && (ldq % 8 == 0);
@@ -396,6 +435,30 @@ int launch_silu_mul_act_quant(const void* gu, int64_t M, int64_t I, int64_t ld, 
   return act_quant_common(true, gu, M, I, ld, q, ldq, s, ssm, sskb, stream);
 }
 
+int launch_silu_mul(const void* gu, int64_t M, int64_t I, int64_t ld, void* h, int64_t ldh,
+                    void* stream) {
+  if (M < 0 || I < 0) return BFP8_ERR_INVALID_ARG;
+  if (M == 0 || I == 0) return BFP8_OK;
+  if (!gu || !h || ld < 2 * I || ldh < I) return BFP8_ERR_INVALID_ARG;
+  int rc = check_device_ptrs({gu, h});
+  if (rc != BFP8_OK) return rc;
+  int sms = 0;
+  rc = sm_count(&sms);
+  if (rc != BFP8_OK) return rc;
+  const int vec = (reinterpret_cast<uintptr_t>(gu) % 16 == 0) && (ld % 8 == 0) && (I % 8 == 0) &&
+                  (reinterpret_cast<uintptr_t>(h) % 16 == 0) && (ldh % 8 == 0);
+  static const int per_sm = resident_blocks(silu_mul_kernel);
+  const int64_t items = M * ((I + 7) / 8);
+  const int64_t want = (items + kThreads - 1) / kThreads;
+  const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+  const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
+  rc = launch_dependent(silu_mul_kernel, blocks, static_cast<cudaStream_t>(stream),
+                        static_cast<const __nv_bfloat16*>(gu), M, I, ld,
+                        static_cast<__nv_bfloat16*>(h), ldh, vec);
+  if (rc != BFP8_OK) return rc;
+  return check_launch();
+}
+
 int launch_moe_gather_act_quant(const void* x, int64_t T, int64_t H, int64_t ldx,
                                 const int32_t* row_token, int64_t R, void* q, int64_t ldq,
                                 float* s, int64_t ssm, int64_t sskb, void* stream) {
@@ -411,8 +474,10 @@ int launch_moe_combine(const void* y, int64_t R, int64_t H, int64_t ldy, const i
   if (R < 0 || H < 0 || T < 0 || topk < 1) return BFP8_ERR_INVALID_ARG;
   if (T == 0 || H == 0) return BFP8_OK;
   if (!y || !token_rows || !token_weights || !out || ldy < H || ldo < H) return BFP8_ERR_INVALID_ARG;
+  int rc = check_device_ptrs({y, token_rows, token_weights, out});
+  if (rc != BFP8_OK) return rc;
   int sms = 0;
-  int rc = sm_count(&sms);
+  rc = sm_count(&sms);
   if (rc != BFP8_OK) return rc;
   const int vec = (reinterpret_cast<uintptr_t>(y) % 16 == 0) && (ldy % 8 == 0) &&
                   (reinterpret_cast<uintptr_t>(out) % 16 == 0) && (ldo % 8 == 0);
@@ -437,6 +502,8 @@ int launch_weight_quant(const float* w, int64_t N, int64_t K, int64_t ldw, void*
   if (scale_dtype != BFP8_DT_BF16 && scale_dtype != BFP8_DT_F32) return BFP8_ERR_SCALE_DTYPE;
   const int64_t Nb = (N + 127) / 128, Kb = (K + 127) / 128;
   if (Nb > 65535 || Kb > 0x7FFFFFFF) return BFP8_ERR_UNSUPPORTED;
+  const int rc = check_device_ptrs({w, q, scale});
+  if (rc != BFP8_OK) return rc;
   dim3 grid(static_cast<unsigned>(Kb), static_cast<unsigned>(Nb));
   weight_quant_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       w, N, K, ldw, static_cast<uint8_t*>(q), ldq, scale, scale_dtype == BFP8_DT_F32, Kb);

@@ -161,13 +161,31 @@ int bfp8_act_quant_group(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
  * projections of the dense FFN [Module w8a8_prefill, first paragraph: the
  * gate/up/down GEMM arm].
  *   gu_bf16 [M, 2I] BF16 (gate columns 0..I-1, up columns I..2I-1), row stride ld
- *   h = bf16_rn( silu(g) * u ) with silu(g) = g / (1 + exp(-g)) in float32,
- *   then the same quantization as bfp8_act_quant_group over [M, I].
+ *   h = bf16_rn( silu(g) * u ), silu(g) = g / (1 + exp(-g)), the value of the
+ *   definition evaluated in double and rounded once to BF16 (see bfp8_silu_mul),
+ *   then the same quantization as bfp8_act_quant_group over [M, I]. Codes and
+ *   scales are bit-exact with the CPU oracle for finite inputs.
  * Output arguments as for bfp8_act_quant_group with K = I.
  */
 int bfp8_silu_mul_act_quant(const void* gu_bf16, int64_t M, int64_t I, int64_t ld,
                             void* q_e4m3, int64_t ldq, float* scales,
                             int64_t s_stride_m, int64_t s_stride_kb, void* stream);
+
+/*
+ * bfp8_silu_mul -- the same glue for the W8A16 arm, whose down projection
+ * takes BF16 activations: h = bf16_rn( silu(g) * u ) without quantization.
+ *   [Module w8a8_prefill, first paragraph: the gate/up/down arm]
+ *   [FP8 Native Serving, "Native FP8 vs dequant-to-BF16": BF16 activations]
+ *   gu_bf16 [M, 2I] BF16, row stride ld >= 2I; h_bf16 [M, I], row stride ldh >= I
+ * Each element is bit-identical to g / (1 + exp(-g)) * u evaluated in double
+ * (g, u widened exactly from BF16) and rounded once to BF16, nearest-even.
+ * The kernel computes it in float32 with an error bound and recomputes in
+ * double the rare elements that lie too close to a BF16 rounding boundary.
+ * M == 0 or I == 0 is a no-op. Errors: INVALID_ARG (null pointers, negative
+ * sizes, ld < 2I, ldh < I, memory that is not on the current device).
+ */
+int bfp8_silu_mul(const void* gu_bf16, int64_t M, int64_t I, int64_t ld, void* h_bf16,
+                  int64_t ldh, void* stream);
 
 /* ---- ahead-of-time weight block quantization (conversion endpoint) ------ */
 /*
@@ -347,12 +365,18 @@ int bfp8_decode_ffn(int32_t arith, const void* x_bf16, int64_t ldx, const void* 
  * device array of BFP8_GEMV_NOALLOC_SCRATCH_BYTES compiled into the library.
  * Every GPU that loads libbfp8.so holds that array until the process exits.
  *  - Limit: the problem must need at most BFP8_GEMV_NOALLOC_SCRATCH_BYTES of
- *    scratch, i.e. bfp8_gemv_decode_workspace(M, N, K) <= 4 MiB. On a
- *    152-SM GB300 that holds any N up to about 54 million rows. Larger
- *    problems return BFP8_ERR_UNSUPPORTED before any GPU work.
- *  - The first call on each device does a one-time set-up: it looks up the
- *    array's device address with cudaGetSymbolAddress. Make that first call
- *    before capturing any stream.
+ *    scratch; bfp8_gemv_decode_workspace(M, N, K) <= 4 MiB is the exact test.
+ *    The scratch holds, each part rounded up to 256 bytes: 4 bytes per
+ *    128-row tile of W (4 * ceil(N/128)), two 128 x 16 float32 partial tiles
+ *    per SM (2.49 MB on a 152-SM GB300), and 4096 + 64 bytes of token tiles
+ *    and factors per 128-column block of K (4160 * ceil(K/128)). On 152 SMs
+ *    that allows K up to 52,352 at N = 5120, and N up to about 36 million
+ *    rows at K = 17,408. Larger problems return BFP8_ERR_UNSUPPORTED before
+ *    any GPU work.
+ *  - The first successful call on each device does a one-time set-up: it
+ *    looks up the array's device address with cudaGetSymbolAddress and keeps
+ *    it. Make that first call before capturing any stream. A lookup that
+ *    fails returns BFP8_ERR_CUDA and is tried again on the next call.
  *  - All calls on one device share the array, and each call clears the
  *    counters it needs on its stream before the kernel runs. Calls that
  *    overlap on the GPU (two streams, or two host threads without ordering)

@@ -29,6 +29,11 @@ def _too_small(fn, *args, **kw):
         fn(*args, **kw)
 
 
+def _bad_layout(fn, *args, **kw):
+    with pytest.raises(ValueError, match="has shape|strides|per-tensor scale needs"):
+        fn(*args, **kw)
+
+
 def test_valid_dense_calls_pass_the_extent_checks(bfp8):
     x = torch.zeros(M, K, dtype=bf16)
     q = torch.zeros(M, K, dtype=u8)
@@ -96,17 +101,55 @@ def test_tensors_too_small_for_the_call_are_refused(bfp8):
                s_stride_m=1, s_stride_kb=M)
     w = torch.zeros(N, K, dtype=u8)
     y = torch.zeros(M, N, dtype=bf16)
-    _too_small(bfp8.bfp8_linear_w8a8, q, s, w, torch.zeros(Nb - 1, Kb, dtype=bf16), y)
+    _bad_layout(bfp8.bfp8_linear_w8a8, q, s, w, torch.zeros(Nb - 1, Kb, dtype=bf16), y)
     _too_small(bfp8.bfp8_linear_w8a8, q, s, w, torch.zeros(Nb, Kb, dtype=bf16), y[: M - 1])
-    _too_small(bfp8.bfp8_linear_w8a8, q, s, w, torch.zeros(3, Kb, dtype=bf16), y,
-               member_rows=[200, 184])                                # needs 4 grid rows
+    _bad_layout(bfp8.bfp8_linear_w8a8, q, s, w, torch.zeros(3, Kb, dtype=bf16), y,
+                member_rows=[200, 184])                               # needs 4 grid rows
     _too_small(bfp8.bfp8_quantize_weight_block, torch.zeros(N, K, dtype=bf16),  # read as f32
                torch.zeros(N, K, dtype=u8), torch.zeros(Nb, Kb, dtype=bf16))
     G, T = 4, 50
     off = torch.tensor([0, 10, 10, 30], dtype=i32)                     # needs G + 1 entries
-    _too_small(bfp8.bfp8_grouped_linear, torch.zeros(T, K, dtype=u8), torch.zeros(T, Kb, dtype=f32),
+    _bad_layout(bfp8.bfp8_grouped_linear, torch.zeros(T, K, dtype=u8), torch.zeros(T, Kb, dtype=f32),
                torch.zeros(G, N, K, dtype=u8), torch.zeros(G, Nb, Kb, dtype=bf16), off,
                torch.zeros(T, N, dtype=bf16))
-    _too_small(bfp8.bfp8_moe_combine, torch.zeros(12, 256, dtype=bf16),
-               torch.zeros(4, 3, dtype=i32), torch.zeros(4, 2, dtype=f32),
-               torch.zeros(4, 256, dtype=bf16))
+    _bad_layout(bfp8.bfp8_moe_combine, torch.zeros(12, 256, dtype=bf16),
+                torch.zeros(4, 3, dtype=i32), torch.zeros(4, 2, dtype=f32),
+                torch.zeros(4, 256, dtype=bf16))
+
+
+def test_layouts_the_library_would_misread_are_refused(bfp8):
+    """The kernels read weights, quantized activations and scale grids as dense
+    row-major data with the pitch implied by K. A transposed grid, a column
+    slice of a wider weight, or a transposed activation would be misread
+    silently, so the binding refuses them by shape and stride."""
+    q = torch.zeros(M, K, dtype=u8)
+    s = torch.zeros(M, Kb, dtype=f32)
+    w = torch.zeros(N, K, dtype=u8)
+    y = torch.zeros(M, N, dtype=bf16)
+    K2 = 256                                             # Kb = 2, Nb = 3: the transpose has another shape
+    q2, s2, w2 = torch.zeros(M, K2, dtype=u8), torch.zeros(M, 2, dtype=f32), torch.zeros(N, K2, dtype=u8)
+    _bad_layout(bfp8.bfp8_linear_w8a8, q2, s2, w2, torch.zeros(2, Nb, dtype=bf16), y)   # [Kb, Nb]
+    _bad_layout(bfp8.bfp8_linear_w8a8, q, s, w, torch.zeros(Kb, Nb, dtype=bf16).t(), y)  # .t() view
+    wide = torch.zeros(N, K + 64, dtype=u8)
+    _bad_layout(bfp8.bfp8_linear_w8a8, q, s, wide[:, :K], torch.zeros(Nb, Kb, dtype=bf16), y)
+    _bad_layout(bfp8.bfp8_linear_w8a16, torch.zeros(M, K, dtype=bf16), wide[:, :K],
+                torch.zeros(Nb, Kb, dtype=bf16), y)
+    _bad_layout(bfp8.bfp8_gemv_decode, torch.zeros(4, K, dtype=bf16), w.t().contiguous().t(),
+                torch.zeros(Nb, Kb, dtype=bf16), y[:4], torch.zeros(1 << 16, dtype=u8))
+    _bad_layout(bfp8.bfp8_linear_w8a8, torch.zeros(K, M, dtype=u8).t(), s, w,
+                torch.zeros(Nb, Kb, dtype=bf16), y)               # transposed activations
+    with pytest.raises(ValueError, match="contiguous columns"):
+        bfp8.bfp8_linear_w8a16(torch.zeros(K, M, dtype=bf16).t(), w,
+                               torch.zeros(Nb, Kb, dtype=bf16), y)
+    with pytest.raises(ValueError, match="contiguous columns"):
+        bfp8.bfp8_linear_w8a8(q, s, w, torch.zeros(Nb, Kb, dtype=bf16),
+                              torch.zeros(N, M, dtype=bf16).t())  # transposed output
+    G, T = 4, 50
+    off = torch.tensor([0, 10, 10, 30, 50], dtype=i32)
+    _bad_layout(bfp8.bfp8_grouped_linear, torch.zeros(T, K2, dtype=u8), torch.zeros(T, 2, dtype=f32),
+                torch.zeros(G, N, K2, dtype=u8), torch.zeros(G, 2, Nb, dtype=bf16), off,
+                torch.zeros(T, N, dtype=bf16))                   # per-expert grids transposed
+    _bad_layout(bfp8.bfp8_grouped_linear, torch.zeros(T, K, dtype=u8), torch.zeros(T, Kb, dtype=f32),
+                torch.zeros(G, N, K, dtype=u8), torch.ones(G - 1, dtype=f32), off,
+                torch.zeros(T, N, dtype=bf16))                   # one multiplier per expert
+

@@ -1,9 +1,11 @@
 """GPU parity: quantizers against the CPU oracle.
 
-bfp8_act_quant_group and bfp8_quantize_weight_block must be bit-exact: codes
-and scales. bfp8_silu_mul_act_quant computes SiLU with the GPU's expf and the
-oracle in float64, so the two can differ by one BF16 ulp of h near a rounding
-point. It is checked by the E4M3 error bound and near-total byte equality.
+bfp8_act_quant_group, bfp8_quantize_weight_block and bfp8_silu_mul_act_quant
+must be bit-exact: codes and scale bits. So must bfp8_silu_mul's BF16 h: the
+oracle evaluates silu(g) * u in float64 and rounds once, and the GPU must give
+the same bits on every finite input, including the products that fall next to
+a BF16 rounding midpoint (where a float32 evaluation alone could round the
+other way).
 """
 
 import numpy as np
@@ -86,24 +88,87 @@ def test_weight_quant_bit_exact(bfp8, cuda_device, N, K, dtype):
     assert np.array_equal(got_s, sr)
 
 
-@pytest.mark.parametrize("M,I", [(8, 256), (949, 17408), (33, 768), (3, 100)])
-def test_silu_mul_act_quant(bfp8, cuda_device, M, I):
-    gu = bits16(synth.activations_bf16(synth.generator(M + I), M, 2 * I))
-    x = to_dev_bf16(gu, cuda_device)
-    Kb = -(-I // 128)
-    q = torch.zeros(M, I, dtype=torch.uint8, device=cuda_device)
-    s = torch.zeros(M, Kb, dtype=torch.float32, device=cuda_device)
+def _silu_quant(bfp8, dev, gu):
+    M, I = gu.shape[0], gu.shape[1] // 2
+    x = to_dev_bf16(gu, dev)
+    q = torch.zeros(M, I, dtype=torch.uint8, device=dev)
+    s = torch.zeros(M, -(-I // 128), dtype=torch.float32, device=dev)
     bfp8.bfp8_silu_mul_act_quant(x, q, s)
     torch.cuda.synchronize()
-    q, s = q.cpu().numpy(), s.cpu().numpy()
-    h = F.bf16_bits_to_f32(Q.silu_mul_bf16(gu)).astype(np.float64)
+    return q.cpu().numpy(), s.cpu().numpy()
+
+
+@pytest.mark.parametrize("M,I", [(8, 256), (949, 17408), (33, 768), (3, 100), (65536, 768)])
+def test_silu_mul_act_quant(bfp8, cuda_device, M, I):
+    """The dense-FFN glue (949 x 17408) and the MoE glue over all routed rows
+    (65,536 x 768), bit-exact on codes and scale bits."""
+    gu = bits16(synth.activations_bf16(synth.generator(M + I), M, 2 * I))
+    q, s = _silu_quant(bfp8, cuda_device, gu)
     qr, sr = Q.act_quant_group(Q.silu_mul_bf16(gu))
-    assert np.mean(q == qr) >= 0.999
-    assert np.allclose(s, sr, rtol=2 ** -7, atol=0)
-    sfull = np.repeat(s.astype(np.float64), 128, axis=1)[:, :I]
-    deq = dec_e4m3(q) * sfull
-    bound = 2 ** -4 * np.abs(h) * (1 + 2 ** -6) + sfull * 2 ** -9
-    assert np.all(np.abs(deq - h) <= bound)
+    assert np.array_equal(s.view(np.uint32), sr.view(np.uint32))
+    assert np.array_equal(q, qr)
+
+
+def _silu_hard_pairs(limit: int, rel: float = 2.0 ** -19):
+    """(g, u) BF16 bit pairs whose product silu(g) * u lies within `rel` of a
+    BF16 rounding midpoint: the inputs where a float32 evaluation with a few
+    ulps of error could round to the wrong neighbour. Found by brute force over
+    every finite BF16 g in [-64, 64) and every u in [1, 2)."""
+    gb = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
+    g = F.bf16_bits_to_f32(gb).astype(np.float64)
+    keep = np.isfinite(g) & (np.abs(g) < 64) & (g != 0)
+    gb, g = gb[keep], g[keep]
+    ub = np.arange(0x3F80, 0x4000, dtype=np.uint16)           # every u in [1, 2)
+    u = F.bf16_bits_to_f32(ub).astype(np.float64)
+    p = (g / (1.0 + np.exp(-g)))[:, None] * u[None, :]
+    a = np.abs(p)
+    e = np.floor(np.log2(a))
+    step = 2.0 ** (np.maximum(e, -126) - 7)                    # BF16 spacing at p
+    frac = a / step - np.floor(a / step)                       # position between neighbours
+    hard = np.abs(frac - 0.5) * step <= rel * a
+    gi, ui = np.nonzero(hard)
+    order = np.random.default_rng(11).permutation(gi.size)[:limit]
+    return gb[gi[order]], ub[ui[order]]
+
+
+def test_silu_mul_near_bf16_midpoints(bfp8, cuda_device):
+    """Rows built from the hardest (g, u) pairs, with random signs on u: both
+    bfp8_silu_mul's h and bfp8_silu_mul_act_quant's codes and scales must be
+    exact."""
+    g, u = _silu_hard_pairs(64 * 1024)
+    assert g.size >= 20000, g.size
+    n = (g.size // 1024) * 1024
+    signs = (np.random.default_rng(3).integers(0, 2, n).astype(np.uint16) << 15)
+    gu = np.concatenate([g[:n].reshape(-1, 1024), (u[:n] | signs).reshape(-1, 1024)], axis=1)
+    h = torch.empty(gu.shape[0], 1024, dtype=torch.bfloat16, device=cuda_device)
+    bfp8.bfp8_silu_mul(to_dev_bf16(gu, cuda_device), h)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits16(h), Q.silu_mul_bf16(gu))
+    q, s = _silu_quant(bfp8, cuda_device, gu)
+    qr, sr = Q.act_quant_group(Q.silu_mul_bf16(gu))
+    assert np.array_equal(s.view(np.uint32), sr.view(np.uint32))
+    assert np.array_equal(q, qr)
+
+
+def test_silu_mul_every_bf16_gate(bfp8, cuda_device):
+    """Every finite BF16 gate value g (all 65,536 patterns but inf and NaN,
+    subnormals and the largest magnitudes included) against every up value u
+    in [1, 2) and their negatives: 16.7 million products, each h bit-exact."""
+    gb = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
+    gb = gb[np.isfinite(F.bf16_bits_to_f32(gb))]
+    I = gb.size
+    ub = np.arange(0x3F80, 0x4000, dtype=np.uint16)
+    ub = np.concatenate([ub, ub | np.uint16(0x8000)])
+    gu = np.empty((ub.size, 2 * I), np.uint16)
+    gu[:, :I] = gb[None, :]
+    gu[:, I:] = ub[:, None]
+    h = torch.empty(ub.size, I, dtype=torch.bfloat16, device=cuda_device)
+    bfp8.bfp8_silu_mul(to_dev_bf16(gu, cuda_device), h)
+    torch.cuda.synchronize()
+    got, ref = bits16(h), Q.silu_mul_bf16(gu)
+    bad = got != ref
+    assert not bad.any(), (int(bad.sum()), [(hex(gu[r, c]), hex(gu[r, I + c]), hex(got[r, c]),
+                                            hex(ref[r, c])) for r, c in np.argwhere(bad)[:5]])
 
 
 def _near_midpoint_groups(seed=5, n_amax=3000, rel=2.0 ** -22, limit_rows=256):
