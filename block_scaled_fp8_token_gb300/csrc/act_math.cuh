@@ -24,13 +24,13 @@ namespace dev {
 // |s - silu(g)| <= 2^-22.2 |silu(g)|, so p is within 2^-22.2 + 2^-24 (relative)
 // of silu(g) u: under 4.5 units in the last place of p. RN_bf16(p) is the
 // correctly rounded result unless a BF16 rounding midpoint lies that close to
-// p, i.e. unless p's low 16 bits lie near 0x8000 (kSiluMidUlps = 8 gives
-// margin). Those elements (about 2^-12 of them) and g outside the range are
-// recomputed in double. The check works on FP32 subnormals too: there every
+// p, i.e. unless p's low 16 bits lie within 4.5 of 0x8000; kSiluMidUlps = 5
+// flags every p within 5 units. Those elements (11 in 65536 of them) and g
+// outside the range are recomputed in double. The check works on FP32 subnormals too: there every
 // rounding is at most half a unit of the fixed subnormal spacing.
 constexpr float kNegLog2eHi = -1.44268798828125f;   // -23637 / 16384
 constexpr float kNegLog2eLoLn2 = -0x1.480fb6p-18f;  // (-log2(e) - kNegLog2eHi) * ln 2
-constexpr uint32_t kSiluMidUlps = 8;
+constexpr uint32_t kSiluMidUlps = 5;
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float r;
@@ -106,10 +106,18 @@ __device__ __forceinline__ float group_scale(float amax) {
 // theorem assumes no underflow; a quotient in the FP32 subnormal range is
 // below 2^-126, far under half the smallest E4M3 step (2^-10), so its code is
 // 0 either way.
+// The remainder step turns a zero quotient into +0 whatever the sign of x
+// (-0 + +0 is +0), while IEEE division keeps -0 / s = -0, which encodes as the
+// E4M3 code 0x80: the sign of x is put back (a no-op for every nonzero x,
+// whose quotient already has it).
+__device__ __forceinline__ float with_sign_of(float q, float x) {
+  return __uint_as_float(__float_as_uint(q) | (__float_as_uint(x) & 0x80000000u));
+}
+
 __device__ __forceinline__ float div_by_scale(float x, float s, float y) {
   const float q0 = x * y;
   const float r = fmaf(-q0, s, x);
-  return fmaf(r, y, q0);
+  return with_sign_of(fmaf(r, y, q0), x);
 }
 
 // div_by_scale on two values at once (packed FP32 operations, the same
@@ -117,7 +125,8 @@ __device__ __forceinline__ float div_by_scale(float x, float s, float y) {
 __device__ __forceinline__ float2 div_by_scale2(float2 x, float2 ns, float2 y) {
   const float2 q0 = __fmul2_rn(x, y);
   const float2 r = __ffma2_rn(q0, ns, x);
-  return __ffma2_rn(r, y, q0);
+  const float2 q = __ffma2_rn(r, y, q0);
+  return make_float2(with_sign_of(q.x, x.x), with_sign_of(q.y, x.y));
 }
 
 }  // namespace dev

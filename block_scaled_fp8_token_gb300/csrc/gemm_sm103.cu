@@ -222,7 +222,22 @@ struct Cfg {
   // tiles are short in K, so the tile-end store was up to 40% of their time.)
   // Dense shapes measured no faster this way: they keep the stores below.
   static constexpr bool kTmaStore = GROUPED && !W8A16 && !SWIGLU;
-  static constexpr uint32_t kStgWarp = kTmaStore ? 8192 : 32 * kStgPitch;
+  static constexpr uint32_t kStgWarp = SWIGLU ? 0 : (kTmaStore ? 8192 : 32 * kStgPitch);
+  // Fused SiLU*up: at the end of a tile the epilogue warps form h =
+  // bf16(silu(g) * u) in float32 (the MUFU-heavy part, spread over 256
+  // threads), stage it in shared memory and go straight on to the next tile.
+  // The staging holds per row [64 h-or-gate pairs | 64 up pairs] (512 bytes
+  // a row, 16-byte chunks swizzled by row): the finished h pair, or for a pair
+  // the float32 path cannot round with certainty (an element next to a BF16
+  // rounding midpoint, or a gate value outside the fast path's range) the
+  // BF16 gate pair in its place, marked in a flag word per thread.
+  // Warp 3 (the SiLU warp) then takes the tile: it resolves the flagged pairs
+  // exactly (double where needed), forms each row's 1x128 scale and E4M3
+  // codes and stores them.
+  static constexpr int kSiluWarp = 3;
+  static constexpr uint32_t kHStgBytes = SWIGLU ? BM * 512 : 0;
+  // flag words [2][BM], then the largest |h| of each half row [2][BM] (BF16 bits)
+  static constexpr uint32_t kFixBytes = SWIGLU ? 4 * BM * 4 : 0;
   // TMEM (512 columns) holds 512/BN partial buffers, so the tensor cores run
   // up to that many K-blocks minus one ahead of the promotion.
   static constexpr uint32_t kTmemCols = 512;
@@ -239,12 +254,14 @@ struct Cfg {
   static constexpr bool kFacWarp = kSplitRegs && (GROUPED || SWIGLU);
   static constexpr int kFacSlots = 4;
   static constexpr uint32_t kFacBytes = 2 * BM * 4;
-  static constexpr uint32_t kOffFac = kOffStg + kEpiWarps * kStgWarp;
+  static constexpr uint32_t kOffFix = kOffStg + kEpiWarps * kStgWarp + kHStgBytes;
+  static constexpr uint32_t kOffFac = kOffFix + kFixBytes;
   static constexpr uint32_t kOffBar = kOffFac + (kFacWarp ? kFacSlots * kFacBytes : 0);
   static constexpr uint32_t kNumBars =
-      3 * STAGES + 2 * kNumBufs + 1 + 2 * kFacSlots + 2 * kRawStages + 2 * kConvBufs;
+      3 * STAGES + 2 * kNumBufs + 1 + 2 * kFacSlots + 2 * kRawStages + 2 * kConvBufs + 2;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr uint32_t kOffOff = kOffMisc + 16;  // misc: TMEM slot, abort flag, last-arriver flag
+  // misc: TMEM slot, abort flag, last-arriver flag, tile handed to the SiLU warp
+  static constexpr uint32_t kOffOff = kOffMisc + 16;
   static constexpr uint32_t kOffPre = kOffOff + (kMaxExperts + 1) * 4;
   static constexpr uint32_t kSmemUsed = GROUPED ? kOffPre + (kMaxExperts + 1) * 4 : kOffOff;
   static constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // 1024-byte alignment slack
@@ -362,11 +379,121 @@ BFP8_DEV void raise_abort(volatile int* abort_flag) {
   atomicExch(&g_gemm_err, static_cast<int>(BFP8_ERR_TIMEOUT));
 }
 
-BFP8_DEV float bf16_round(float a) { return __bfloat162float(__float2bfloat16_rn(a)); }
 
 BFP8_DEV uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+BFP8_DEV float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
+BFP8_DEV float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+BFP8_DEV uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+BFP8_DEV uint32_t min_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// h for a BF16 pair (gate pair gb, up pair ub) by the exact scalar path,
+// packed like pack_bf16x2. Out of line: only flagged pairs take it.
+static __device__ __noinline__ uint32_t silu_mul_pair_exact(uint32_t gb, uint32_t ub) {
+  const float h0 = silu_mul_bf16_round(__uint_as_float(gb << 16), __uint_as_float(ub << 16));
+  const float h1 = silu_mul_bf16_round(__uint_as_float(gb & 0xFFFF0000u),
+                                       __uint_as_float(ub & 0xFFFF0000u));
+  return (__float_as_uint(h0) >> 16) | (__float_as_uint(h1) & 0xFFFF0000u);
+}
+
+// The SiLU warp's work on one staged fused gate/up tile: per row, h over its
+// 128 columns, the row's 1x128 scale and its E4M3 codes. Rows go in blocks of
+// 32, one row per lane first: a row with flagged pairs gets their exact h
+// (written back to the staging) and its maximum again; every row gets its
+// scale and reciprocal, and one store writes the block's scales. Then 8
+// lanes take a row, each 16 consecutive columns (two 16-byte chunks of h
+// pairs), four rows per step, with the row's scale by shuffle and one 16-byte
+// store of codes per lane. The warp issues few memory instructions: they
+// share the pipe with the epilogue's tensor-memory loads.
+__device__ __forceinline__ void silu_quant_tile(const GemmParams& p, const Tile& tl, uint32_t stg,
+                                                const uint32_t* flags, int lane) {
+  const int rq = lane >> 3;         // row of the step this lane takes
+  const int j = lane & 7;           // its 16-column slice
+  const int col0 = 16 * j;
+  const bool vec = p.vec_store && col0 + 16 <= tl.n_valid;
+#pragma unroll 1
+  for (int rb = 0; rb < tl.m_valid; rb += 32) {
+    const uint32_t ra = static_cast<uint32_t>(rb + lane) & (BM - 1);
+    const uint32_t f0 = flags[ra], f1 = flags[BM + ra];
+    uint32_t am = max(flags[2 * BM + ra], flags[3 * BM + ra]);
+    if (__any_sync(0xffffffffu, (f0 | f1) != 0u)) {
+      if (f0 | f1) {
+        // this lane's row: exact h for its flagged pairs, then its maximum
+        const uint32_t row = stg + ra * 512u, sw = ra & 7u;
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t f = hf ? f1 : f0;
+          while (f) {
+            const uint32_t pr = 32u * hf + static_cast<uint32_t>(__ffs(f) - 1);
+            f &= f - 1u;
+            const uint32_t ag = row + (((pr >> 2) ^ sw) << 4) + (pr & 3u) * 4u;
+            const uint32_t au = row + (((16u + (pr >> 2)) ^ sw) << 4) + (pr & 3u) * 4u;
+            uint32_t gb, ub;
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(gb) : "r"(ag));
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(ub) : "r"(au));
+            const uint32_t hb = silu_mul_pair_exact(gb, ub);
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(ag), "r"(hb) : "memory");
+          }
+        }
+        uint32_t mx = 0u;
+        for (int c = 0; c < 16; ++c) {
+          const uint4 v = lds128(row + ((static_cast<uint32_t>(c) ^ sw) << 4));
+          mx = max_u16x2(mx, v.x & 0x7FFF7FFFu);
+          mx = max_u16x2(mx, v.y & 0x7FFF7FFFu);
+          mx = max_u16x2(mx, v.z & 0x7FFF7FFFu);
+          mx = max_u16x2(mx, v.w & 0x7FFF7FFFu);
+        }
+        am = max(mx & 0xFFFFu, mx >> 16);
+      }
+      __syncwarp();
+    }
+    const float sc_a = group_scale(__uint_as_float(am << 16));
+    const float rc_a = __frcp_rn(sc_a);
+    if (rb + lane < tl.m_valid)
+      p.s_h[(static_cast<int64_t>(tl.a_row0) + rb + lane) * p.sh_sm + (tl.n_out0 / 128) * p.sh_skb] = sc_a;
+    const int nrows = min(32, tl.m_valid - rb);
+#pragma unroll 1
+    for (int i = 0; i < nrows; i += 4) {
+      const int ri = i + rq;
+      const uint32_t r = static_cast<uint32_t>(rb + ri) & (BM - 1);
+      const uint32_t row = stg + r * 512u;
+      const uint4 h0 = lds128(row + ((static_cast<uint32_t>(2 * j) ^ (r & 7u)) << 4));
+      const uint4 h1 = lds128(row + ((static_cast<uint32_t>(2 * j + 1) ^ (r & 7u)) << 4));
+      const float sc = __shfl_sync(0xffffffffu, sc_a, ri & 31);
+      const float rc = __shfl_sync(0xffffffffu, rc_a, ri & 31);
+      const float2 y2 = make_float2(rc, rc), ns2 = make_float2(-sc, -sc);
+      const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+      uint32_t wq[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 q0 = div_by_scale2(make_float2(lo_bf16(hw[2 * q]), hi_bf16(hw[2 * q])), ns2, y2);
+        const float2 q1 =
+            div_by_scale2(make_float2(lo_bf16(hw[2 * q + 1]), hi_bf16(hw[2 * q + 1])), ns2, y2);
+        wq[q] = static_cast<uint32_t>(f32x2_to_e4m3x2(q0.x, q0.y)) |
+                (static_cast<uint32_t>(f32x2_to_e4m3x2(q1.x, q1.y)) << 16);
+      }
+      if (ri < nrows) {
+        uint8_t* dst = p.q_h + (static_cast<int64_t>(tl.a_row0) + rb + ri) * p.ldq + tl.n_out0 + col0;
+        if (vec) {
+          *reinterpret_cast<uint4*>(dst) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            if (col0 + e < tl.n_valid) dst[e] = static_cast<uint8_t>(wq[e >> 2] >> (8 * (e & 3)));
+        }
+      }
+    }
+  }
 }
 
 template <int BN, int STAGES, bool W8A16, bool GROUPED, bool SWIGLU>
@@ -403,9 +530,15 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
   auto cv_empty = [&](int c) {
     return bar0 + 8u * (kW16Bar0 + 2 * C::kRawStages + C::kConvBufs + c);
   };
+  // the fused SiLU*up hand-off: staging full (8 epilogue warps arrive) / empty (SiLU warp)
+  const uint32_t stg_full = bar0 + 8u * (kW16Bar0 + 2 * C::kRawStages + 2 * C::kConvBufs);
+  const uint32_t stg_empty = stg_full + 8u;
+  const uint32_t hstg = base + C::kOffStg;  // [BM][128] BF16 h, swizzled 16-byte chunks
+  uint32_t* pair_flags = reinterpret_cast<uint32_t*>(base_ptr + C::kOffFix);  // [2][BM]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::kOffMisc + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(base_ptr + C::kOffMisc + 8);
+  volatile int* stg_tile = reinterpret_cast<volatile int*>(base_ptr + C::kOffMisc + 12);
   int* s_off = reinterpret_cast<int*>(base_ptr + C::kOffOff);
   int* s_pre = reinterpret_cast<int*>(base_ptr + C::kOffPre);
 
@@ -431,7 +564,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
       mbar_init(cv_full(c), C::kConvWarps);
       mbar_init(cv_empty(c), 1);
     }
+    mbar_init(stg_full, C::kEpiWarps);
+    mbar_init(stg_empty, 1);
     *abort_flag = 0;
+    *stg_tile = -1;
     mbar_fence_init();
   }
   if (warp == 0 && lane == 0) {
@@ -652,6 +788,28 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
         }
       }
       if (!ok) raise_abort(abort_flag);
+    } else if (SWIGLU && warp == C::kSiluWarp) {
+      // ------------------------------------------------------------ SiLU*up + quant
+      // Takes each tile the epilogue hands over (tile index -1 ends the work),
+      // writes h's codes and scales, and frees the staging for the next tile.
+      pdl_wait();
+      uint32_t ph = 0;
+      bool ok = true;
+      for (;;) {
+        if (!__all_sync(0xffffffffu, mbar_wait_sleep(stg_full, ph, abort_flag))) {
+          ok = false;
+          break;
+        }
+        const int t = *stg_tile;
+        if (t < 0) break;
+        Tile tl;
+        decode_tile<C::kOutCols, GROUPED>(p, s_off, s_pre, t, tl);
+        silu_quant_tile(p, tl, hstg, pair_flags, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(stg_empty);
+        ph ^= 1u;
+      }
+      if (!ok) raise_abort(abort_flag);
     }
   } else if (warp < C::kEpiWarp0 + C::kEpiWarps) {
     if constexpr (C::kSplitRegs) warpgroup_reg_alloc<C::kEpiRegs>();
@@ -668,6 +826,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
     uint32_t bphase = 0;
     int fslot = 0;          // factor ring slot (W8A8)
     uint32_t fphase = 0;
+    uint32_t handed = 0;    // tiles handed to the SiLU warp
     bool ok = true;
     // Every epilogue warp walks every segment, even after a failed wait, so
     // that all of them reach the same named barriers (those cannot time out).
@@ -844,56 +1003,82 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
         if (ew == 0 && lane == 0) p.ws_counters[t] = 0;  // leave the workspace clean
       }
       if constexpr (SWIGLU) {
-        // Fused dense-FFN glue: h = bf16(silu(bf16(gate)) * bf16(up)), then the
-        // 1x128 quantization of h. A group is one row's 128 tile columns,
-        // split over this thread (64) and the thread of the other warpgroup
-        // with the same row; they swap maxima through shared memory. All
-        // epilogue warps reach both barriers whatever their `ok`.
-        float* xchg = reinterpret_cast<float*>(base_ptr + C::kOffStg);  // [2][BM] row maxima
-        const int col0 = h * 64;
-        float amax = 0.0f;
+        // Fused dense-FFN glue, this thread's share: its row's 64 h values,
+        // h = bf16(silu(bf16(g)) * bf16(u)), the gate and up accumulators
+        // rounded to BF16 exactly where the unfused GEMM would store them.
+        // Float32 fast path (act_math.cuh); a pair that the fast path cannot
+        // round with certainty is staged as its gate and up values and
+        // flagged for the SiLU warp, which takes the tile from the staging.
+        const bool w_ok = mbar_wait(stg_empty, (handed & 1u) ^ 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, w_ok)) ok = false;
+        if (ok) {
+          const float2 c_hi = make_float2(kNegLog2eHi, kNegLog2eHi);
+          const float2 c_lo = make_float2(kNegLog2eLoLn2, kNegLog2eLoLn2);
+          const float2 one = make_float2(1.0f, 1.0f);
+          // BF16 gate and up pairs first: the FP32 accumulator dies here
+          uint32_t gw[32], uw[32], hw[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int cc = col0 + 2 * j;
-          float h0 = silu_mul_bf16_round(bf16_round(acc[j].x), bf16_round(acc[32 + j].x));
-          float h1 = silu_mul_bf16_round(bf16_round(acc[j].y), bf16_round(acc[32 + j].y));
-          if (cc >= tl.n_valid) h0 = 0.0f;
-          if (cc + 1 >= tl.n_valid) h1 = 0.0f;
-          acc[j] = make_float2(h0, h1);
-          amax = fmaxf(amax, fmaxf(fabsf(h0), fabsf(h1)));
-        }
-        xchg[h * BM + row_in_tile] = amax;
-        named_bar_sync(1, 32 * C::kEpiWarps);
-        amax = fmaxf(amax, xchg[(h ^ 1) * BM + row_in_tile]);
-        named_bar_sync(1, 32 * C::kEpiWarps);  // both read before the next tile rewrites them
-        if (ok && row_ok) {
-          const float sc = group_scale(amax);
-          const float rc = __frcp_rn(sc);
-          uint8_t* dst = p.q_h + arow * p.ldq + tl.n_out0 + col0;
-          const bool full = p.vec_store && col0 + 64 <= tl.n_valid;
+          for (int jj = 0; jj < 32; ++jj) {
+            gw[jj] = pack_bf16x2(acc[jj].x, acc[jj].y);
+            uw[jj] = pack_bf16x2(acc[32 + jj].x, acc[32 + jj].y);
+          }
+          uint32_t fmask = 0u, gmax = 0u, gmin = 0xFFFFFFFFu;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {  // 16 codes at a time
-            uint32_t wq[4];
+          for (int jj = 0; jj < 32; ++jj) {
+            const uint32_t gb = gw[jj], ub = uw[jj];
+            const float2 g = make_float2(lo_bf16(gb), hi_bf16(gb));
+            const float2 u = make_float2(lo_bf16(ub), hi_bf16(ub));
+            const float2 ea = __fmul2_rn(g, c_hi);
+            const float2 e0 = make_float2(ex2_approx(ea.x), ex2_approx(ea.y));
+            const float2 ex = __ffma2_rn(e0, __fmul2_rn(g, c_lo), e0);
+            const float2 d = __fadd2_rn(ex, one);
+            const float2 sg = __fmul2_rn(g, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+            const float2 pr = __fmul2_rn(sg, u);
+            hw[jj] = pack_bf16x2(pr.x, pr.y);
+            // |g| range of the fast path over the pair (zero maps to the top
+            // of the second range, so it never counts as tiny)
+            const uint32_t a2 = gb & 0x7FFF7FFFu;
+            gmax = max_u16x2(gmax, a2);
+            gmin = min_u16x2(gmin, (a2 + 0x7FFF7FFFu) & 0x7FFF7FFFu);
+            if (near_bf16_midpoint(pr.x) || near_bf16_midpoint(pr.y)) fmask |= 1u << jj;
+          }
+          // some |g| >= 64, or 0 < |g| < 2^-100: every pair goes the exact way
+          if (max(gmax & 0xFFFFu, gmax >> 16) >= 0x4280u ||
+              min(gmin & 0xFFFFu, gmin >> 16) < 0x0D80u - 1u)
+            fmask = 0xFFFFFFFFu;
+          // columns past the tile's valid width hold 0 (their gate rows belong
+          // to the up member); then the largest |h| of this half row
+          if (tl.n_valid < C::kOutCols) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int j = 8 * i + 2 * k;
-              const uint16_t lo = f32x2_to_e4m3x2(div_by_scale(acc[j].x, sc, rc),
-                                                  div_by_scale(acc[j].y, sc, rc));
-              const uint16_t hi = f32x2_to_e4m3x2(div_by_scale(acc[j + 1].x, sc, rc),
-                                                  div_by_scale(acc[j + 1].y, sc, rc));
-              wq[k] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-            }
-            if (full) {
-              reinterpret_cast<uint4*>(dst)[i] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 16; ++e)
-                if (col0 + 16 * i + e < tl.n_valid)
-                  dst[16 * i + e] = static_cast<uint8_t>(wq[e >> 2] >> (8 * (e & 3)));
+            for (int jj = 0; jj < 32; ++jj) {
+              const int col = h * 64 + 2 * jj;
+              hw[jj] &= (col < tl.n_valid ? 0x0000FFFFu : 0u) | (col + 1 < tl.n_valid ? 0xFFFF0000u : 0u);
+              if (col >= tl.n_valid) fmask &= ~(1u << jj);
             }
           }
-          if (h == 0) p.s_h[arow * p.sh_sm + (tl.n_out0 / 128) * p.sh_skb] = sc;
+          uint32_t hmax = 0u;
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) hmax = max_u16x2(hmax, hw[jj] & 0x7FFF7FFFu);
+          // pair jj: h (or the gate pair when flagged) in the first half of
+          // the row, the up pair in the second
+          const uint32_t rowa = hstg + static_cast<uint32_t>(row_in_tile) * 512u;
+          const uint32_t sw = static_cast<uint32_t>(row_in_tile & 7);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t v[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v[k] = ((fmask >> (4 * c + k)) & 1u) ? gw[4 * c + k] : hw[4 * c + k];
+            sts128(rowa + ((static_cast<uint32_t>(8 * h + c) ^ sw) << 4), make_uint4(v[0], v[1], v[2], v[3]));
+            sts128(rowa + ((static_cast<uint32_t>(16 + 8 * h + c) ^ sw) << 4),
+                   make_uint4(uw[4 * c], uw[4 * c + 1], uw[4 * c + 2], uw[4 * c + 3]));
+          }
+          pair_flags[h * BM + row_in_tile] = fmask;
+          pair_flags[(2 + h) * BM + row_in_tile] = max(hmax & 0xFFFFu, hmax >> 16);
+          if (ew == 0 && lane == 0) *stg_tile = t;
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(stg_full);
+        ++handed;
         continue;
       }
       if (!ok) continue;
@@ -973,6 +1158,13 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
       // complete only with the tensor stores
       if (lane == 0) bulk_wait_all();
       __syncwarp();
+    }
+    if constexpr (SWIGLU) {
+      // no more tiles: once the SiLU warp has taken the last one, tell it to stop
+      mbar_wait(stg_empty, (handed & 1u) ^ 1u, abort_flag);
+      if (ew == 0 && lane == 0) *stg_tile = -1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(stg_full);
     }
     if (!ok) raise_abort(abort_flag);
   } else {
@@ -1388,7 +1580,7 @@ int launch_grouped_w8a8_swiglu(const void* q_a, const float* s_a, int64_t sa_sm,
   rc = sk_setup(p, tile_bound, kBN8, workspace, ws_bytes, stream);
   if (rc != BFP8_OK) return rc;
   const CUtensorMap ty{};
-  return launch<kBN8, kStages8, false, true, true>(ta, tb, ty, p, 0x7FFFFFFF, stream);
+  return launch<kBN8, kStagesSwiglu, false, true, true>(ta, tb, ty, p, 0x7FFFFFFF, stream);
 }
 
 int gemm_read_clear_error() {
