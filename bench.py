@@ -81,6 +81,48 @@ def _peaks():
     return {"hbm_gbs": 6800.0, "bf16": 1900.0, "source": "fallback"}
 
 
+def measure_fp8_peak(torch, dev, n: int = 8192, reps: int = 10) -> dict:
+    """Dense FP8 (E4M3) tensor throughput of this GPU through the vendor
+    library: torch._scaled_mm on n x n x n with per-tensor scales, best of
+    `reps` CUDA-event timings after warm-up. The W8A8 rooflines use
+    max(this, 2 x the measured BF16 burst)."""
+    try:
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()   # column-major operand
+        one = torch.ones((), device=dev, dtype=torch.float32)
+        for _ in range(3):
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        del a, b
+        torch.cuda.empty_cache()
+        return {"tflops": round(2 * n ** 3 / (best * 1e-3) / 1e12, 1),
+                "how": f"torch._scaled_mm E4M3 {n}^3, per-tensor scales, BF16 out, best of {reps}"}
+    except (RuntimeError, AttributeError, TypeError) as exc:
+        return {"tflops": None, "how": f"unavailable: {exc}"[:200]}
+
+
+def fp8_denominator(peaks, fp8_meas) -> tuple[float, str]:
+    """The W8A8 roofline denominator: max(measured FP8, 2 x measured BF16 burst)."""
+    derived = 2.0 * peaks["bf16"]
+    meas = fp8_meas.get("tflops") if fp8_meas else None
+    if meas is not None and meas >= derived:
+        return meas, f"measured FP8 dense ({fp8_meas['how']})"
+    note = f"{peaks['source']} bf16 burst {peaks['bf16']} x 2 (FP8:BF16 nominal 4.5:2.25)"
+    if meas is not None:
+        note += f"; above the measured FP8 {meas} ({fp8_meas['how']})"
+    return derived, note
+
+
 def _dist():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -157,6 +199,95 @@ def parse_clock_samples(lines, t_begin=None, t_end=None) -> dict:
             "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# NVML clocks-event-reason bits (nvml.h)
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+class NvmlSampler:
+    """SM clock, power and throttle-reason samples read through NVML (the
+    driver's libnvidia-ml, by ctypes) every ~1 ms on a background thread, kept
+    only while the timed region runs (begin() / end()), so that a timed region
+    of a few milliseconds still has samples. Reads settings only."""
+
+    def __init__(self, device_index: int):
+        import ctypes
+        import threading
+
+        self.ok = False
+        self.samples = []
+        self.t_begin = self.t_end = None
+        self._stop = threading.Event()
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        idx = int(vis) if vis.strip().isdigit() else device_index
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(h)) != 0:
+                return
+            self.lib, self.h, self.ct = lib, h, ctypes
+            reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+            self.reasons_fn = reasons or lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            self.max_mhz = (float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0
+                            else None)
+            self.ok = self._read() is not None
+        except (OSError, AttributeError):
+            self.ok = False
+        if self.ok:
+            self.thread = threading.Thread(target=self._loop, daemon=True)
+
+    def _read(self):
+        ct = self.ct
+        mhz, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz)) != 0:   # NVML_CLOCK_SM
+            return None
+        p = float(mw.value) / 1000.0 if self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw)) == 0 else None
+        r = int(rs.value) if self.reasons_fn(self.h, ct.byref(rs)) == 0 else 0
+        return time.time(), float(mhz.value), p, r
+
+    def _loop(self):
+        while not self._stop.is_set():
+            s = self._read()
+            if s is not None:
+                self.samples.append(s)
+            time.sleep(0.001)
+
+    def start(self):
+        self.thread.start()
+        time.sleep(0.05)
+
+    def begin(self):
+        self.t_begin = time.time()
+
+    def end(self):
+        self.t_end = time.time()
+
+    def window(self, t_begin, t_end) -> dict:
+        """Summary of the samples taken in [t_begin, t_end]."""
+        rows = [x for x in self.samples if t_begin <= x[0] <= t_end]
+        sm = [x[1] for x in rows]
+        pw = [x[2] for x in rows if x[2] is not None]
+        reasons = sorted({name for x in rows for bit, name in NVML_REASONS.items() if x[3] & bit})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "power_w": round(statistics.median(pw), 1) if pw else None,
+                "reasons": reasons, "samples": len(sm), "source": "nvml, ~1 ms polling"}
+
+    def stop(self) -> dict:
+        time.sleep(0.01)
+        self._stop.set()
+        self.thread.join(timeout=2)
+        return self.window(self.t_begin, self.t_end)
+
+
+def clock_sampler(device_index: int):
+    """NVML sampler when the driver library answers, else nvidia-smi."""
+    s = NvmlSampler(device_index)
+    return s if s.ok else ClockSampler(device_index)
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples, kept only while the timed
     region runs (begin() / end() mark it). The raw samples go to
@@ -229,6 +360,8 @@ def run_ours(args, rank, world, local):
     wdn, sdn = quantize(d["w_down"])
     del d
     torch.cuda.synchronize()
+    fp8_meas = measure_fp8_peak(torch, dev)
+    fp8_peak, fp8_source = fp8_denominator(peaks, fp8_meas)
 
     qa = torch.empty(M_TOK, HID, dtype=torch.uint8, device=dev)
     sa = torch.empty(M_TOK, HID // 128, dtype=torch.float32, device=dev)
@@ -264,7 +397,7 @@ def run_ours(args, rank, world, local):
     if bfp8.bfp8_device_status() != 0:
         raise RuntimeError("device status not OK after warm-up")
 
-    clocks = ClockSampler(local)
+    clocks = clock_sampler(local)
     clocks.start()
     barrier(dist_mod)
     torch.cuda.synchronize()
@@ -336,7 +469,7 @@ def run_ours(args, rank, world, local):
         raise RuntimeError("pipelined end-to-end output differs from the device result")
 
     decode = run_decode(bfp8, torch, dev, wgu, sgu, wdn, sdn, peaks)
-    workloads = None if args.no_workloads else run_workloads(bfp8, torch, dev, peaks)
+    workloads = None if args.no_workloads else run_workloads(bfp8, torch, dev, peaks, fp8_peak)
     status = bfp8.bfp8_device_status()
     if status != 0:
         raise RuntimeError(f"device status {bfp8.bfp8_status_string(status)}")
@@ -345,7 +478,6 @@ def run_ours(args, rank, world, local):
         return None
     tflops = FLOPS_STEP * world / (ms_max * 1e-3) / 1e12
     achieved = FLOPS_GATE_UP / (gu_ms * 1e-3) / 1e12
-    fp8_peak = 2.0 * peaks["bf16"]
     out = {
         "metric": METRIC,
         "value": round(tflops, 2),
@@ -375,7 +507,8 @@ def run_ours(args, rank, world, local):
             "frac": round(achieved / fp8_peak, 4),
             "traffic": ncu_traffic("gemm_gate_up_silu_quant")[0],
             "traffic_note": ncu_traffic("gemm_gate_up_silu_quant")[1],
-            "peak_source": f"{peaks['source']} bf16 burst {peaks['bf16']} x 2 (FP8:BF16 nominal ratio 4.5:2.25)",
+            "peak_source": fp8_source,
+            "fp8_measured": fp8_meas,
             "launch_ms": round(gu_ms, 4),
         },
         "e2e": {
@@ -546,11 +679,24 @@ def _moe_routing(torch, gen, dev, c):
     return offsets, row_token, row_of.reshape(T, k), weights
 
 
-def setup_case(case, bfp8, torch, dev, gen, decode_m=16):
+def setup_case(case, bfp8, torch, dev, gen, decode_m=16, l2_ring=0):
     """Device buffers for one launch of the hot path on a synthetic workload.
     Returns (launch, work, unit, bound): work is algorithmic FLOPs (TFLOP/s
-    cases) or bytes (GB/s cases) per launch."""
+    cases) or bytes (GB/s cases) per launch. With l2_ring > 0, the dense GEMM
+    cases whose weights are smaller than l2_ring bytes rotate over enough
+    weight copies to cover it, one copy per launch, so that no launch finds
+    its weights in L2."""
     from block_scaled_fp8_token_gb300 import synth
+
+    def ring(w, sw):
+        n = max(1, -(-l2_ring // w.numel())) if l2_ring else 1
+        copies = [(w, sw)] + [(w.clone(), sw.clone()) for _ in range(n - 1)]
+        state = {"i": 0}
+
+        def nxt():
+            state["i"] = (state["i"] + 1) % len(copies)
+            return copies[state["i"]]
+        return nxt
 
     def qweight(N, K, G=None):
         if G is None:
@@ -593,7 +739,8 @@ def setup_case(case, bfp8, torch, dev, gen, decode_m=16):
                 2 * M_TOK * N * K, "TFLOP/s", "tensor-bf16"
         ws = torch.empty(bfp8.bfp8_linear_w8a8_workspace(M_TOK, N, K, members),
                          dtype=torch.uint8, device=dev)
-        return (lambda: bfp8.bfp8_linear_w8a8(qa, sa, w, sw, y, member_rows=members,
+        nxt = ring(w, sw)
+        return (lambda: bfp8.bfp8_linear_w8a8(qa, sa, *nxt(), y, member_rows=members,
                                               workspace=ws)), 2 * M_TOK * N * K, "TFLOP/s", "tensor"
     if case == "gate_up_silu_quant":
         w, sw = qweight(2 * INTER, HID)
@@ -624,8 +771,9 @@ def setup_case(case, bfp8, torch, dev, gen, decode_m=16):
         y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         ws = torch.empty(bfp8.bfp8_linear_w8a8_workspace(M, N, K, members), dtype=torch.uint8,
                          device=dev)
-        return (lambda: bfp8.bfp8_linear_w8a8(qa, sa, w, sw, y, member_rows=members, workspace=ws)), \
-            2 * M * N * K, "TFLOP/s", "tensor"
+        nxt = ring(w, sw)
+        return (lambda: bfp8.bfp8_linear_w8a8(qa, sa, *nxt(), y, member_rows=members,
+                                              workspace=ws)), 2 * M * N * K, "TFLOP/s", "tensor"
     if case in ("moe_gather_quant", "moe_combine", "moe_layer"):
         c = synth.MOE_PREFILL
         T, E, k, H, I = c["tokens"], c["experts"], c["top_k"], c["hidden"], c["inter"]
@@ -729,31 +877,44 @@ WORKLOAD_CASES = ("gate_up", "qkv", "o_proj", "moe_gate_up_silu_quant", "moe_gat
                   "moe_combine")
 
 
-def run_workloads(bfp8, torch, dev, peaks, steps: int = 50) -> dict:
+def run_workloads(bfp8, torch, dev, peaks, fp8_peak, steps: int = 50) -> dict:
     """Per-launch throughput of the hot path on the other workloads (attention
     projections at M=4096, MoE experts over 65,536 routed rows, the W8A16 arm,
-    the two quantizers), each against its own roofline."""
+    the two quantizers), each against its own roofline, with the SM clock
+    seen during its timed launches."""
     from block_scaled_fp8_token_gb300 import synth
 
-    out = {"timing": f"mean of {steps} back-to-back launches after 3 warm-up "
-                     "launches (GEMM inputs exceed L2 except the quantizers')", "cases": {}}
+    l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    out = {"timing": f"mean of {steps} back-to-back launches after 3 warm-up launches; the "
+                     f"dense GEMMs rotate over weight copies covering >= 2x the {l2 >> 20} MB L2, "
+                     "the MoE expert weights (201-403 MB) and the W8A16 weights exceed it; the "
+                     "quantizers' inputs do not", "cases": {}}
+    clocks = NvmlSampler(dev.index or 0)
+    if clocks.ok:
+        clocks.start()
     for case in WORKLOAD_CASES:
-        launch, work, unit, bound = setup_case(case, bfp8, torch, dev, synth.generator(0))
+        launch, work, unit, bound = setup_case(case, bfp8, torch, dev, synth.generator(0),
+                                               l2_ring=2 * l2)
         for _ in range(3):
             launch()
         torch.cuda.synchronize()
+        tb = time.time()
         ms = time_back_to_back(torch, launch, steps)
+        te = time.time()
         if unit == "TFLOP/s":
             rate = work / (ms * 1e-3) / 1e12
-            peak = 2.0 * peaks["bf16"] if bound == "tensor" else peaks["bf16"]
+            peak = fp8_peak if bound == "tensor" else peaks["bf16"]
         else:
             rate = work / (ms * 1e-3) / 1e9
             peak = peaks["hbm_gbs"]
         out["cases"][case] = {"ms": round(ms, 5), "rate": round(rate, 1), "unit": unit,
                               "bound": bound, "peak": round(peak, 1),
-                              "frac": round(rate / peak, 4), "work_per_launch": work}
+                              "frac": round(rate / peak, 4), "work_per_launch": work,
+                              "clocks": clocks.window(tb, te) if clocks.ok else None}
         del launch
         torch.cuda.empty_cache()
+    if clocks.ok:
+        clocks.stop()
     if bfp8.bfp8_device_status() != 0:
         raise RuntimeError("device status not OK after the workload sweep")
     return out

@@ -91,3 +91,23 @@ def test_reference_arm_json_line(capsys):
     assert out["cpu_baseline"]["kind"] == "oracle" and out["cpu_baseline"]["cores"] >= 1
     assert out["config"]["sample_rows"] == 2
     assert out["e2e"]["h2d_bytes_per_step"] == 0 and out["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_nvml_window_summary_and_fp8_denominator():
+    """The NVML sampler's summary keeps only samples inside the timed window
+    and decodes the throttle-reason bits; the W8A8 roofline denominator is
+    max(measured FP8, 2 x measured BF16) and says which one it is."""
+    s = bench.NvmlSampler.__new__(bench.NvmlSampler)
+    s.max_mhz = 2070.0
+    s.samples = [(0.5, 900.0, 100.0, 0x0), (1.0, 1950.0, 1300.0, 0x4), (1.5, 1980.0, 1350.0, 0x4),
+                 (2.0, 2000.0, 1390.0, 0x0), (3.0, 600.0, 90.0, 0x1)]
+    w = s.window(0.9, 2.1)
+    assert w["samples"] == 3 and w["sm_mhz"] == 1980.0 and w["reasons"] == ["sw_power_cap"]
+    assert w["power_w"] == 1350.0 and w["sm_max_mhz"] == 2070.0
+    peaks = {"bf16": 1871.8, "source": "measured", "hbm_gbs": 6751.7}
+    d, note = bench.fp8_denominator(peaks, {"tflops": 4100.0, "how": "x"})
+    assert d == 4100.0 and note.startswith("measured FP8")
+    d, note = bench.fp8_denominator(peaks, {"tflops": 3000.0, "how": "x"})
+    assert d == 2 * 1871.8 and "above the measured FP8 3000.0" in note
+    d, _ = bench.fp8_denominator(peaks, {"tflops": None, "how": "unavailable"})
+    assert d == 2 * 1871.8

@@ -115,7 +115,8 @@ def _silu_hard_pairs(limit: int, rel: float = 2.0 ** -19):
     ulps of error could round to the wrong neighbour. Found by brute force over
     every finite BF16 g in [-64, 64) and every u in [1, 2)."""
     gb = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
-    g = F.bf16_bits_to_f32(gb).astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        g = F.bf16_bits_to_f32(gb).astype(np.float64)
     keep = np.isfinite(g) & (np.abs(g) < 64) & (g != 0)
     gb, g = gb[keep], g[keep]
     ub = np.arange(0x3F80, 0x4000, dtype=np.uint16)           # every u in [1, 2)
