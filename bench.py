@@ -279,6 +279,8 @@ class NvmlSampler:
         time.sleep(0.01)
         self._stop.set()
         self.thread.join(timeout=2)
+        if self.t_begin is None or self.t_end is None:
+            return {}
         return self.window(self.t_begin, self.t_end)
 
 

@@ -111,3 +111,14 @@ def test_nvml_window_summary_and_fp8_denominator():
     assert d == 2 * 1871.8 and "above the measured FP8 3000.0" in note
     d, _ = bench.fp8_denominator(peaks, {"tflops": None, "how": "unavailable"})
     assert d == 2 * 1871.8
+
+
+def test_nvml_stop_without_a_timed_window():
+    import threading
+
+    s = bench.NvmlSampler.__new__(bench.NvmlSampler)
+    s.samples, s.t_begin, s.t_end, s.max_mhz = [], None, None, None
+    s._stop = threading.Event()
+    s.thread = threading.Thread(target=lambda: None)
+    s.thread.start()
+    assert s.stop() == {}
