@@ -80,8 +80,104 @@ __device__ __forceinline__ float f64_to_bf16_value(double x) {
   return sign ? -f : f;
 }
 
-// The fallback: the definition evaluated in double, rounded once to BF16.
+// ---- double-float arithmetic: a value hi + lo held as two FP32 numbers, used
+// by the fallback below. The elementary steps are the error-free transforms
+// (Knuth's TwoSum, Dekker's Fast2Sum, the FMA product error); every operation
+// uses the round-to-nearest intrinsics so that none is fused or reordered.
+struct ff {
+  float hi, lo;
+};
+__device__ __forceinline__ ff two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, e};
+}
+__device__ __forceinline__ ff fast_two_sum(float a, float b) {  // |a| >= |b| or a == 0
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ ff two_prod(float a, float b) {
+  const float p = __fmul_rn(a, b);
+  return {p, __fmaf_rn(a, b, -p)};
+}
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+  const ff s = two_sum(a.hi, b.hi);
+  return fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+__device__ __forceinline__ ff ff_mul(ff a, ff b) {
+  const ff p = two_prod(a.hi, b.hi);
+  return fast_two_sum(p.hi, __fmaf_rn(a.hi, b.lo, __fmaf_rn(a.lo, b.hi, p.lo)));
+}
+
+// e^x as hi + lo with relative error below 2^-46, for |x| < 64. x = k ln2 + r
+// with k the integer nearest x / ln2 and |r| <= 0.35: ln2 is split in three
+// parts, the first of 16 significant bits so that k times it is exact, and
+// e^r is its Taylor series to degree 11 (the first dropped term is below
+// 2^-47), degrees 7 to 11 in FP32 (their rounding reaches the sum below
+// 2^-47) and the rest in double-float by Horner's rule. Then e^x = 2^k e^r.
+__device__ __forceinline__ ff ff_exp(float x) {
+  constexpr float kLn2Hi = 0x1.62e4p-1f, kLn2Lo = 0x1.7f7d1cp-20f, kLn2Lo2 = 0x1.ef357ap-45f;
+  const float kf = rintf(x * 1.44269504f);
+  const float t = __fsub_rn(x, __fmul_rn(kf, kLn2Hi));   // exact
+  const ff kl = two_prod(kf, kLn2Lo);
+  const ff r0 = two_sum(t, -kl.hi);
+  const ff r = fast_two_sum(r0.hi, __fsub_rn(r0.lo, __fmaf_rn(kf, kLn2Lo2, kl.lo)));
+  // 1/n! as hi + lo, n = 0 .. 11
+  constexpr float c_hi[12] = {1.0f, 1.0f, 0.5f, 0x1.555556p-3f, 0x1.555556p-5f, 0x1.111112p-7f,
+                              0x1.6c16c2p-10f, 0x1.a01a02p-13f, 0x1.a01a02p-16f, 0x1.71de3ap-19f,
+                              0x1.27e4fcp-22f, 0x1.ae6456p-26f};
+  constexpr float c_lo[7] = {0.0f, 0.0f, 0.0f, -0x1.555556p-28f, -0x1.555556p-30f,
+                             -0x1.dddddep-32f, -0x1.27d27ep-35f};
+  float tail = c_hi[11];
+#pragma unroll
+  for (int n = 10; n >= 7; --n) tail = __fmaf_rn(tail, r.hi, c_hi[n]);
+  ff acc{tail, 0.0f};
+#pragma unroll
+  for (int n = 6; n >= 0; --n) acc = ff_add(ff{c_hi[n], c_lo[n]}, ff_mul(acc, r));
+  const float scale = __int_as_float((static_cast<int>(kf) + 127) << 23);   // 2^k, exact
+  return {__fmul_rn(acc.hi, scale), __fmul_rn(acc.lo, scale)};
+}
+
+// BF16 rounding of hi + lo (nearest, ties to even) for a finite hi + lo
+// above 2^-90 in magnitude: their FP32 sum s rounds like the exact value
+// unless s is itself a BF16 midpoint; then the sign of the remainder decides,
+// by moving s one FP32 unit toward it.
+__device__ __forceinline__ float ff_to_bf16_value(ff v) {
+  const ff s = fast_two_sum(v.hi, v.lo);
+  uint32_t b = __float_as_uint(s.hi);
+  if ((b & 0xFFFFu) == 0x8000u && s.lo != 0.0f) b += ((s.lo > 0.0f) == (s.hi > 0.0f)) ? 1u : 0xFFFFFFFFu;
+  return __bfloat162float(__float2bfloat16_rn(__uint_as_float(b)));
+}
+
+// The fallback for the elements the float32 path cannot round with
+// certainty: h = bf16(g / (1 + exp(-g)) * u), the value of that double-
+// precision expression rounded once.
+//  - For BF16 g with -64 < g < 34 and |g| >= 2^-45, in double-float (about
+//    2^-44 relative): e = exp(-g), d = 1 + e, q = g / d (FP32 quotient plus
+//    the correction of its remainder), q u. There the exact value lies
+//    either inside the open interval between two BF16 midpoints with room
+//    far above double rounding, or next to a midpoint by a margin that both
+//    evaluations resolve alike (a product g u on a midpoint moves off it by
+//    at least |g|/2 or e^-34 relative, both far above 2^-52), so the two
+//    roundings agree except within about 2^-44 of a midpoint.
+//  - Elsewhere (|g| below 2^-45, where double arithmetic turns 1 + exp(-g)
+//    into exactly 2; g >= 34, where it comes within a unit of exactly 1;
+//    g <= -64; and results below 2^-90) it is evaluated in double precision,
+//    the same expression in the same order.
 static __device__ __noinline__ float silu_mul_bf16_slow(float g, float u) {
+  const uint32_t ag = __float_as_uint(g) & 0x7FFFFFFFu;
+  if (ag >= 0x29000000u && g < 34.0f && g > -64.0f) {
+    const ff e = ff_exp(-g);
+    const ff d = ff_add(ff{1.0f, 0.0f}, e);
+    const float q1 = __fdiv_rn(g, d.hi);
+    const float rem = __fsub_rn(__fmaf_rn(-q1, d.hi, g), __fmul_rn(q1, d.lo));
+    const ff q = fast_two_sum(q1, __fdiv_rn(rem, d.hi));
+    const ff p = two_prod(q.hi, u);
+    const ff v{p.hi, __fmaf_rn(q.lo, u, p.lo)};
+    const float av = fabsf(v.hi);
+    if (av >= 0x1p-90f && av <= 0x1p127f) return ff_to_bf16_value(v);
+  }
   const double gd = g;
   return f64_to_bf16_value(gd / (1.0 + exp(-gd)) * static_cast<double>(u));
 }
