@@ -231,10 +231,11 @@ struct Cfg {
   // the float32 path cannot round with certainty (an element next to a BF16
   // rounding midpoint, or a gate value outside the fast path's range) the
   // BF16 gate pair in its place, marked in a flag word per thread.
-  // Warp 3 (the SiLU warp) then takes the tile: it resolves the flagged pairs
-  // exactly (double where needed), forms each row's 1x128 scale and E4M3
-  // codes and stores them.
-  static constexpr int kSiluWarp = 3;
+  // Warps 2 and 3 (the SiLU warps) then take the tile, alternate blocks of 32
+  // rows each: they resolve the flagged pairs exactly, form each row's 1x128
+  // scale and E4M3 codes and store them. (These instances have no factor
+  // warp: their promotion factors come from the in-loop fetch.)
+  static constexpr int kSiluWarp0 = 2, kSiluWarps = 2;
   static constexpr uint32_t kHStgBytes = SWIGLU ? BM * 512 : 0;
   // flag words [2][BM], then the largest |h| of each half row [2][BM] (BF16 bits)
   static constexpr uint32_t kFixBytes = SWIGLU ? 4 * BM * 4 : 0;
@@ -251,7 +252,7 @@ struct Cfg {
   // and multiplying on its critical path. (Measured: 3-5% faster MoE, 1%
   // faster fused dense gate/up, 1-2% slower plain dense shapes, which keep
   // the in-loop fetch.)
-  static constexpr bool kFacWarp = kSplitRegs && (GROUPED || SWIGLU);
+  static constexpr bool kFacWarp = kSplitRegs && GROUPED && !SWIGLU;
   static constexpr int kFacSlots = 4;
   static constexpr uint32_t kFacBytes = 2 * BM * 4;
   static constexpr uint32_t kOffFix = kOffStg + kEpiWarps * kStgWarp + kHStgBytes;
@@ -408,7 +409,8 @@ static __device__ __noinline__ uint32_t silu_mul_pair_exact(uint32_t gb, uint32_
 }
 
 // The SiLU warp's work on one staged fused gate/up tile: per row, h over its
-// 128 columns, the row's 1x128 scale and its E4M3 codes. Rows go in blocks of
+// 128 columns, the row's 1x128 scale and its E4M3 codes. Warp sw of nsw takes
+// every nsw-th block of 32 rows, starting at block sw. Rows go in blocks of
 // 32, one row per lane first: a row with flagged pairs gets their exact h
 // (written back to the staging) and its maximum again; every row gets its
 // scale and reciprocal, and one store writes the block's scales. Then 8
@@ -417,13 +419,13 @@ static __device__ __noinline__ uint32_t silu_mul_pair_exact(uint32_t gb, uint32_
 // store of codes per lane. The warp issues few memory instructions: they
 // share the pipe with the epilogue's tensor-memory loads.
 __device__ __forceinline__ void silu_quant_tile(const GemmParams& p, const Tile& tl, uint32_t stg,
-                                                const uint32_t* flags, int lane) {
+                                                const uint32_t* flags, int lane, int sw, int nsw) {
   const int rq = lane >> 3;         // row of the step this lane takes
   const int j = lane & 7;           // its 16-column slice
   const int col0 = 16 * j;
   const bool vec = p.vec_store && col0 + 16 <= tl.n_valid;
 #pragma unroll 1
-  for (int rb = 0; rb < tl.m_valid; rb += 32) {
+  for (int rb = 32 * sw; rb < tl.m_valid; rb += 32 * nsw) {
     const uint32_t ra = static_cast<uint32_t>(rb + lane) & (BM - 1);
     const uint32_t f0 = flags[ra], f1 = flags[BM + ra];
     uint32_t am = max(flags[2 * BM + ra], flags[3 * BM + ra]);
@@ -565,7 +567,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
       mbar_init(cv_empty(c), 1);
     }
     mbar_init(stg_full, C::kEpiWarps);
-    mbar_init(stg_empty, 1);
+    mbar_init(stg_empty, C::kSiluWarps);
     *abort_flag = 0;
     *stg_tile = -1;
     mbar_fence_init();
@@ -788,7 +790,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
         }
       }
       if (!ok) raise_abort(abort_flag);
-    } else if (SWIGLU && warp == C::kSiluWarp) {
+    } else if (SWIGLU && warp >= C::kSiluWarp0 && warp < C::kSiluWarp0 + C::kSiluWarps) {
       // ------------------------------------------------------------ SiLU*up + quant
       // Takes each tile the epilogue hands over (tile index -1 ends the work),
       // writes h's codes and scales, and frees the staging for the next tile.
@@ -804,7 +806,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
         if (t < 0) break;
         Tile tl;
         decode_tile<C::kOutCols, GROUPED>(p, s_off, s_pre, t, tl);
-        silu_quant_tile(p, tl, hstg, pair_flags, lane);
+        silu_quant_tile(p, tl, hstg, pair_flags, lane, warp - C::kSiluWarp0, C::kSiluWarps);
         __syncwarp();
         if (lane == 0) mbar_arrive(stg_empty);
         ph ^= 1u;
