@@ -699,15 +699,11 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
       int t, kb0, kb1;
       while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!__all_sync(0xffffffffu, mbar_wait_sleep(tempty_bar(buf), bphase ^ 1u, abort_flag))) {
-            ok = false;
-            break;
-          }
-          if (!__all_sync(0xffffffffu, mbar_wait_sleep(full_bar(stage), phase, abort_flag))) {
-            ok = false;
-            break;
-          }
-          if (W8A16 && !__all_sync(0xffffffffu, mbar_wait_sleep(cv_full(cs), cphase, abort_flag))) {
+          // one vote for all of this K-block's waits
+          const bool w_ok = mbar_wait_sleep(tempty_bar(buf), bphase ^ 1u, abort_flag) &&
+                            mbar_wait_sleep(full_bar(stage), phase, abort_flag) &&
+                            (!W8A16 || mbar_wait_sleep(cv_full(cs), cphase, abort_flag));
+          if (!__all_sync(0xffffffffu, w_ok)) {
             ok = false;
             break;
           }
@@ -852,8 +848,9 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
       // a warp that stalled on a load there would hold up the TMEM buffer for
       // every other warp. s_w is fetched 32 K-blocks at a time, one K-block
       // per lane, as raw bits (a window ahead), and each K-block takes its
-      // value with a shuffle; s_a is loaded at the top of its K-block and
-      // multiplied in after the wait.
+      // value with a shuffle; s_a is loaded one K-block ahead (loaded at the
+      // top of its own K-block, its latency held up the promotion of every
+      // K-block: the fused gate/up launch took 11% longer).
       auto sw_raw = [&](int64_t idx, int k) -> uint32_t {
         uint32_t r = 0u;
         if (k < kb1) {
@@ -875,7 +872,12 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
       // the up half's factor exists only with the fused SiLU*up epilogue
       // (without the factor warp: W8A16, whose factor is s_w alone)
       uint32_t sw_cur = 0u, su_cur = 0u, sw_nxt = 0u, su_nxt = 0u;
+      auto sa_load = [&](int k) -> float {
+        return (W8A16 || !row_ok || k >= kb1) ? (W8A16 ? 1.0f : 0.0f) : __ldg(sa_row + k * p.sa_skb);
+      };
+      float sa_nxt = 0.0f;   // s_a of the next K-block
       if constexpr (!C::kFacWarp) {
+        sa_nxt = sa_load(kb0);
         sw_cur = sw_raw(sw_idx, kb0 + lane);
         su_cur = SWIGLU ? sw_raw(sw_idx_up, kb0 + lane) : 0u;
         sw_nxt = sw_raw(sw_idx, kb0 + 32 + lane);
@@ -900,7 +902,8 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
           }
           const uint32_t sw_bits = __shfl_sync(0xffffffffu, sw_cur, wl);
           const uint32_t su_bits = SWIGLU ? __shfl_sync(0xffffffffu, su_cur, wl) : 0u;
-          const float sa = (W8A16 || !row_ok) ? (W8A16 ? 1.0f : 0.0f) : __ldg(sa_row + kb * p.sa_skb);
+          const float sa = sa_nxt;
+          sa_nxt = sa_load(kb + 1);
           const bool w_ok = mbar_wait(tfull_bar(buf), bphase, abort_flag);
           if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
           f = W8A16 ? sw_value(sw_bits) : sa * sw_value(sw_bits);

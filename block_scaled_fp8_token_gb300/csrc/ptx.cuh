@@ -97,10 +97,14 @@ BFP8_DEV bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
   return ok != 0;
 }
 // mbar_wait with hardware suspension between tests; same limits and result.
+// The clock is read only once the first test has failed: on a phase that is
+// already complete the wait costs one test (reading the global timer first
+// took about four times as long).
 BFP8_DEV bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
   constexpr uint32_t kHintNs = 2000;
+  if (mbar_try_wait_hint(bar, parity, kHintNs)) return true;
   const uint64_t t0 = globaltimer();
-  for (uint32_t i = 0;; ++i) {
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait_hint(bar, parity, kHintNs)) return true;
     if ((i & 7u) == 7u) {
       if (*abort_flag) return false;
