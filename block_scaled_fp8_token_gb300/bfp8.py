@@ -104,6 +104,7 @@ _SIGS = {
     "bfp8_moe_combine": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _i32, _vp, _i64,
                                         _vp]),
     "bfp8_device_status": (ctypes.c_int, [_vp]),
+    "bfp8_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -606,3 +607,10 @@ def bfp8_moe_combine(y, token_rows, token_weights, out, stream=None) -> None:
 
 def bfp8_device_status(stream=None) -> int:
     return int(_lib.bfp8_device_status(_stream(stream)))
+
+
+def bfp8_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Launch the bounded-wait self-test (a barrier whose second arrival never
+    comes); the next bfp8_device_status() reports the timeout."""
+    _check(_lib.bfp8_selftest_wait_timeout(int(limit_ns), _stream(stream)),
+           "bfp8_selftest_wait_timeout")

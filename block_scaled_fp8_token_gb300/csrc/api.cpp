@@ -515,6 +515,10 @@ int bfp8_grouped_linear_silu_quant(const void* q_a, const float* s_a, int64_t s_
                                     sh_stride_m, sh_stride_kb, workspace, ws_bytes, stream);
 }
 
+int bfp8_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+  return launch_wait_selftest(limit_ns, stream);
+}
+
 int bfp8_device_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return BFP8_ERR_CUDA;

@@ -118,6 +118,8 @@ int launch_decode_ffn(int32_t arith, const void* x, int64_t ldx, const void* w_g
 // Device error words, one per translation unit with bounded waits: read and
 // clear. Return BFP8_OK, BFP8_ERR_TIMEOUT or BFP8_ERR_CUDA.
 int gemm_read_clear_error();
+// One bounded wait that runs out after limit_ns (0 < limit_ns <= 2 s).
+int launch_wait_selftest(uint64_t limit_ns, void* stream);
 int gemv_read_clear_error();
 
 }  // namespace bfp8

@@ -1588,6 +1588,35 @@ int launch_grouped_w8a8_swiglu(const void* q_a, const float* s_a, int64_t sa_sm,
   return launch<kBN8, kStagesSwiglu, false, true, true>(ta, tb, ty, p, 0x7FFFFFFF, stream);
 }
 
+// The bounded waits' self-test: a barrier that expects two arrivals gets one.
+// Warp 0 waits on it the way the promotion warps wait, warp 1 the way the
+// control warps wait (suspending); both give up after limit_ns, and the
+// timeout is recorded in the device error word like any kernel's.
+__global__ void __launch_bounds__(64, 1) wait_selftest_kernel(unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_word;
+  volatile int* abort_flag = &abort_word;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 2);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_arrive(b);   // the second arrival is withheld
+  __syncthreads();
+  const bool ok = (threadIdx.x >> 5) == 0
+                      ? __all_sync(0xffffffffu, mbar_wait(b, 0, abort_flag, limit_ns))
+                      : __all_sync(0xffffffffu, mbar_wait_sleep(b, 0, abort_flag, limit_ns));
+  if (!ok && (threadIdx.x & 31) == 0) raise_abort(abort_flag);
+}
+
+int launch_wait_selftest(uint64_t limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns > kWaitLimitNs) return BFP8_ERR_INVALID_ARG;
+  wait_selftest_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns);
+  return check_launch();
+}
+
 int gemm_read_clear_error() {
   int v = 0;
   const int zero = 0;

@@ -69,15 +69,17 @@ BFP8_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 // Wait for the phase with the given parity to complete. Returns false if the
 // CTA-wide abort flag is raised or the time limit runs out; in the latter case
-// the caller raises the abort flag and the device error word.
-BFP8_DEV bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+// the caller raises the abort flag and the device error word. (Kernels use the
+// default limit; the wait self-test passes a short one.)
+BFP8_DEV bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
+                        unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0u) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) return false;
+      if (globaltimer() - t0 > limit_ns) return false;
     }
   }
 }
@@ -100,7 +102,8 @@ BFP8_DEV bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
 // The clock is read only once the first test has failed: on a phase that is
 // already complete the wait costs one test (reading the global timer first
 // took about four times as long).
-BFP8_DEV bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+BFP8_DEV bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
+                              unsigned long long limit_ns = kWaitLimitNs) {
   constexpr uint32_t kHintNs = 2000;
   if (mbar_try_wait_hint(bar, parity, kHintNs)) return true;
   const uint64_t t0 = globaltimer();
@@ -108,7 +111,7 @@ BFP8_DEV bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const volatile int*
     if (mbar_try_wait_hint(bar, parity, kHintNs)) return true;
     if ((i & 7u) == 7u) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) return false;
+      if (globaltimer() - t0 > limit_ns) return false;
     }
   }
 }

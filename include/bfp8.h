@@ -521,6 +521,19 @@ int bfp8_moe_combine(const void* y_bf16, int64_t R, int64_t H, int64_t ldy,
  */
 int bfp8_device_status(void* stream);
 
+/*
+ * bfp8_selftest_wait_timeout -- exercise the bounded device waits: launch one
+ * CTA on `stream` whose barrier gets one of the two arrivals it expects. Two
+ * warps wait on it, one in the promotion warps' spinning form and one in the
+ * control warps' suspending form; both give up after limit_ns nanoseconds and
+ * record BFP8_ERR_TIMEOUT in the device error word, which the next
+ * bfp8_device_status() returns (and clears). The kernel then exits normally:
+ * the context stays usable. This is a library diagnostic, not part of the
+ * projection. Errors: INVALID_ARG unless 0 < limit_ns <= 2e9 (the kernels'
+ * own limit).
+ */
+int bfp8_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

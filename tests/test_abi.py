@@ -123,6 +123,9 @@ def test_every_entry_point_refuses_bad_arguments_without_gpu(bfp8):
         (lib.bfp8_moe_gather_act_quant(p, 8, 256, 256, p, -1, p, 256, p, 2, 1, None), INVAL),
         (lib.bfp8_moe_combine(p, 16, 256, 256, p, p, 8, 0, p, 256, None), INVAL),
         (lib.bfp8_moe_combine(p, 16, 256, 256, p, p, 8, 2, p, 255, None), INVAL),
+        # wait self-test: the limit must lie in (0, 2 s]
+        (lib.bfp8_selftest_wait_timeout(0, None), INVAL),
+        (lib.bfp8_selftest_wait_timeout(2_000_000_001, None), INVAL),
     ]
     for i, (got, want) in enumerate(cases):
         assert got == want, (i, got, want)
