@@ -96,9 +96,17 @@ def dense_ffn(seed: int = 0, M: int | None = None) -> dict:
     return {"w_gate_up": w_gu, "w_down": w_d, "x": x}
 
 
-def decode_tokens(seed: int, M: int, K: int) -> torch.Tensor:
-    """BF16 [M, K] N(0, 1) decode tokens (no outliers)."""
-    return activations_bf16(generator(seed), M, K)
+# outlier recipes of the activation workloads: 1% of entries x20 (the single
+# linear) and 0.5% of channels x30 (the dense-FFN prefill)
+OUTLIERS = {"entries": dict(frac=0.01, factor=20.0), "channels": dict(frac=0.005, factor=30.0)}
+
+
+def decode_tokens(seed: int, M: int, K: int, outlier: str | None = None) -> torch.Tensor:
+    """BF16 [M, K] N(0, 1) decode tokens, optionally with one of the
+    activation workloads' outlier patterns (OUTLIERS)."""
+    if outlier is None:
+        return activations_bf16(generator(seed), M, K)
+    return activations_bf16(generator(seed), M, K, outlier=outlier, **OUTLIERS[outlier])
 
 
 def attention(seed: int = 0, M: int | None = None) -> dict:

@@ -15,6 +15,9 @@ decode shapes (hidden 5120, intermediate 17408; gate/up [34816, 5120], down
   token entries far below their block's maximum to within 2^-17 of it) move
   single h values by one BF16 ulp, a quantization-level difference, so each
   token meets the same accuracy gate as W8A8.
+* Tokens: plain N(0, 1), and with the activation workloads' outlier
+  patterns (1% of entries x20, 0.5% of channels x30), the W8A16 arm's
+  hi/lo token split at its worst case.
 * Both: a CUDA graph captured around one step and replayed on new tokens
   gives the same bytes as an eager step on those tokens, and M = 1 (smallest)
   and M = 16 (the limit) both run.
@@ -74,13 +77,14 @@ def _chain_of_entry_points(bfp8, dev, x, w):
     return y
 
 
-@pytest.mark.parametrize("M", [1, 4, 16])
+@pytest.mark.parametrize("M,outlier", [(1, None), (4, None), (16, None), (1, "entries"),
+                                       (16, "entries"), (16, "channels")])
 @pytest.mark.parametrize("arith", ["w8a16", "w8a8"])
-def test_decode_step(bfp8, cuda_device, weights, arith, M):
+def test_decode_step(bfp8, cuda_device, weights, arith, M, outlier):
     dev = cuda_device
     host, w = weights
     code = bfp8.BFP8_DECODE_W8A8 if arith == "w8a8" else bfp8.BFP8_DECODE_W8A16
-    xb = bits16(synth.decode_tokens(300 + M, M, H))
+    xb = bits16(synth.decode_tokens(300 + M, M, H, outlier))
     x = to_dev_bf16(xb, dev)
     y = _step(bfp8, dev, x, w, code)
     ref = CH.decode_ffn(xb, *host, arith=arith)
