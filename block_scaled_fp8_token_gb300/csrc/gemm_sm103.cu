@@ -275,9 +275,34 @@ struct Cfg {
 // Work item t is one M tile of one N tile of TW output columns (M tiles
 // fastest). The up-half fields serve the fused SiLU*up epilogue, whose tile of
 // TW output columns reads TW gate rows and the TW matching up rows of W.
+// The expert of grouped tile t: the last e >= e_hint with s_pre[e] <= t
+// (t < s_pre[G]). Each caller walks its tiles in increasing order, so the
+// search starts at the previous tile's expert. lane >= 0: the whole
+// (converged) warp tests 32 expert boundaries at once and a ballot counts
+// those at or before t (s_pre is non-decreasing, so they are lanes 0..n-1);
+// lane < 0: one thread scans forward. (A binary search over all experts took
+// ~900 clk of every grouped tile end; the forward scan ~600.)
+BFP8_DEV int find_expert(const int* s_pre, int G, int t, int e_hint, int lane) {
+  int e = e_hint;
+  if (lane < 0) {
+#pragma unroll 1
+    while (s_pre[e + 1] <= t) ++e;
+    return e;
+  }
+#pragma unroll 1
+  for (;;) {
+    const int i = e + 1 + lane;
+    const uint32_t m = __ballot_sync(0xffffffffu, i <= G && s_pre[i] <= t);
+    const int n = __popc(m);
+    e += n;
+    if (n < 32) return e;
+  }
+}
+
 template <int TW, bool GROUPED>
 __device__ __forceinline__ void decode_tile(const GemmParams& p, const int* s_off,
-                                            const int* s_pre, int t, Tile& tl) {
+                                            const int* s_pre, int t, Tile& tl, int& e_hint,
+                                            int lane) {
   if (!GROUPED) {
     const int nt = t / p.m_tiles;
     const int mt = t - nt * p.m_tiles;
@@ -296,13 +321,8 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, const int* s_of
     tl.b_row0_up = p.up_row0 + nl0;
     tl.srow_up = p.up_sbase + nl0 / 128;
   } else {
-    int lo = 0, hi = p.G;  // invariant: s_pre[lo] <= t < s_pre[hi]
-#pragma unroll 1
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_pre[mid] <= t) lo = mid; else hi = mid;
-    }
-    const int e = lo;
+    const int e = find_expert(s_pre, p.G, t, e_hint, lane);
+    e_hint = e;
     const int row0 = s_off[e];
     const int rows = s_off[e + 1] - row0;
     const int units = (rows + BM - 1) / BM;
@@ -600,9 +620,12 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
   // also needs every CTA to own at least one K-block unit of the split part.
   const int waves = (total + ncl - 1) / ncl;
   // Dense: last-wave fill < 85% (O at M=4096, 84%, gains 4%; QKV at 93% loses
-  // 2%; gate/up at 89%, plain or fused, gains nothing in the chain). Grouped
-  // tiles are short and their split tiles cost more: < 80%.
-  const int fill_pct = GROUPED ? 80 : 85;
+  // 2%; plain gate/up at 89% gains nothing). The fused SiLU*up instance splits
+  // below 95%: its tile end is longer, and at 89% (the dense-FFN gate/up,
+  // 1,088 tiles) the 24 CTAs with an eighth whole tile ran ~30 us past the
+  // others (-4% with the split). Grouped tiles are short and their split
+  // tiles cost more: < 80%.
+  const int fill_pct = GROUPED ? 80 : (SWIGLU ? 95 : 85);
   const bool sparse_tail = waves > 0 && 100 * total < fill_pct * waves * ncl;
   const bool sk = p.stream_k && sparse_tail &&
                   sk_geo(true, total, p.Kb, ncl, 0).U >= static_cast<int64_t>(ncl);
@@ -619,11 +642,12 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
         uint32_t phase = 0, armed = 0, armed_phase = 0;
         bool ok = true;
         bool a_ready = false;    // activations are read only after the dependency wait
+        int e_hint = 0;        // grouped: expert of the previous tile
         SegIter it = seg_begin(sk, total, p.Kb, cid, ncl, mu_lock);
         int t, kb0, kb1;
         while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
           Tile tl;
-          decode_tile<C::kOutCols, GROUPED>(p, s_off, s_pre, t, tl);
+          decode_tile<C::kOutCols, GROUPED>(p, s_off, s_pre, t, tl, e_hint, -1);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait_sleep(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
             const uint32_t sA = base + stage * C::kStage;
@@ -668,11 +692,12 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
         int rs = 0;
         uint32_t rphase = 0, armed = 0, armed_phase = 0;
         bool ok = true;
+        int e_hint = 0;
         SegIter it = seg_begin(sk, total, p.Kb, cid, ncl, mu_lock);
         int t, kb0, kb1;
         while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
           Tile tl;
-          decode_tile<C::kOutCols, GROUPED>(p, s_off, s_pre, t, tl);
+          decode_tile<C::kOutCols, GROUPED>(p, s_off, s_pre, t, tl, e_hint, -1);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait_sleep(raw_empty(rs), rphase ^ 1u, abort_flag)) { ok = false; break; }
             const uint32_t sR = base + C::kOffRaw + rs * C::kBRawBytes;
@@ -756,18 +781,23 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
       int slot = 0;
       uint32_t fphase = 0;
       bool ok = true;
+      int e_hint = 0;
       SegIter it = seg_begin(sk, total, p.Kb, cid, ncl, mu_lock);
       int t, kb0, kb1;
       while (ok && next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
         Tile tl;
-        decode_tile<C::kOutCols, GROUPED>(p, s_off, s_pre, t, tl);
+        decode_tile<C::kOutCols, GROUPED>(p, s_off, s_pre, t, tl, e_hint, lane);
         const int64_t sw_base = GROUPED ? tl.expert * p.sw_expert_stride : 0;
         const int srow0 = SWIGLU ? tl.srow0 : tl.srow0;
         const int srow1 = SWIGLU ? tl.srow_up : min(tl.srow0 + C::kEpiCols / 128, tl.srow_last);
         const int64_t i0 = sw_base + static_cast<int64_t>(srow0) * p.sw_rs;
         const int64_t i1 = sw_base + static_cast<int64_t>(srow1) * p.sw_rs;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait_sleep(fempty_bar(slot), fphase ^ 1u, abort_flag)) { ok = false; break; }
+          // voted: the warp stays converged for the warp-wide tile decode
+          if (!__all_sync(0xffffffffu, mbar_wait_sleep(fempty_bar(slot), fphase ^ 1u, abort_flag))) {
+            ok = false;
+            break;
+          }
           const float w0 = fscale(i0 + static_cast<int64_t>(kb) * p.sw_ks);
           const float w1 = fscale(i1 + static_cast<int64_t>(kb) * p.sw_ks);
           float* f = fac + slot * (2 * BM);
@@ -793,6 +823,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
       pdl_wait();
       uint32_t ph = 0;
       bool ok = true;
+      int e_hint = 0;        // tiles arrive in increasing order
       for (;;) {
         if (!__all_sync(0xffffffffu, mbar_wait_sleep(stg_full, ph, abort_flag))) {
           ok = false;
@@ -801,7 +832,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
         const int t = *stg_tile;
         if (t < 0) break;
         Tile tl;
-        decode_tile<C::kOutCols, GROUPED>(p, s_off, s_pre, t, tl);
+        decode_tile<C::kOutCols, GROUPED>(p, s_off, s_pre, t, tl, e_hint, lane);
         silu_quant_tile(p, tl, hstg, pair_flags, lane, warp - C::kSiluWarp0, C::kSiluWarps);
         __syncwarp();
         if (lane == 0) mbar_arrive(stg_empty);
@@ -828,11 +859,12 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, W8A16, GROUPED, SWIGLU>::kThre
     bool ok = true;
     // Every epilogue warp walks every segment, even after a failed wait, so
     // that all of them reach the same named barriers (those cannot time out).
+    int e_hint = 0;
     SegIter it = seg_begin(sk, total, p.Kb, cid, ncl, mu_lock);
     int t, kb0, kb1;
     while (next_seg(sk, it, total, p.Kb, t, kb0, kb1)) {
       Tile tl;
-      decode_tile<C::kOutCols, GROUPED>(p, s_off, s_pre, t, tl);
+      decode_tile<C::kOutCols, GROUPED>(p, s_off, s_pre, t, tl, e_hint, lane);
       const bool row_ok = row_in_tile < tl.m_valid;
       const int64_t arow = static_cast<int64_t>(tl.a_row0) + row_in_tile;
       // This warp's columns of the tile: 128 consecutive ones (one weight-scale
