@@ -164,28 +164,28 @@ int launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s
   return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? BFP8_OK : BFP8_ERR_CUDA;
 }
 
-// One CTA per K-block, 64 threads: thread t handles token t / 4 and the 32
-// values [32*(t%4), +32) of the block. Writes the hi/lo E4M3 rows of the
-// block's 32 x 128 token tile (row-major; TMA applies the swizzle on load)
-// and 2^-e per token. Tokens past M get zero rows.
+// One CTA per K-block, 256 threads: thread t handles token t / 16 and the 8
+// values [8*(t%16), +8) of the block (16 threads per token: the exact SiLU*up
+// of the second split is ~40 instructions a value, and 64 threads a block
+// left it latency-bound). Writes the hi/lo E4M3 rows of the block's 32 x 128
+// token tile (row-major; TMA applies the swizzle on load) and 2^-e per token.
+// Tokens past M get zero rows.
 // It also clears the GEMV's split-tile counters; the GEMV touches them only
 // after its griddepcontrol.wait.
 // SILU == true: x is a gate/up output [M, 2K] (gate columns 0..K-1, up columns
 // K..2K-1) and the tokens are h = bf16(silu(gate) * up), formed with the same
 // arithmetic as the SiLU*up quantizer.
-BFP8_DEV void load_token_words(const __nv_bfloat16* row, bool in_range, int c0, int K,
-                               uint32_t (&xw)[16]) {
-  if (in_range && c0 + 32 <= K) {
-    const uint4* src = reinterpret_cast<const uint4*>(row + c0);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint4 v = src[c];
-      xw[4 * c] = v.x; xw[4 * c + 1] = v.y; xw[4 * c + 2] = v.z; xw[4 * c + 3] = v.w;
-    }
+constexpr int kSplitThreads = 256;
+
+BFP8_DEV void load_token_words8(const __nv_bfloat16* row, bool in_range, int c0, int K,
+                                uint32_t (&xw)[4]) {
+  if (in_range && c0 + 8 <= K) {
+    const uint4 v = *reinterpret_cast<const uint4*>(row + c0);   // 16-byte aligned: ldx % 8 == 0
+    xw[0] = v.x; xw[1] = v.y; xw[2] = v.z; xw[3] = v.w;
   } else {
     const uint16_t* xr = reinterpret_cast<const uint16_t*>(row);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < 4; ++j) {
       const uint32_t lo = (in_range && c0 + 2 * j < K) ? xr[c0 + 2 * j] : 0u;
       const uint32_t hi = (in_range && c0 + 2 * j + 1 < K) ? xr[c0 + 2 * j + 1] : 0u;
       xw[j] = lo | (hi << 16);
@@ -194,7 +194,7 @@ BFP8_DEV void load_token_words(const __nv_bfloat16* row, bool in_range, int c0, 
 }
 
 template <bool SILU>
-__global__ void __launch_bounds__(64) gemv_split_tokens_kernel(
+__global__ void __launch_bounds__(kSplitThreads) gemv_split_tokens_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t ldx, int32_t M, int32_t K,
     uint8_t* __restrict__ xtile, float* __restrict__ xinv, int32_t* __restrict__ counters,
     int32_t n_counters) {
@@ -203,35 +203,38 @@ __global__ void __launch_bounds__(64) gemv_split_tokens_kernel(
   // workspace, or wrote x) is still running: wait for it before any access.
   pdl_wait();
   const int kb = blockIdx.x;
-  for (int i = kb * 64 + threadIdx.x; i < n_counters; i += gridDim.x * 64) counters[i] = 0;
-  const int tok = threadIdx.x >> 2, q4 = threadIdx.x & 3;
-  const int c0 = kb * 128 + 32 * q4;
-  const __nv_bfloat16* row = x + static_cast<int64_t>(tok < M ? tok : 0) * ldx;
-  uint32_t xw[16];
-  load_token_words(row, tok < M, c0, K, xw);
+  for (int i = kb * kSplitThreads + threadIdx.x; i < n_counters; i += gridDim.x * kSplitThreads)
+    counters[i] = 0;
+  const int tok = threadIdx.x >> 4, s16 = threadIdx.x & 15;
+  const int c0 = kb * 128 + 8 * s16;
+  const bool live = tok < M;
+  const __nv_bfloat16* row = x + static_cast<int64_t>(live ? tok : 0) * ldx;
+  uint32_t xw[4];
+  load_token_words8(row, live, c0, K, xw);
   if constexpr (SILU) {
-    uint32_t uw[16];
-    load_token_words(row + K, tok < M, c0, K, uw);
+    uint32_t uw[4];
+    load_token_words8(row + K, live, c0, K, uw);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < 4; ++j) {
       const float h0 = silu_mul_bf16_round(__uint_as_float(xw[j] << 16), __uint_as_float(uw[j] << 16));
       const float h1 = silu_mul_bf16_round(__uint_as_float(xw[j] & 0xFFFF0000u),
                                            __uint_as_float(uw[j] & 0xFFFF0000u));
       xw[j] = (__float_as_uint(h0) >> 16) | (__float_as_uint(h1) & 0xFFFF0000u);
     }
   }
-  // the row's max |x| (non-negative BF16 patterns order like their values)
+  // the token's max |x| over the block (non-negative BF16 patterns order like
+  // their values), across its 16 threads
   uint32_t m = 0;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) m = __vmaxu2(m, xw[j] & 0x7FFF7FFFu);
+  for (int j = 0; j < 4; ++j) m = __vmaxu2(m, xw[j] & 0x7FFF7FFFu);
   m = max(m & 0xFFFFu, m >> 16);
-  m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-  m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
   const int e = min(max(134 - static_cast<int>((m >> 7) & 0xFFu), -126), 126);
   const float up = __int_as_float((e + 127) << 23);
-  uint32_t hw[8], lw[8];
+  uint32_t hw[2], lw[2];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
+  for (int j = 0; j < 4; ++j) {
     const float v0 = __uint_as_float(xw[j] << 16) * up;
     const float v1 = __uint_as_float(xw[j] & 0xFFFF0000u) * up;
     const uint16_t hi = f32x2_to_e4m3x2(v0, v1);
@@ -245,13 +248,11 @@ __global__ void __launch_bounds__(64) gemv_split_tokens_kernel(
       lw[j >> 1] = lo;
     }
   }
-  uint4* dh = reinterpret_cast<uint4*>(xtile + (static_cast<int64_t>(kb) * 32 + tok) * 128 + 32 * q4);
-  uint4* dl = reinterpret_cast<uint4*>(xtile + (static_cast<int64_t>(kb) * 32 + 16 + tok) * 128 + 32 * q4);
-  dh[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-  dh[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-  dl[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-  dl[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
-  if (q4 == 0) xinv[kb * 16 + tok] = __int_as_float((127 - e) << 23);
+  *reinterpret_cast<uint2*>(xtile + (static_cast<int64_t>(kb) * 32 + tok) * 128 + 8 * s16) =
+      make_uint2(hw[0], hw[1]);
+  *reinterpret_cast<uint2*>(xtile + (static_cast<int64_t>(kb) * 32 + 16 + tok) * 128 + 8 * s16) =
+      make_uint2(lw[0], lw[1]);
+  if (s16 == 0) xinv[kb * 16 + tok] = __int_as_float((127 - e) << 23);
 }
 
 // Clears the split-tile counters ahead of the W8A8 arm's GEMV, which runs as
@@ -611,9 +612,9 @@ int launch_kernels(const void* x, int64_t ldx, uint8_t* xtile, float* xinv, cons
                    const CUtensorMap& tx, const GemvParams& p, void* stream, bool silu = false) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-  int rc = silu ? launch_pdl(gemv_split_tokens_kernel<true>, dim3(p.Kb), dim3(64), 0, st, xb, ldx,
+  int rc = silu ? launch_pdl(gemv_split_tokens_kernel<true>, dim3(p.Kb), dim3(kSplitThreads), 0, st, xb, ldx,
                              p.M, p.K, xtile, xinv, p.counters, p.RT)
-                : launch_pdl(gemv_split_tokens_kernel<false>, dim3(p.Kb), dim3(64), 0, st, xb, ldx,
+                : launch_pdl(gemv_split_tokens_kernel<false>, dim3(p.Kb), dim3(kSplitThreads), 0, st, xb, ldx,
                              p.M, p.K, xtile, xinv, p.counters, p.RT);
   if (rc != BFP8_OK) return rc;
   rc = check_launch();
