@@ -28,9 +28,9 @@ constexpr int kThreads = 256;
 // the 8-column chunks that start at 32 i + 8 ql (i = 0..3), so each 16-byte
 // load of a quad covers 64 contiguous bytes and each 8-byte store 32. The
 // per-group work (the maximum over the quad, the scale, its reciprocal, the
-// scale store, the index update) is spread over 32 elements per lane.
+// scale store, the index update) is spread over 32 elements per lane. (Small
+// inputs use 16 lanes a group: act_quant_kernel's GT.)
 constexpr int kQuad = 4;
-constexpr int kChunks = 4;
 
 // row[c .. c+8) as four bf16x2 words, zero past K. FULL: the caller knows the
 // chunk is in range and 16-byte aligned.
@@ -74,7 +74,11 @@ __device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w 
 // BF16-rounded h), and every quotient is the correctly rounded x / s.
 // FULL: K is a multiple of 128 and every row and pitch is aligned for 16-byte
 // loads and 8-byte stores, so no chunk needs a bounds or alignment test.
-template <bool SILU, bool FULL>
+// GT threads share a 128-value group, 128 / GT values each: 4 (32 values a
+// thread) for large inputs; 16 (8 values) when the groups are too few to fill
+// the GPU with 4 threads each (the decode step's SiLU*up quantization of 16
+// tokens is ~40 instructions a value and ran latency-bound on 4).
+template <bool SILU, bool FULL, int GT = kQuad>
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K, int64_t ld,
     uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s, int64_t ssm, int64_t sskb,
@@ -83,9 +87,10 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(
   pdl_launch_dependents();
   pdl_wait();
   const int64_t Kb = (K + 127) / 128;
-  const int ql = threadIdx.x & (kQuad - 1);
-  const int64_t quad = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / kQuad;
-  const int64_t nquad = static_cast<int64_t>(gridDim.x) * blockDim.x / kQuad;
+  constexpr int kCh = 16 / GT;  // 8-value chunks per thread
+  const int ql = threadIdx.x & (GT - 1);
+  const int64_t quad = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / GT;
+  const int64_t nquad = static_cast<int64_t>(gridDim.x) * blockDim.x / GT;
   // (m, g) of this quad's group, advanced by nquad groups per pass without a division
   int64_t m = quad / Kb, g = quad - m * Kb;
   const int64_t dm = nquad / Kb, dg = nquad - dm * Kb;
@@ -94,19 +99,19 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(
     const int64_t src = !live ? -1 : (rows ? static_cast<int64_t>(__ldg(rows + m)) : m);
     const bool ok = src >= 0 && src < n_src;
     const __nv_bfloat16* row = x + (ok ? src : 0) * ld;
-    const int64_t c0 = g * 128 + ql * 8;
-    uint32_t a[kChunks][4];
-    float h[SILU ? kChunks : 1][8];
+    const int64_t c0 = g * 128 + ql * 8;   // chunk i at c0 + 8 * GT * i
+    uint32_t a[kCh][4];
+    float h[SILU ? kCh : 1][8];
     float amax;
     if constexpr (SILU) {
       amax = 0.0f;
 #pragma unroll
-      for (int i = 0; i < kChunks; ++i) {
+      for (int i = 0; i < kCh; ++i) {
         uint32_t u[4] = {0u, 0u, 0u, 0u};
         a[i][0] = a[i][1] = a[i][2] = a[i][3] = 0u;
         if (ok) {
-          load_chunk<FULL>(row, c0 + 32 * i, K, vec_in, a[i]);
-          load_chunk<FULL>(row + K, c0 + 32 * i, K, vec_in, u);
+          load_chunk<FULL>(row, c0 + 8 * GT * i, K, vec_in, a[i]);
+          load_chunk<FULL>(row + K, c0 + 8 * GT * i, K, vec_in, u);
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -115,21 +120,21 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(
           amax = fmaxf(amax, fmaxf(fabsf(h[i][2 * j]), fabsf(h[i][2 * j + 1])));
         }
       }
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+#pragma unroll
+      for (int o = 1; o < GT; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     } else {
       uint32_t mx = 0u;
 #pragma unroll
-      for (int i = 0; i < kChunks; ++i) {
+      for (int i = 0; i < kCh; ++i) {
         a[i][0] = a[i][1] = a[i][2] = a[i][3] = 0u;
-        if (ok) load_chunk<FULL>(row, c0 + 32 * i, K, vec_in, a[i]);
+        if (ok) load_chunk<FULL>(row, c0 + 8 * GT * i, K, vec_in, a[i]);
 #pragma unroll
         for (int j = 0; j < 4; ++j) mx = max_u16x2(mx, a[i][j] & 0x7FFF7FFFu);
       }
       // |x| of a finite BF16 orders like its bit pattern with the sign cleared
       uint32_t am = max(mx & 0xFFFFu, mx >> 16);
-      am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
-      am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
+#pragma unroll
+      for (int o = 1; o < GT; o <<= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, o));
       amax = __uint_as_float(am << 16);
     }
     const float sc = group_scale(amax);
@@ -137,7 +142,7 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(
     const float2 y2 = make_float2(rc, rc), ns2 = make_float2(-sc, -sc);
     uint8_t* qrow = q + (live ? m : 0) * ldq;
 #pragma unroll
-    for (int i = 0; i < kChunks; ++i) {
+    for (int i = 0; i < kCh; ++i) {
       uint16_t p[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -148,7 +153,7 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(
       }
       const uint32_t w0 = static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[1]) << 16);
       const uint32_t w1 = static_cast<uint32_t>(p[2]) | (static_cast<uint32_t>(p[3]) << 16);
-      const int64_t c = c0 + 32 * i;
+      const int64_t c = c0 + 8 * GT * i;
       if (!live) continue;
       if (FULL || (vec_out && c + 8 <= K)) {
         *reinterpret_cast<uint2*>(qrow + c) = make_uint2(w0, w1);
@@ -407,7 +412,9 @@ int act_quant_common(bool silu, const void* x, int64_t M, int64_t K, int64_t ld,
       resident_blocks(act_quant_kernel<false, false>), resident_blocks(act_quant_kernel<true, false>),
       resident_blocks(act_quant_kernel<false, true>), resident_blocks(act_quant_kernel<true, true>)};
   const int64_t items = M * Kb;
-  const int64_t per_block = kThreads / kQuad;   // groups one block covers per pass
+  // 16 lanes a group when 4 would not give every SM two blocks
+  const bool wide = items * kQuad < static_cast<int64_t>(2 * sms) * kThreads;
+  const int64_t per_block = kThreads / (wide ? 16 : kQuad);   // groups one block covers per pass
   const int64_t want = (items + per_block - 1) / per_block;
   const int64_t cap = static_cast<int64_t>(sms) * per_sm[(silu ? 1 : 0) + (full ? 2 : 0)];
   const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
@@ -417,8 +424,13 @@ int act_quant_common(bool silu, const void* x, int64_t M, int64_t K, int64_t ld,
                             static_cast<uint8_t*>(q), ldq, s, ssm, sskb, vec_in, vec_out, rows,
                             rows ? n_src : M);
   };
-  const int lrc = silu ? (full ? go(act_quant_kernel<true, true>) : go(act_quant_kernel<true, false>))
-                       : (full ? go(act_quant_kernel<false, true>) : go(act_quant_kernel<false, false>));
+  int lrc;
+  if (wide)
+    lrc = silu ? (full ? go(act_quant_kernel<true, true, 16>) : go(act_quant_kernel<true, false, 16>))
+               : (full ? go(act_quant_kernel<false, true, 16>) : go(act_quant_kernel<false, false, 16>));
+  else
+    lrc = silu ? (full ? go(act_quant_kernel<true, true>) : go(act_quant_kernel<true, false>))
+               : (full ? go(act_quant_kernel<false, true>) : go(act_quant_kernel<false, false>));
   if (lrc != BFP8_OK) return lrc;
   return check_launch();
 }
