@@ -171,6 +171,23 @@ def test_grouped_fused_small_with_empty_experts(bfp8, cuda_device, I):
            _grouped_h_ref(qa, sa, qw, sw, offsets, rows), f"grouped fused I={I}")
 
 
+def test_grouped_fused_sparse_experts(bfp8, cuda_device):
+    """200 experts, most of them empty: the SiLU warps and the epilogue find
+    each tile's expert more than 32 experts past the previous one's."""
+    from test_gpu_grouped import sparse_offsets
+    offsets = sparse_offsets()
+    G, I, K = 200, 128, 256
+    g = synth.generator(47)
+    qw, sw = _stack_members(synth.weight_stack_f32(g, G, 2 * I, K).numpy(), I)
+    xb = bits16(synth.activations_bf16(g, offsets[-1], K))
+    qa, sa = Q.act_quant_group(xb)
+    q, s = _grouped_fused(bfp8, cuda_device, qa, sa, qw, sw, offsets)
+    rows = np.arange(offsets[-1])
+    q_ref, s_ref = CH.grouped_gate_up_silu_quant(qa, sa, qw, sw, offsets)
+    _check(q.cpu().numpy(), s.cpu().numpy(), q_ref, s_ref,
+           _grouped_h_ref(qa, sa, qw, sw, offsets, rows), "grouped fused sparse experts")
+
+
 def test_grouped_fused_moe_workload(bfp8, cuda_device):
     """8192 tokens x top-8 of 128 experts (65,536 routed rows), hidden 2048,
     expert gate/up [1536, 2048]: sampled rows of every expert against the

@@ -53,6 +53,31 @@ def test_grouped_small_with_empty_experts(bfp8, cuda_device, stream_k):
     assert_close(y, L.grouped_linear_w8a8(qa, sa, qw, sw, offsets), "grouped small")
 
 
+# 200 experts, a few with rows, the others empty: a tile's expert can lie more
+# than 32 experts past the previous tile's, so every walker's expert lookup
+# (a warp-wide ballot over 32 expert boundaries at a time) takes several steps.
+SPARSE_ROWS = {0: 130, 37: 60, 75: 200, 76: 5, 150: 129, 199: 70}
+
+
+def sparse_offsets(G=200):
+    offsets = [0]
+    for e in range(G):
+        offsets.append(offsets[-1] + SPARSE_ROWS.get(e, 0))
+    return offsets
+
+
+@pytest.mark.parametrize("stream_k", [True, False], ids=["stream_k", "whole_tiles"])
+def test_grouped_sparse_experts(bfp8, cuda_device, stream_k):
+    offsets = sparse_offsets()
+    G, N, K = 200, 256, 256
+    g = synth.generator(45)
+    qw, sw = _stack_quant(synth.weight_stack_f32(g, G, N, K).numpy())
+    xb = bits16(synth.activations_bf16(g, offsets[-1], K))
+    qa, sa = Q.act_quant_group(xb)
+    y = gpu_bf16_to_f64(_grouped(bfp8, cuda_device, qa, sa, qw, sw, offsets, stream_k))
+    assert_close(y, L.grouped_linear_w8a8(qa, sa, qw, sw, offsets), "grouped sparse experts")
+
+
 def test_grouped_moe_workload(bfp8, cuda_device):
     d = synth.moe(0)
     c = synth.MOE_PREFILL
