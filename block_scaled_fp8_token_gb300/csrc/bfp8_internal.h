@@ -56,10 +56,15 @@ inline bool weight_scale_f32(int32_t d) {
 inline bool weight_scale_per_tensor(int32_t d) { return (d & BFP8_SCALE_PER_TENSOR) != 0; }
 
 // Launchers (argument checks beyond the common ones happen inside).
+// The two 1x128 quantizers can also zero n_clear int32 counters at `clear`
+// once the previous kernel on the stream has finished (the decode step hands
+// them the next GEMV's tile counters); M and K must then be nonzero.
 int launch_act_quant(const void* x, int64_t M, int64_t K, int64_t ldx, void* q, int64_t ldq,
-                     float* s, int64_t ssm, int64_t sskb, void* stream);
+                     float* s, int64_t ssm, int64_t sskb, void* stream, int32_t* clear = nullptr,
+                     int32_t n_clear = 0);
 int launch_silu_mul_act_quant(const void* gu, int64_t M, int64_t I, int64_t ld, void* q,
-                              int64_t ldq, float* s, int64_t ssm, int64_t sskb, void* stream);
+                              int64_t ldq, float* s, int64_t ssm, int64_t sskb, void* stream,
+                              int32_t* clear = nullptr, int32_t n_clear = 0);
 int launch_silu_mul(const void* gu, int64_t M, int64_t I, int64_t ld, void* h, int64_t ldh,
                     void* stream);
 int launch_moe_gather_act_quant(const void* x, int64_t T, int64_t H, int64_t ldx,
@@ -106,7 +111,9 @@ int launch_gemv(const void* x, int64_t ldx, const void* w, const void* w_scale,
 int launch_gemv_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
                      const void* w, const void* w_scale, int32_t w_scale_dtype, int64_t M,
                      int64_t N, int64_t K, void* y, int64_t ldy, const MemberTable& mt,
-                     void* workspace, size_t ws_bytes, void* stream);
+                     void* workspace, size_t ws_bytes, void* stream, bool clear_counters = true);
+// The W8A8 GEMV's tile counters: at the workspace's start, one per 128 rows of N.
+int32_t gemv_counter_count(int64_t N);
 
 // The dense-FFN decode step (gate/up GEMV -> SiLU*up -> down GEMV).
 size_t decode_ffn_workspace_bytes(int64_t M, int64_t H, int64_t I, int32_t arith, int sms);

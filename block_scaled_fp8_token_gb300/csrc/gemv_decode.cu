@@ -655,6 +655,8 @@ WsLayout ws_layout(int64_t N, int64_t K, int sms) {
 
 }  // namespace
 
+int32_t gemv_counter_count(int64_t N) { return static_cast<int32_t>((N + kRows - 1) / kRows); }
+
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K, int sms) {
   (void)M;
   if (N <= 0 || K <= 0 || sms <= 0) return 0;
@@ -731,7 +733,7 @@ int launch_gemv(const void* x, int64_t ldx, const void* w, const void* w_scale,
 int launch_gemv_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t sa_skb,
                      const void* w, const void* w_scale, int32_t w_scale_dtype, int64_t M,
                      int64_t N, int64_t K, void* y, int64_t ldy, const MemberTable& mt,
-                     void* workspace, size_t ws_bytes, void* stream) {
+                     void* workspace, size_t ws_bytes, void* stream, bool clear_counters) {
   if (reinterpret_cast<uintptr_t>(q_a) % 16 != 0) return BFP8_ERR_UNSUPPORTED;
   if (sa_sm < 0 || sa_skb < 0) return BFP8_ERR_INVALID_ARG;
   int rc = check_device_ptrs({q_a, s_a, w, w_scale, y, workspace});
@@ -752,10 +754,12 @@ int launch_gemv_w8a8(const void* q_a, const float* s_a, int64_t sa_sm, int64_t s
                     CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != BFP8_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  rc = launch_pdl(gemv_clear_counters_kernel, dim3(1), dim3(256), 0, st, p.counters, p.RT);
-  if (rc != BFP8_OK) return rc;
-  rc = check_launch();
-  if (rc != BFP8_OK) return rc;
+  if (clear_counters) {   // else the kernel before this one on the stream zeroed them
+    rc = launch_pdl(gemv_clear_counters_kernel, dim3(1), dim3(256), 0, st, p.counters, p.RT);
+    if (rc != BFP8_OK) return rc;
+    rc = check_launch();
+    if (rc != BFP8_OK) return rc;
+  }
   rc = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel<true>), kSmemBytes);
   if (rc != BFP8_OK) return rc;
   cudaLaunchConfig_t cfg{};
@@ -860,15 +864,21 @@ int launch_decode_ffn(int32_t arith, const void* x, int64_t ldx, const void* w_g
   float* sx = reinterpret_cast<float*>(ws + l.sx);
   uint8_t* qh = ws + l.qh;
   float* sh = reinterpret_cast<float*>(ws + l.sh);
-  rc = launch_act_quant(x, M, H, ldx, qx, H, sx, Hb, 1, stream);
+  // each quantizer zeroes the tile counters of the GEMV that follows it (the
+  // GEMV counters sit at the scratch region's start), once the kernel before
+  // it, which may be the previous GEMV still counting there, has finished
+  int32_t* counters = static_cast<int32_t*>(scratch);
+  rc = launch_act_quant(x, M, H, ldx, qx, H, sx, Hb, 1, stream, counters,
+                        gemv_counter_count(2 * I));
   if (rc != BFP8_OK) return rc;
   rc = launch_gemv_w8a8(qx, sx, Hb, 1, w_gu, s_gu, w_scale_dtype, M, 2 * I, H, gu, 2 * I, gu_mt,
-                        scratch, scratch_bytes, stream);
+                        scratch, scratch_bytes, stream, /*clear_counters=*/false);
   if (rc != BFP8_OK) return rc;
-  rc = launch_silu_mul_act_quant(gu, M, I, 2 * I, qh, I, sh, Ib, 1, stream);
+  rc = launch_silu_mul_act_quant(gu, M, I, 2 * I, qh, I, sh, Ib, 1, stream, counters,
+                                 gemv_counter_count(H));
   if (rc != BFP8_OK) return rc;
   return launch_gemv_w8a8(qh, sh, Ib, 1, w_dn, s_dn, w_scale_dtype, M, H, I, y, ldy, dn_mt,
-                          scratch, scratch_bytes, stream);
+                          scratch, scratch_bytes, stream, /*clear_counters=*/false);
 }
 
 // ---------------------------------------------------------------------------

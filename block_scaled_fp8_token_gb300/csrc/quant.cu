@@ -82,10 +82,15 @@ template <bool SILU, bool FULL, int GT = kQuad>
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t M, int64_t K, int64_t ld,
     uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s, int64_t ssm, int64_t sskb,
-    int vec_in, int vec_out, const int32_t* __restrict__ rows, int64_t n_src) {
+    int vec_in, int vec_out, const int32_t* __restrict__ rows, int64_t n_src,
+    int32_t* __restrict__ clr, int32_t n_clr) {
   // a programmatic dependent of the previous kernel: wait before any access
   pdl_launch_dependents();
   pdl_wait();
+  // zero a following kernel's counters (the decode step's GEMV tile counters),
+  // which saves that kernel a launch of its own
+  if (clr != nullptr && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < n_clr; i += blockDim.x) clr[i] = 0;
   const int64_t Kb = (K + 127) / 128;
   constexpr int kCh = 16 / GT;  // 8-value chunks per thread
   const int ql = threadIdx.x & (GT - 1);
@@ -391,16 +396,18 @@ int resident_blocks(Kernel kernel) {
 
 int act_quant_common(bool silu, const void* x, int64_t M, int64_t K, int64_t ld, void* q,
                      int64_t ldq, float* s, int64_t ssm, int64_t sskb, void* stream,
-                     const int32_t* rows = nullptr, int64_t n_src = 0) {
-  if (M < 0 || K < 0) return BFP8_ERR_INVALID_ARG;
-  if (M == 0 || K == 0) return BFP8_OK;
+                     const int32_t* rows = nullptr, int64_t n_src = 0, int32_t* clr = nullptr,
+                     int32_t n_clr = 0) {
+  if (M < 0 || K < 0 || n_clr < 0) return BFP8_ERR_INVALID_ARG;
+  // an empty input launches nothing, so it cannot carry a counter clear
+  if (M == 0 || K == 0) return clr ? BFP8_ERR_INVALID_ARG : BFP8_OK;
   if (!x || !q || !s) return BFP8_ERR_INVALID_ARG;
   const int64_t width = silu ? 2 * K : K;
   if (ld < width || ldq < K) return BFP8_ERR_INVALID_ARG;
   const int64_t Kb = (K + 127) / 128;
   if (ssm < 0 || sskb < 0 || (M > 1 && ssm == 0) || (Kb > 1 && sskb == 0))
     return BFP8_ERR_INVALID_ARG;
-  int rc = check_device_ptrs({x, q, s, rows});
+  int rc = check_device_ptrs({x, q, s, rows, clr});
   if (rc != BFP8_OK) return rc;
   int sms = 0;
   rc = sm_count(&sms);
@@ -422,7 +429,7 @@ int act_quant_common(bool silu, const void* x, int64_t M, int64_t K, int64_t ld,
   auto go = [&](auto kernel) {
     return launch_dependent(kernel, blocks, st, static_cast<const __nv_bfloat16*>(x), M, K, ld,
                             static_cast<uint8_t*>(q), ldq, s, ssm, sskb, vec_in, vec_out, rows,
-                            rows ? n_src : M);
+                            rows ? n_src : M, clr, clr ? n_clr : 0);
   };
   int lrc;
   if (wide)
@@ -438,13 +445,17 @@ int act_quant_common(bool silu, const void* x, int64_t M, int64_t K, int64_t ld,
 }  // namespace
 
 int launch_act_quant(const void* x, int64_t M, int64_t K, int64_t ldx, void* q, int64_t ldq,
-                     float* s, int64_t ssm, int64_t sskb, void* stream) {
-  return act_quant_common(false, x, M, K, ldx, q, ldq, s, ssm, sskb, stream);
+                     float* s, int64_t ssm, int64_t sskb, void* stream, int32_t* clear,
+                     int32_t n_clear) {
+  return act_quant_common(false, x, M, K, ldx, q, ldq, s, ssm, sskb, stream, nullptr, 0, clear,
+                          n_clear);
 }
 
 int launch_silu_mul_act_quant(const void* gu, int64_t M, int64_t I, int64_t ld, void* q,
-                              int64_t ldq, float* s, int64_t ssm, int64_t sskb, void* stream) {
-  return act_quant_common(true, gu, M, I, ld, q, ldq, s, ssm, sskb, stream);
+                              int64_t ldq, float* s, int64_t ssm, int64_t sskb, void* stream,
+                              int32_t* clear, int32_t n_clear) {
+  return act_quant_common(true, gu, M, I, ld, q, ldq, s, ssm, sskb, stream, nullptr, 0, clear,
+                          n_clear);
 }
 
 int launch_silu_mul(const void* gu, int64_t M, int64_t I, int64_t ld, void* h, int64_t ldh,
