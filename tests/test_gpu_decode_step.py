@@ -131,3 +131,26 @@ def test_decode_step_in_a_cuda_graph(bfp8, cuda_device, weights, arith):
         torch.cuda.synchronize()
         eager = _step(bfp8, dev, x.clone(), w, code)
         assert torch.equal(y.view(torch.int16), eager.view(torch.int16)), seed
+
+
+@pytest.mark.parametrize("arith", ["w8a16", "w8a8"])
+def test_decode_step_on_a_dirty_workspace(bfp8, cuda_device, weights, arith):
+    """The step zeroes the GEMVs' split-tile counters itself (the token split
+    for W8A16, each 1x128 quantizer for W8A8): a workspace full of stale bytes
+    gives the bytes of a zeroed one, and y is fully written."""
+    dev = cuda_device
+    _, w = weights
+    code = bfp8.BFP8_DECODE_W8A8 if arith == "w8a8" else bfp8.BFP8_DECODE_W8A16
+    M = 4
+    x = to_dev_bf16(bits16(synth.decode_tokens(404, M, H)), dev)
+    n_ws = bfp8.bfp8_decode_ffn_workspace(M, H, I, code)
+    clean = torch.zeros(n_ws, dtype=torch.uint8, device=dev)
+    dirty = torch.full((n_ws,), 0xA5, dtype=torch.uint8, device=dev)
+    y0 = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    y1 = torch.full((M, H), float("nan"), dtype=torch.bfloat16, device=dev)
+    bfp8.bfp8_decode_ffn(x, *w, y0, clean, arith=code)
+    bfp8.bfp8_decode_ffn(x, *w, y1, dirty, arith=code)
+    torch.cuda.synchronize()
+    assert bfp8.bfp8_device_status() == 0
+    assert not torch.isnan(y1).any()
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))

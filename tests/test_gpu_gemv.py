@@ -147,3 +147,35 @@ def test_gemv_w8a8_decode_workload(bfp8, cuda_device, which, M, outlier):
     cols = sample_indices(N, 1500, seed=M + 7)
     assert_close(gpu_bf16_to_f64(y)[:, cols], L.linear_w8a8(qa, sa, q, s, members, cols=cols),
                  f"decode w8a8 {which} M={M}")
+
+
+@pytest.mark.parametrize("arm", ["w8a16", "w8a8"])
+def test_gemv_on_a_dirty_workspace(bfp8, cuda_device, arm):
+    """Each call zeroes its split-tile counters before the GEMV counts on them
+    (the token split, or the W8A8 arm's clearing kernel): a workspace full of
+    stale bytes gives the bytes of a zeroed one. At [1000, 2048] every
+    128-row tile is split over 16 CTAs, so every output goes through a
+    counter."""
+    dev = cuda_device
+    M, N, K = 5, 1000, 2048
+    g = synth.generator(77)
+    q, s = quantize_members(synth.weight_f32(g, N, K).numpy(), None)
+    xb = bits16(synth.activations_bf16(g, M, K))
+    w, sw = to_dev_u8(q, dev), scale_to_dev(s, dev)
+    n_ws = bfp8.bfp8_gemv_decode_workspace(M, N, K)
+    ys = []
+    for fill in (0x00, 0xA5):
+        ws = torch.full((n_ws,), fill, dtype=torch.uint8, device=dev)
+        y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=dev)
+        if arm == "w8a16":
+            bfp8.bfp8_gemv_decode(to_dev_bf16(xb, dev), w, sw, y, ws)
+        else:
+            from oracle import quant as Q
+            qa, sa = Q.act_quant_group(xb)
+            bfp8.bfp8_gemv_decode_w8a8(to_dev_u8(qa, dev), torch.from_numpy(sa).to(dev), w, sw,
+                                       y, ws)
+        torch.cuda.synchronize()
+        assert bfp8.bfp8_device_status() == 0
+        assert not torch.isnan(y).any()
+        ys.append(y)
+    assert torch.equal(ys[0].view(torch.int16), ys[1].view(torch.int16))
