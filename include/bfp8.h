@@ -306,7 +306,9 @@ size_t bfp8_gemv_decode_workspace(int64_t M, int64_t N, int64_t K);
  *   q_a    [M, K] E4M3 from bfp8_act_quant_group, row stride K bytes, 16-byte aligned
  *   s_a    float32 activation scales as bfp8_linear_w8a8
  *   other arguments, the workspace (bfp8_gemv_decode_workspace bytes) and
- *   requirements as bfp8_gemv_decode. One kernel launch.
+ *   requirements as bfp8_gemv_decode. Two kernel launches: a one-CTA kernel
+ *   that zeroes the workspace's tile counters, then the GEMV as its
+ *   programmatic dependent.
  */
 int bfp8_gemv_decode_w8a8(const void* q_a, const float* s_a, int64_t s_stride_m,
                           int64_t s_stride_kb, const void* w_e4m3, const void* w_scale,
@@ -332,7 +334,9 @@ enum bfp8_decode_arith { BFP8_DECODE_W8A16 = 0, BFP8_DECODE_W8A8 = 1 };
  *   formed inside the down GEMV's token split).
  * arith = BFP8_DECODE_W8A8: x is quantized as bfp8_act_quant_group, the
  *   gate/up GEMV is bfp8_gemv_decode_w8a8, h is quantized as
- *   bfp8_silu_mul_act_quant, and the down GEMV is bfp8_gemv_decode_w8a8.
+ *   bfp8_silu_mul_act_quant, and the down GEMV is bfp8_gemv_decode_w8a8
+ *   (4 launches: each quantizer also zeroes the tile counters of the GEMV
+ *   that follows it, in place of that GEMV's clearing kernel).
  * The result equals that sequence of entry points byte for byte.
  *   x_bf16     [M, H] BF16, row stride ldx (ldx % 8 == 0, 16-byte aligned)
  *   w_gate_up  [2I, H] E4M3, gate rows over up rows; s_gate_up its
