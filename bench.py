@@ -657,7 +657,7 @@ def run_decode(bfp8, torch, dev, wgu, sgu, wdn, sdn, peaks):
 
 # --------------------------------------------------------------------------- single-launch mode
 PROFILE_CASES = ("act_quant", "gate_up", "gate_up_silu_quant", "silu_quant", "down",
-                 "moe_gate_up_silu_quant", "gemv_gate_up", "gemv_down", "decode_step",
+                 "moe_gate_up_silu_quant", "gemv_gate_up", "gemv_down", "decode_step", "decode_step_w8a8",
                  "qkv", "o_proj", "moe_gate_up", "moe_down", "w8a16_gate_up",
                  "moe_gather_quant", "moe_combine", "moe_layer")
 
@@ -764,14 +764,16 @@ def setup_case(case, bfp8, torch, dev, gen, decode_m=16, l2_ring=0):
         ws = torch.empty(bfp8.bfp8_gemv_decode_workspace(M, N, K), dtype=torch.uint8, device=dev)
         return (lambda: bfp8.bfp8_gemv_decode(x, w, sw, y, ws, member_rows=members)), \
             N * K + sw.numel() * 2 + 2 * M * K + 2 * M * N, "GB/s", "hbm"
-    if case == "decode_step":
+    if case in ("decode_step", "decode_step_w8a8"):
         M = decode_m
+        arith = bfp8.BFP8_DECODE_W8A8 if case == "decode_step_w8a8" else bfp8.BFP8_DECODE_W8A16
         wg, sg = qweight(2 * INTER, HID)
         wd, sd = qweight(HID, INTER)
         x = synth.decode_tokens(2, M, HID).to(dev)
         y = torch.empty(M, HID, dtype=torch.bfloat16, device=dev)
-        ws = torch.empty(bfp8.bfp8_decode_ffn_workspace(M, HID, INTER), dtype=torch.uint8, device=dev)
-        return (lambda: bfp8.bfp8_decode_ffn(x, wg, sg, wd, sd, y, ws)), \
+        ws = torch.empty(bfp8.bfp8_decode_ffn_workspace(M, HID, INTER, arith), dtype=torch.uint8,
+                         device=dev)
+        return (lambda: bfp8.bfp8_decode_ffn(x, wg, sg, wd, sd, y, ws, arith=arith)), \
             wg.numel() + wd.numel() + 2 * (sg.numel() + sd.numel()) + 2 * M * HID * 2, "GB/s", "hbm"
     if case in ("qkv", "o_proj"):
         c = synth.ATTENTION_PROJ
