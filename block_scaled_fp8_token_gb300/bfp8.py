@@ -565,8 +565,15 @@ def bfp8_decode_ffn(x, w_gate_up, s_gate_up, w_down, s_down, y, workspace,
     _layout(w_down, "w_down", (H, I))
     _grid_span(s_down, "s_down", Hb, Ib)
     _out(y, "y", M, H, 2)
+    # the library takes one scale dtype code for both grids
+    sdt = _scale_dtype(s_gate_up)
+    if _scale_dtype(s_down) != sdt:
+        raise ValueError("bfp8: s_gate_up and s_down must have the same dtype and kind (both "
+                         "block grids or both one multiplier): the call reads both with one "
+                         f"scale dtype, got {s_gate_up.dtype} rank {s_gate_up.dim()} and "
+                         f"{s_down.dtype} rank {s_down.dim()}")
     _check(_lib.bfp8_decode_ffn(arith, _ptr(x), x.stride(0), _ptr(w_gate_up), _ptr(s_gate_up),
-                                _ptr(w_down), _ptr(s_down), _scale_dtype(s_gate_up), M, H, I,
+                                _ptr(w_down), _ptr(s_down), sdt, M, H, I,
                                 _ptr(y), y.stride(0), *_ws(workspace),
                                 _stream(stream)),
            "bfp8_decode_ffn")

@@ -153,3 +153,20 @@ def test_layouts_the_library_would_misread_are_refused(bfp8):
                 torch.zeros(G, N, K, dtype=u8), torch.ones(G - 1, dtype=f32), off,
                 torch.zeros(T, N, dtype=bf16))                   # one multiplier per expert
 
+
+def test_decode_step_scales_must_share_one_dtype_and_kind(bfp8):
+    """bfp8_decode_ffn takes one scale dtype code for its two grids, so a
+    BF16 grid beside an F32 one, or a block grid beside one multiplier, would
+    be misread (a one-element tensor read as a grid, past its end)."""
+    Hh, Ii = 256, 384
+    x = torch.zeros(2, Hh, dtype=bf16)
+    wgu, wd = torch.zeros(2 * Ii, Hh, dtype=u8), torch.zeros(Hh, Ii, dtype=u8)
+    y, ws = torch.zeros(2, Hh, dtype=bf16), torch.zeros(1 << 16, dtype=u8)
+    for sgu, sd in ((torch.zeros(6, 2, dtype=bf16), torch.zeros(2, 3, dtype=f32)),
+                    (torch.zeros(6, 2, dtype=bf16), torch.ones((), dtype=bf16)),
+                    (torch.ones((), dtype=f32), torch.zeros(2, 3, dtype=f32))):
+        with pytest.raises(ValueError, match="same dtype and kind"):
+            bfp8.bfp8_decode_ffn(x, wgu, sgu, wd, sd, y, ws)
+    for sgu, sd in ((torch.ones((), dtype=f32), torch.ones((), dtype=f32)),
+                    (torch.zeros(6, 2, dtype=f32), torch.zeros(2, 3, dtype=f32))):
+        _device_error(bfp8.bfp8_decode_ffn, x, wgu, sgu, wd, sd, y, ws)

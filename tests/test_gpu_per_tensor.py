@@ -131,6 +131,34 @@ def test_decode_gemv_both_arms(bfp8, cuda_device, M):
                  L.linear_w8a8(qa, sa, q, grid, members, cols=cols), "gemv w8a8 per-tensor")
 
 
+@pytest.mark.parametrize("sd", ["f32", "bf16"])
+def test_decode_step_with_one_multiplier_per_weight(bfp8, cuda_device, sd):
+    """The dense-FFN decode step with a per-tensor multiplier for each of its
+    two weights gives the bytes of the same step on the expanded grids, in
+    both arithmetics."""
+    dev = cuda_device
+    M, H, I = 5, 1024, 1536
+    g = synth.generator(65)
+    qgu, sgu = Q.quantize_weight_tensor(synth.weight_f32(g, 2 * I, H).numpy(), sd)
+    qd, sdn = Q.quantize_weight_tensor(synth.weight_f32(g, H, I).numpy(), sd)
+    ggu = Q.tensor_scale_grid(sgu, 2 * I, H, [I, I])
+    gd = Q.tensor_scale_grid(sdn, H, I)
+    x = to_dev_bf16(bits16(synth.decode_tokens(75, M, H)), dev)
+    wgu, wd = to_dev_u8(qgu, dev), to_dev_u8(qd, dev)
+    for arith in (bfp8.BFP8_DECODE_W8A16, bfp8.BFP8_DECODE_W8A8):
+        ys = []
+        for scales in ((_scalar_dev(sgu, dev), _scalar_dev(sdn, dev)),
+                       (scale_to_dev(ggu, dev), scale_to_dev(gd, dev))):
+            ws = torch.empty(bfp8.bfp8_decode_ffn_workspace(M, H, I, arith), dtype=torch.uint8,
+                             device=dev)
+            y = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+            bfp8.bfp8_decode_ffn(x, wgu, scales[0], wd, scales[1], y, ws, arith=arith)
+            torch.cuda.synchronize()
+            assert bfp8.bfp8_device_status() == 0
+            ys.append(y)
+        assert _same(ys[0], ys[1]), arith
+
+
 def test_library_refuses_a_per_tensor_flag_on_an_unknown_dtype(bfp8, cuda_device):
     dev = cuda_device
     x = torch.zeros(4, 128, dtype=torch.bfloat16, device=dev)
