@@ -207,6 +207,7 @@ def bfp8_act_quant_group(x, q, scales, s_stride_m=None, s_stride_kb=None, stream
     M, K = x.shape
     ssm = scales.stride(0) if s_stride_m is None else s_stride_m
     sskb = scales.stride(1) if s_stride_kb is None else s_stride_kb
+    _dtypes(x=(x, "bf16"), q=(q, "e4m3"), scales=(scales, "f32"))
     _rows(x, "x")
     _span(x, "x", M, K, x.stride(0), 1, 2)
     _out(q, "q", M, K, 1)
@@ -221,6 +222,7 @@ def bfp8_silu_mul_act_quant(gu, q, scales, s_stride_m=None, s_stride_kb=None, st
     M, two_i = gu.shape
     ssm = scales.stride(0) if s_stride_m is None else s_stride_m
     sskb = scales.stride(1) if s_stride_kb is None else s_stride_kb
+    _dtypes(gu=(gu, "bf16"), q=(q, "e4m3"), scales=(scales, "f32"))
     _rows(gu, "gu")
     _span(gu, "gu", M, two_i, gu.stride(0), 1, 2)
     _out(q, "q", M, two_i // 2, 1)
@@ -234,6 +236,7 @@ def bfp8_silu_mul_act_quant(gu, q, scales, s_stride_m=None, s_stride_kb=None, st
 def bfp8_silu_mul(gu, h, stream=None) -> None:
     """h = bf16(silu(gate) * up) for gu = [gate | up] ([M, 2I] BF16); h [M, I] BF16."""
     M, two_i = gu.shape
+    _dtypes(gu=(gu, "bf16"), h=(h, "bf16"))
     _rows(gu, "gu")
     _span(gu, "gu", M, two_i, gu.stride(0), 1, 2)
     _out(h, "h", M, two_i // 2, 2)
@@ -244,6 +247,7 @@ def bfp8_silu_mul(gu, h, stream=None) -> None:
 
 def bfp8_quantize_weight_block(w, q, scale, stream=None) -> None:
     N, K = w.shape
+    _dtypes(w=(w, "f32"), q=(q, "e4m3"))
     _rows(w, "w")
     _span(w, "w", N, K, w.stride(0), 1, 4)  # float32, as the library reads it
     _out(q, "q", N, K, 1)
@@ -290,6 +294,22 @@ def _layout(t, name: str, shape, pitch: int | None = None) -> None:
         if shape[d] > 1 and st != w:
             raise ValueError(f"bfp8: {name} has strides {list(t.stride())}; the library reads it "
                              f"as row-major with strides {want}")
+
+
+_KINDS = {"bf16": (torch.bfloat16,), "e4m3": (torch.uint8, torch.float8_e4m3fn),
+          "f32": (torch.float32,), "i32": (torch.int32,)}
+
+
+def _dtypes(**args) -> None:
+    """Each tensor must hold the element type the library reads or writes at
+    that argument (name=(tensor, kind)): a tensor of another type would be
+    reinterpreted byte for byte. E4M3 data may be uint8 or float8_e4m3fn."""
+    for name, (t, kind) in args.items():
+        if t is None or isinstance(t, int):
+            continue
+        if t.dtype not in _KINDS[kind]:
+            allowed = " or ".join(str(d) for d in _KINDS[kind])
+            raise ValueError(f"bfp8: {name} must be {allowed}, got {t.dtype}")
 
 
 def _rows(t, name: str) -> None:
@@ -370,6 +390,7 @@ def bfp8_linear_w8a8(q_a, s_a, w, w_scale, y, member_rows=None, s_stride_m=None,
     ssm = s_a.stride(0) if s_stride_m is None else s_stride_m
     sskb = s_a.stride(1) if s_stride_kb is None else s_stride_kb
     Kb = -(-K // 128)
+    _dtypes(q_a=(q_a, "e4m3"), s_a=(s_a, "f32"), w=(w, "e4m3"), y=(y, "bf16"))
     _layout(q_a, "q_a", (M, K))
     _span(s_a, "s_a", M, Kb, ssm, sskb, 4)
     _layout(w, "w", (N, K))
@@ -386,6 +407,7 @@ def bfp8_linear_w8a8(q_a, s_a, w, w_scale, y, member_rows=None, s_stride_m=None,
 def bfp8_linear_w8a16(x, w, w_scale, y, member_rows=None, stream=None) -> None:
     M, K = x.shape
     N = w.shape[0]
+    _dtypes(x=(x, "bf16"), w=(w, "e4m3"), y=(y, "bf16"))
     _rows(x, "x")
     _span(x, "x", M, K, x.stride(0), 1, 2)
     _layout(w, "w", (N, K))
@@ -405,6 +427,7 @@ def bfp8_gemv_decode_workspace(M: int, N: int, K: int) -> int:
 def bfp8_gemv_decode(x, w, w_scale, y, workspace, member_rows=None, stream=None) -> None:
     M, K = x.shape
     N = w.shape[0]
+    _dtypes(x=(x, "bf16"), w=(w, "e4m3"), y=(y, "bf16"))
     _rows(x, "x")
     _span(x, "x", M, K, x.stride(0), 1, 2)
     _layout(w, "w", (N, K))
@@ -426,6 +449,7 @@ def bfp8_gemv_decode_w8a8(q_a, s_a, w, w_scale, y, workspace, member_rows=None, 
     ssm = s_a.stride(0) if s_stride_m is None else s_stride_m
     sskb = s_a.stride(1) if s_stride_kb is None else s_stride_kb
     Kb = -(-K // 128)
+    _dtypes(q_a=(q_a, "e4m3"), s_a=(s_a, "f32"), w=(w, "e4m3"), y=(y, "bf16"))
     _layout(q_a, "q_a", (M, K))
     _span(s_a, "s_a", M, Kb, ssm, sskb, 4)
     _layout(w, "w", (N, K))
@@ -445,6 +469,7 @@ def bfp8_gemv_decode_noalloc(x, w, w_scale, y, member_rows=None, stream=None) ->
     allocate device memory; its scratch is a fixed array inside the library."""
     M, K = x.shape
     N = w.shape[0]
+    _dtypes(x=(x, "bf16"), w=(w, "e4m3"), y=(y, "bf16"))
     _rows(x, "x")
     _span(x, "x", M, K, x.stride(0), 1, 2)
     _layout(w, "w", (N, K))
@@ -468,6 +493,8 @@ def bfp8_grouped_linear(q_a, s_a, w, w_scale, offsets, y, s_stride_m=None, s_str
     ssm = s_a.stride(0) if s_stride_m is None else s_stride_m
     sskb = s_a.stride(1) if s_stride_kb is None else s_stride_kb
     Kb = -(-K // 128)
+    _dtypes(q_a=(q_a, "e4m3"), s_a=(s_a, "f32"), w=(w, "e4m3"), offsets=(offsets, "i32"),
+            y=(y, "bf16"))
     _layout(q_a, "q_a", (T, K))
     _span(s_a, "s_a", T, Kb, ssm, sskb, 4)
     _layout(w, "w", (G, N, K))
@@ -497,6 +524,8 @@ def bfp8_linear_w8a8_silu_quant(q_a, s_a, w, w_scale, q_h, s_h, s_stride_m=None,
     hsm = s_h.stride(0) if sh_stride_m is None else sh_stride_m
     hskb = s_h.stride(1) if sh_stride_kb is None else sh_stride_kb
     Kb = -(-K // 128)
+    _dtypes(q_a=(q_a, "e4m3"), s_a=(s_a, "f32"), w=(w, "e4m3"), q_h=(q_h, "e4m3"),
+            s_h=(s_h, "f32"))
     _layout(q_a, "q_a", (M, K))
     _span(s_a, "s_a", M, Kb, ssm, sskb, 4)
     _layout(w, "w", (2 * I, K))
@@ -528,6 +557,8 @@ def bfp8_grouped_linear_silu_quant(q_a, s_a, w, w_scale, offsets, q_h, s_h, s_st
     hsm = s_h.stride(0) if sh_stride_m is None else sh_stride_m
     hskb = s_h.stride(1) if sh_stride_kb is None else sh_stride_kb
     Kb = -(-K // 128)
+    _dtypes(q_a=(q_a, "e4m3"), s_a=(s_a, "f32"), w=(w, "e4m3"), offsets=(offsets, "i32"),
+            q_h=(q_h, "e4m3"), s_h=(s_h, "f32"))
     _layout(q_a, "q_a", (T, K))
     _span(s_a, "s_a", T, Kb, ssm, sskb, 4)
     _layout(w, "w", (G, 2 * I, K))
@@ -558,6 +589,8 @@ def bfp8_decode_ffn(x, w_gate_up, s_gate_up, w_down, s_down, y, workspace,
     M, H = x.shape
     I = w_down.shape[1]
     Hb, Ib = -(-H // 128), -(-I // 128)
+    _dtypes(x=(x, "bf16"), w_gate_up=(w_gate_up, "e4m3"), w_down=(w_down, "e4m3"),
+            y=(y, "bf16"))
     _rows(x, "x")
     _span(x, "x", M, H, x.stride(0), 1, 2)
     _layout(w_gate_up, "w_gate_up", (2 * I, H))
@@ -586,6 +619,7 @@ def bfp8_moe_gather_act_quant(x, row_token, q, scales, s_stride_m=None, s_stride
     R = row_token.shape[0]
     ssm = scales.stride(0) if s_stride_m is None else s_stride_m
     sskb = scales.stride(1) if s_stride_kb is None else s_stride_kb
+    _dtypes(x=(x, "bf16"), row_token=(row_token, "i32"), q=(q, "e4m3"), scales=(scales, "f32"))
     _rows(x, "x")
     _span(x, "x", T, H, x.stride(0), 1, 2)
     _layout(row_token, "row_token", (R,))
@@ -601,6 +635,8 @@ def bfp8_moe_combine(y, token_rows, token_weights, out, stream=None) -> None:
     """out[t] = bf16(sum_j token_weights[t, j] * y[token_rows[t, j]]), slot order j."""
     R, H = y.shape
     T, topk = token_rows.shape
+    _dtypes(y=(y, "bf16"), token_rows=(token_rows, "i32"), token_weights=(token_weights, "f32"),
+            out=(out, "bf16"))
     _rows(y, "y")
     _span(y, "y", R, H, y.stride(0), 1, 2)
     _layout(token_rows, "token_rows", (T, topk))

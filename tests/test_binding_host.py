@@ -105,8 +105,6 @@ def test_tensors_too_small_for_the_call_are_refused(bfp8):
     _too_small(bfp8.bfp8_linear_w8a8, q, s, w, torch.zeros(Nb, Kb, dtype=bf16), y[: M - 1])
     _bad_layout(bfp8.bfp8_linear_w8a8, q, s, w, torch.zeros(3, Kb, dtype=bf16), y,
                 member_rows=[200, 184])                               # needs 4 grid rows
-    _too_small(bfp8.bfp8_quantize_weight_block, torch.zeros(N, K, dtype=bf16),  # read as f32
-               torch.zeros(N, K, dtype=u8), torch.zeros(Nb, Kb, dtype=bf16))
     G, T = 4, 50
     off = torch.tensor([0, 10, 10, 30], dtype=i32)                     # needs G + 1 entries
     _bad_layout(bfp8.bfp8_grouped_linear, torch.zeros(T, K, dtype=u8), torch.zeros(T, Kb, dtype=f32),
@@ -170,3 +168,37 @@ def test_decode_step_scales_must_share_one_dtype_and_kind(bfp8):
     for sgu, sd in ((torch.ones((), dtype=f32), torch.ones((), dtype=f32)),
                     (torch.zeros(6, 2, dtype=f32), torch.zeros(2, 3, dtype=f32))):
         _device_error(bfp8.bfp8_decode_ffn, x, wgu, sgu, wd, sd, y, ws)
+
+
+def test_tensors_of_another_element_type_are_refused(bfp8):
+    """The library reads each argument as one element type; a tensor of another
+    type (a float32 activation, int64 offsets, a BF16 weight to quantize) would
+    be reinterpreted byte for byte, so the binding refuses it by dtype. E4M3
+    data is accepted as uint8 or float8_e4m3fn."""
+    x = torch.zeros(M, K, dtype=bf16)
+    q = torch.zeros(M, K, dtype=u8)
+    s = torch.zeros(M, Kb, dtype=f32)
+    w = torch.zeros(N, K, dtype=u8)
+    sw = torch.zeros(Nb, Kb, dtype=bf16)
+    y = torch.zeros(M, N, dtype=bf16)
+
+    def refused(fn, *args, **kw):
+        with pytest.raises(ValueError, match="must be torch"):
+            fn(*args, **kw)
+
+    refused(bfp8.bfp8_act_quant_group, x.float(), q, s)
+    refused(bfp8.bfp8_act_quant_group, x, q, s.double())
+    refused(bfp8.bfp8_linear_w8a8, q, s, w, sw, y.float())
+    refused(bfp8.bfp8_linear_w8a8, q.to(torch.int8), s, w, sw, y)
+    refused(bfp8.bfp8_linear_w8a16, x.half(), w, sw, y)
+    refused(bfp8.bfp8_quantize_weight_block, torch.zeros(N, K, dtype=bf16), w, sw)
+    G, T = 4, 50
+    refused(bfp8.bfp8_grouped_linear, torch.zeros(T, K, dtype=u8), torch.zeros(T, Kb, dtype=f32),
+            torch.zeros(G, N, K, dtype=u8), torch.zeros(G, Nb, Kb, dtype=bf16),
+            torch.tensor([0, 10, 10, 30, 50]), torch.zeros(T, N, dtype=bf16))   # int64 offsets
+    refused(bfp8.bfp8_moe_combine, torch.zeros(12, 256, dtype=bf16),
+            torch.zeros(4, 3, dtype=i32), torch.zeros(4, 3, dtype=bf16),
+            torch.zeros(4, 256, dtype=bf16))
+    # float8_e4m3fn views of the same bytes pass the dtype check (and stop at the device check)
+    _device_error(bfp8.bfp8_linear_w8a8, q.view(torch.float8_e4m3fn), s,
+                  w.view(torch.float8_e4m3fn), sw, y)
