@@ -107,6 +107,61 @@ def test_w8a8_stream_k_deterministic(bfp8, cuda_device):
     assert_close(gpu_bf16_to_f64(ys[0]), L.linear_w8a8(qa, sa, q, s), "stream-K")
 
 
+def test_stream_k_workspaces_full_of_stale_bytes(bfp8, cuda_device):
+    """Every call clears its stream-K tile counters on its stream before the
+    kernel runs, and each partial tile is written before it is read, so a
+    workspace full of stale bytes gives the bytes of a zeroed one: the dense
+    projection, the fused gate/up and the per-expert projection, each at a
+    size whose tail wave is split."""
+    dev = cuda_device
+    xb, q, s = _problem(78, 300, 1024, 4096)
+    qa, sa = Q.act_quant_group(xb)
+    a, sad = to_dev_u8(qa, dev), torch.from_numpy(sa).to(dev)
+    w, swd = to_dev_u8(q, dev), scale_to_dev(s, dev)
+    I = 512                                                # fused: [gate; up] = the first 1024 rows
+
+    def dense(ws):
+        y = torch.full((300, 1024), float("nan"), dtype=torch.bfloat16, device=dev)
+        bfp8.bfp8_linear_w8a8(a, sad, w, swd, y, workspace=ws)
+        return [y.view(torch.int16)]
+
+    def fused(ws):
+        qh = torch.full((300, I), 0xAA, dtype=torch.uint8, device=dev)
+        sh = torch.full((300, I // 128), -1.0, dtype=torch.float32, device=dev)
+        bfp8.bfp8_linear_w8a8_silu_quant(a, sad, w, swd, qh, sh, workspace=ws)
+        return [qh, sh.view(torch.int32)]
+
+    G, T = 3, 300
+    off = torch.tensor([0, 7, 7, T], dtype=torch.int32, device=dev)
+    wg = w[:768].reshape(1, 768, 4096).expand(G, 768, 4096).contiguous()
+    sg = swd[:6].reshape(1, 6, 32).expand(G, 6, 32).contiguous()
+
+    def grouped(ws):
+        y = torch.full((T, 768), float("nan"), dtype=torch.bfloat16, device=dev)
+        bfp8.bfp8_grouped_linear(a, sad, wg, sg, off, y, workspace=ws)
+        return [y.view(torch.int16)]
+
+    for name, call, n_ws in (
+            ("dense", dense, bfp8.bfp8_linear_w8a8_workspace(300, 1024, 4096)),
+            ("fused", fused, bfp8.bfp8_linear_w8a8_silu_quant_workspace(300, I, 4096)),
+            ("grouped", grouped, bfp8.bfp8_grouped_linear_workspace(T, G, 768, 4096))):
+        assert n_ws > 0, name
+        outs = []
+        for fill in (0x00, 0xA5):
+            outs.append(call(torch.full((n_ws,), fill, dtype=torch.uint8, device=dev)))
+        torch.cuda.synchronize()
+        assert bfp8.bfp8_device_status() == 0
+        for u, v in zip(*outs):
+            assert torch.equal(u, v), name
+    ref = L.linear_w8a8(qa, sa, q, s)
+    y = torch.empty(300, 1024, dtype=torch.bfloat16, device=dev)
+    bfp8.bfp8_linear_w8a8(a, sad, w, swd, y,
+                          workspace=torch.full((bfp8.bfp8_linear_w8a8_workspace(300, 1024, 4096),),
+                                               0xA5, dtype=torch.uint8, device=dev))
+    torch.cuda.synchronize()
+    assert_close(gpu_bf16_to_f64(y), ref, "stream-K on a stale workspace")
+
+
 def test_w8a8_mn_major_scales_and_padded_output(bfp8, cuda_device):
     xb, q, s = _problem(5, 150, 320, 512)
     qa, sa = Q.act_quant_group(xb)
