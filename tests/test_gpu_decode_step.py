@@ -154,3 +154,28 @@ def test_decode_step_on_a_dirty_workspace(bfp8, cuda_device, weights, arith):
     assert bfp8.bfp8_device_status() == 0
     assert not torch.isnan(y1).any()
     assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+
+
+@pytest.mark.parametrize("arith", ["w8a16", "w8a8"])
+def test_decode_steps_on_two_streams_at_once(bfp8, cuda_device, weights, arith):
+    """Two steps in flight at once on two streams, each with its own
+    workspace, give the bytes of the same steps run one after the other: the
+    calls share no device state but their arguments."""
+    dev = cuda_device
+    _, w = weights
+    code = bfp8.BFP8_DECODE_W8A8 if arith == "w8a8" else bfp8.BFP8_DECODE_W8A16
+    M = 16
+    xs = [to_dev_bf16(bits16(synth.decode_tokens(seed, M, H)), dev) for seed in (405, 406)]
+    want = [_step(bfp8, dev, x, w, code) for x in xs]
+    n_ws = bfp8.bfp8_decode_ffn_workspace(M, H, I, code)
+    streams = [torch.cuda.Stream(device=dev) for _ in xs]
+    wss = [torch.empty(n_ws, dtype=torch.uint8, device=dev) for _ in xs]
+    ys = [torch.empty(M, H, dtype=torch.bfloat16, device=dev) for _ in xs]
+    torch.cuda.synchronize()
+    for _ in range(4):
+        for x, s, ws, y in zip(xs, streams, wss, ys):
+            bfp8.bfp8_decode_ffn(x, *w, y, ws, arith=code, stream=s)
+    torch.cuda.synchronize()
+    assert bfp8.bfp8_device_status() == 0
+    for y, ref in zip(ys, want):
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
