@@ -134,3 +134,33 @@ def test_grouped_strided_output_keeps_padding(bfp8, cuda_device, pad):
     assert bfp8.bfp8_device_status() == 0
     assert torch.isnan(yb[:, N:].float()).all()
     assert_close(gpu_bf16_to_f64(y), L.grouped_linear_w8a8(qa, sa, qw, sw, offsets), f"grouped pad {pad}")
+
+
+def test_grouped_on_two_streams_at_once(bfp8, cuda_device):
+    """Two per-expert projections with different offset tables in flight at
+    once on two streams, each with its own stream-K workspace, give the bytes
+    of the same calls run one after the other (each CTA builds its tile
+    schedule from its own call's table)."""
+    dev = cuda_device
+    G, N, K = 6, 384, 256
+    tables = ([0, 3, 3, 200, 330, 331, 331], [0, 0, 129, 129, 129, 250, 331])
+    g = synth.generator(42)
+    qw, sw = _stack_quant(synth.weight_stack_f32(g, G, N, K).numpy())
+    xb = bits16(synth.activations_bf16(g, 331, K, outlier="entries", frac=0.01, factor=20.0))
+    qa, sa = Q.act_quant_group(xb)
+    want = [_grouped(bfp8, dev, qa, sa, qw, sw, t) for t in tables]
+    a, sad = to_dev_u8(qa, dev), torch.from_numpy(sa).to(dev)
+    w, swd = to_dev_u8(qw, dev), scale_to_dev(sw, dev)
+    offs = [torch.tensor(t, dtype=torch.int32, device=dev) for t in tables]
+    wss = [torch.empty(bfp8.bfp8_grouped_linear_workspace(331, G, N, K), dtype=torch.uint8,
+                       device=dev) for _ in tables]
+    ys = [torch.empty(331, N, dtype=torch.bfloat16, device=dev) for _ in tables]
+    streams = [torch.cuda.Stream(device=dev) for _ in tables]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for off, ws, y, s in zip(offs, wss, ys, streams):
+            bfp8.bfp8_grouped_linear(a, sad, w, swd, off, y, workspace=ws, stream=s)
+    torch.cuda.synchronize()
+    assert bfp8.bfp8_device_status() == 0
+    for y, ref in zip(ys, want):
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
